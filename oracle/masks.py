@@ -1,0 +1,206 @@
+"""Oracle: dense visibility masks, canonical Interval Tables and Tile-State Bitmaps.
+
+Test infrastructure only (see the package header).
+
+What the paper fixes (CompileMask, sections 2.1, 3.3.1, 3.3.2):
+  * visibility is a property of each (query row i, key column j) pair; the mask boundaries come
+    from per-batch metadata (sequence lengths, segment boundaries), section 1 / 2.2;
+  * the Execution Descriptor holds, per row, the visible key intervals, padded with zero-length
+    intervals up to the count the compiler derived (section 3.3.1);
+  * it also holds two bits per tile telling whether the tile is empty, full or partial
+    (section 3.3.1), which is the classification tiled attention needs (section 2.1);
+  * forward and backward traversals get their own descriptors (section 3.2.2 / 3.3): the backward
+    one lists, per key column, the visible query intervals.
+
+Readings taken where the pages are silent (each is listed in the design notes):
+  * an interval is stored as (start, end), half open; an empty or padding interval is (0, 0);
+  * tile codes 0 = empty, 1 = partial, 2 = full, packed 16 tiles per uint32, tile t of a row at
+    bits 2*(t % 16) of word t // 16;
+  * slot order within a row is the order in which the rule names the intervals;
+  * workload 5: prefix rows are causal over the prefix; the "previous document" of the first
+    document is empty, and the prefix is not a document.
+
+Segment conventions: seg_row[k] is the first position of segment k, seg_row[nseg] = S.
+  workload 3: segment 0 is the prompt (P = seg_row[1]), segments 1..4 the responses;
+  workload 4: segment 0 is the history (h = seg_row[1]), segment 1 the candidates;
+  workload 5: segment 0 is the system prefix (b = seg_row[1]), segments 1.. the documents.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+PREV_DOC_HEAD = 64  # workload 5: tokens of the previous document that stay visible
+
+
+def num_intervals(wid: int) -> tuple[int, int]:
+    """Forward / backward interval counts of each workload's rule (max over its regions)."""
+    return {1: (1, 1), 2: (1, 1), 3: (2, 1), 4: (2, 1), 5: (3, 2)}[wid]
+
+
+def segment_index(seg_row: np.ndarray, nseg: int, pos: np.ndarray) -> np.ndarray:
+    """Index k of the segment holding each position: seg_row[k] <= pos < seg_row[k+1]."""
+    bounds = np.asarray(seg_row[: nseg + 1], dtype=np.int64)
+    return np.searchsorted(bounds, pos, side="right") - 1
+
+
+# ------------------------------------------------------------------------------------------------
+# dense masks: the visibility rule of each workload, written directly as a predicate on (i, j)
+# ------------------------------------------------------------------------------------------------
+def dense_mask(wid: int, seg_row: np.ndarray, nseg: int, S: int,
+               rows: np.ndarray | None = None, cols: np.ndarray | None = None) -> np.ndarray:
+    """bool [len(rows), len(cols)]: True where query row i may attend to key column j."""
+    i = (np.arange(S) if rows is None else np.asarray(rows)).astype(np.int64)[:, None]
+    j = (np.arange(S) if cols is None else np.asarray(cols)).astype(np.int64)[None, :]
+    seg = np.asarray(seg_row, dtype=np.int64)
+    ki = segment_index(seg, nseg, i)          # segment of the query row
+    start_i = seg[ki]                         # first position of that segment
+    if wid == 1:   # packed documents: row i sees [doc_start(i), i + 1)
+        return (j >= start_i) & (j <= i)
+    if wid == 2:   # causal: row i sees [0, i + 1)
+        return np.broadcast_to(j <= i, (i.shape[0], j.shape[1])).copy()
+    if wid == 3:   # prompt rows causal; a response row sees [0, P) and [resp_start(i), i + 1)
+        P = seg[1]
+        prompt = (i < P) & (j <= i)
+        response = (i >= P) & ((j < P) | ((j >= start_i) & (j <= i)))
+        return prompt | response
+    if wid == 4:   # history rows causal; candidate row i sees [0, h) and [i, i + 1)
+        h = seg[1]
+        history = (i < h) & (j <= i)
+        candidate = (i >= h) & ((j < h) | (j == i))
+        return history | candidate
+    if wid == 5:   # prefix causal; document row sees [0, b), head of previous doc, own doc causal
+        b = seg[1]
+        prefix = (i < b) & (j <= i)
+        prev = np.maximum(ki - 1, 0)
+        prev_start = seg[prev]
+        prev_len = seg[np.minimum(prev + 1, nseg)] - prev_start
+        head_end = prev_start + np.minimum(PREV_DOC_HEAD, prev_len)
+        has_prev_doc = ki >= 2
+        doc = (i >= b) & ((j < b)
+                          | (has_prev_doc & (j >= prev_start) & (j < head_end))
+                          | ((j >= start_i) & (j <= i)))
+        return prefix | doc
+    raise ValueError(wid)
+
+
+# ------------------------------------------------------------------------------------------------
+# canonical Interval Tables (closed form per region, in the rule's slot order)
+# ------------------------------------------------------------------------------------------------
+def _slot(lo: int, hi: int, S: int) -> tuple[int, int]:
+    lo = min(max(lo, 0), S)
+    hi = min(max(hi, 0), S)
+    return (lo, hi) if hi > lo else (0, 0)
+
+
+def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.ndarray:
+    """int32 [NI_f, S, 2]: the visible key intervals of every query row."""
+    ni, _ = num_intervals(wid)
+    out = np.zeros((ni, S, 2), dtype=np.int32)
+    seg = [int(x) for x in seg_row[: nseg + 1]]
+    for i in range(S):
+        k = int(segment_index(np.asarray(seg), nseg, np.array([i]))[0])
+        if wid == 1:
+            slots = [(seg[k], i + 1)]
+        elif wid == 2:
+            slots = [(0, i + 1)]
+        elif wid == 3:
+            slots = [(0, i + 1)] if k == 0 else [(0, seg[1]), (seg[k], i + 1)]
+        elif wid == 4:
+            slots = [(0, i + 1)] if k == 0 else [(0, seg[1]), (i, i + 1)]
+        elif wid == 5:
+            if k == 0:
+                slots = [(0, i + 1)]
+            elif k == 1:
+                slots = [(0, seg[1]), (0, 0), (seg[k], i + 1)]
+            else:
+                ps, pe = seg[k - 1], seg[k]
+                slots = [(0, seg[1]), (ps, min(ps + PREV_DOC_HEAD, pe)), (seg[k], i + 1)]
+        else:
+            raise ValueError(wid)
+        for n, (lo, hi) in enumerate(slots):
+            out[n, i] = _slot(lo, hi, S)
+    return out
+
+
+def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.ndarray:
+    """int32 [NI_b, S, 2]: for every key column j, the query rows that see it."""
+    _, ni = num_intervals(wid)
+    out = np.zeros((ni, S, 2), dtype=np.int32)
+    seg = [int(x) for x in seg_row[: nseg + 1]]
+    for j in range(S):
+        k = int(segment_index(np.asarray(seg), nseg, np.array([j]))[0])
+        end_k = seg[k + 1]
+        if wid == 1:
+            slots = [(j, end_k)]
+        elif wid == 2:
+            slots = [(j, S)]
+        elif wid == 3:
+            slots = [(j, S)] if k == 0 else [(j, end_k)]
+        elif wid == 4:
+            slots = [(j, S)] if k == 0 else [(j, j + 1)]
+        elif wid == 5:
+            if k == 0:
+                slots = [(j, S)]
+            else:
+                nxt = (0, 0)
+                if j < seg[k] + PREV_DOC_HEAD and k + 1 < nseg:
+                    nxt = (seg[k + 1], seg[k + 2])
+                slots = [(j, end_k), nxt]
+        else:
+            raise ValueError(wid)
+        for n, (lo, hi) in enumerate(slots):
+            out[n, j] = _slot(lo, hi, S)
+    return out
+
+
+def intervals_to_mask(table: np.ndarray, S: int) -> np.ndarray:
+    """Dense bool [S, S] of the union of each row's intervals (row r, column c)."""
+    c = np.arange(S)[None, :]
+    m = np.zeros((table.shape[1], S), dtype=bool)
+    for n in range(table.shape[0]):
+        m |= (c >= table[n, :, 0:1]) & (c < table[n, :, 1:2])
+    return m
+
+
+# ------------------------------------------------------------------------------------------------
+# Tile-State Bitmaps
+# ------------------------------------------------------------------------------------------------
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+def tile_states_of(mask: np.ndarray, tile_r: int, tile_c: int) -> np.ndarray:
+    """uint8 [R/tile_r, C/tile_c]: 0 if no pair of the tile is visible, 2 if all are, else 1."""
+    R, C = mask.shape
+    assert R % tile_r == 0 and C % tile_c == 0
+    t = mask.reshape(R // tile_r, tile_r, C // tile_c, tile_c)
+    anyv = t.any(axis=(1, 3))
+    allv = t.all(axis=(1, 3))
+    return np.where(allv, FULL, np.where(anyv, PARTIAL, EMPTY)).astype(np.uint8)
+
+
+def tile_states(wid: int, seg_row: np.ndarray, nseg: int, S: int, tile: int = 128,
+                backward: bool = False) -> np.ndarray:
+    """Tile states of the forward mask, or of its transpose for the backward descriptor.
+
+    Built one tile-row at a time from the dense predicate so that 32K masks fit in memory.
+    """
+    nt = S // tile
+    out = np.zeros((nt, nt), dtype=np.uint8)
+    for t in range(nt):
+        span = np.arange(t * tile, (t + 1) * tile)
+        if backward:  # rows of the transposed mask = key columns of the forward mask
+            block = dense_mask(wid, seg_row, nseg, S, rows=None, cols=span).T
+        else:
+            block = dense_mask(wid, seg_row, nseg, S, rows=span, cols=None)
+        out[t] = tile_states_of(block, tile, tile)[0]
+    return out
+
+
+def pack_tile_states(codes: np.ndarray) -> np.ndarray:
+    """uint32 [R, ceil(C/16)]: 2 bits per tile, tile c at bits 2*(c % 16) of word c // 16."""
+    R, C = codes.shape
+    W = (C + 15) // 16
+    out = np.zeros((R, W), dtype=np.uint64)
+    for c in range(C):
+        out[:, c // 16] |= codes[:, c].astype(np.uint64) << np.uint64(2 * (c % 16))
+    return out.astype(np.uint32)
