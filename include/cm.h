@@ -1,0 +1,161 @@
+/*
+ * cm.h -- C ABI of the descriptor-guided masked attention library (libcm.so).
+ *
+ * The operations follow "CompileMask: Bridging the Gap Between Expressiveness and Efficiency in
+ * Attention Masking":
+ *   - section 3.2 (MaskSpec, Regions with a row guard and a visibility rule) and section 3.2.2
+ *     (symbolic lowering: AST, DNF normalisation, interval extraction, canonicalisation)
+ *       -> cm_compile_spec / cm_spec_* (offline, host only);
+ *   - section 3.3 and 3.3.1 (online preprocess kernel evaluating the compiled endpoints against
+ *     batch metadata; Execution Descriptor = Interval Table padded with zero-length intervals
+ *     plus 2-bit Tile-State Bitmaps; separate forward and backward descriptors)
+ *       -> cm_descriptor_sizes / cm_build_descriptor;
+ *   - section 3.3.2 (descriptor-guided attention: skip empty tiles, run full tiles unmasked,
+ *     check partial tiles against the endpoints with unsigned arithmetic, -inf before the
+ *     online softmax) and section 4.4 (unsigned visible-interval check)
+ *       -> cm_attn_fwd / cm_attn_bwd.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer named "device" must point to memory of the current CUDA device.  The library
+ *     allocates no device memory: the caller owns every buffer and must keep it alive until the
+ *     work queued on `stream` has finished.  The only heap object the library owns is the host
+ *     cm_spec returned by cm_compile_spec (free it with cm_spec_free).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work is queued on it and
+ *     the call returns without waiting; nothing runs on the CPU in place of a kernel.
+ *   - Return value: CM_OK (0) or a negative CM_ERR_* code.  Arguments are validated on the host
+ *     before anything is queued; a call that fails validation queues nothing.  Errors detected on
+ *     the device (bad segment metadata, a bounded wait that expired) are recorded in the
+ *     descriptor's status word and reported by cm_get_status.
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous, layout [B][H][S][d].  The LSE is
+ *     fp32 [B][H][S] in natural log.  Row i of a descriptor is a query row (forward) or a key
+ *     column (backward).
+ *   - Supported shapes: d in {64, 128}; S a positive multiple of 128; tile = 128.
+ */
+#ifndef CM_H_
+#define CM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CM_API __attribute__((visibility("default")))
+
+enum {
+  CM_OK = 0,
+  CM_ERR_PARSE = -1,        /* spec text does not parse or uses an unsupported form */
+  CM_ERR_INVALID_ARG = -2,  /* null pointer, bad size, descriptor/shape mismatch */
+  CM_ERR_UNSUPPORTED = -3,  /* valid request outside the supported shapes (d, S, tile, limits) */
+  CM_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+  CM_ERR_TIMEOUT = -5,      /* device status: a bounded wait inside a kernel expired */
+  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation */
+};
+
+/* Opaque compiled MaskSpec (host memory, owned by the caller after cm_compile_spec). */
+typedef struct cm_spec cm_spec;
+
+/* Per-batch metadata (section 1 / 2.2: sequence lengths and segment boundaries).
+ *   seg  device int32 [B][nseg_max + 1]: seg[b][0] = 0, strictly increasing up to
+ *        seg[b][nseg[b]] = S; entries after nseg[b] are ignored.
+ *   nseg device int32 [B]: segment count of each sample, 1 <= nseg[b] <= nseg_max. */
+typedef struct cm_meta {
+  const int32_t* seg;
+  const int32_t* nseg;
+  int32_t nseg_max;
+} cm_meta;
+
+/* Execution Descriptor (section 3.3.1), forward and backward halves.  All buffers are device
+ * memory allocated by the caller with the sizes from cm_descriptor_sizes.
+ *   itab_f  int32 [B][ni_f][S][2]  (start, end) of each visible key interval of query row i,
+ *           half open; unused slots and empty intervals are (0, 0)
+ *   bm_f    uint32 [B][S/tile][ceil((S/tile)/16)]  2 bits per (q-tile, k-tile):
+ *           0 empty, 1 partial, 2 full; k-tile t at bits 2*(t % 16) of word t / 16
+ *   itab_b  int32 [B][ni_b][S][2]  visible query intervals of key column j
+ *   bm_b    uint32 [B][S/tile][ceil((S/tile)/16)]  (k-tile, q-tile) states
+ *   sched_f int32 [B * S/tile]  forward work order: (b << 16 | q_tile), most tiles first
+ *   sched_b int32 [B * S/tile]  backward work order: (b << 16 | k_tile), most tiles first
+ *   status  int32 [1]           device error word, cleared by cm_build_descriptor */
+typedef struct cm_descriptor {
+  int32_t B, S, tile, ni_f, ni_b;
+  int32_t* itab_f;
+  uint32_t* bm_f;
+  int32_t* itab_b;
+  uint32_t* bm_b;
+  int32_t* sched_f;
+  int32_t* sched_b;
+  int32_t* status;
+} cm_descriptor;
+
+/* ---- offline compiler (host only; section 3.2.2) ------------------------------------------- */
+
+/* Parse and lower a MaskSpec.  Text: one Region per line,
+ *     region <guard> : <rule>
+ * <guard> is `all` or a boolean expression of the row index i; <rule> is a boolean expression
+ * over i and the other index j (&&, ||, !, comparisons < <= > >= == !=).  Integer terms: i, j,
+ * S, nseg, integer constants, + - and multiplication by a constant, min(a, b), max(a, b),
+ * seg_idx(e), seg_start(e), seg_end(e), seg_start_at(k), seg_end_at(k).  Lines starting with '#'
+ * are comments.  Regions are tried in order; the first whose guard holds applies to the row.
+ * On success *out receives a new cm_spec.  On CM_ERR_PARSE a message is written to err (if
+ * err_len > 0). */
+CM_API int cm_compile_spec(const char* text, cm_spec** out, char* err, size_t err_len);
+
+/* Free a spec from cm_compile_spec (NULL is ignored). */
+CM_API void cm_spec_free(cm_spec* spec);
+
+/* The compiler-derived interval count (max slots over the Regions), section 3.3.1. */
+CM_API int cm_spec_num_intervals(const cm_spec* spec, int* ni_max);
+
+/* Human-readable lowered form (Regions, slot endpoints, slot conditions) written to buf as a
+ * NUL-terminated string; *needed (if not NULL) receives the full length + 1.  Host only. */
+CM_API int cm_spec_describe(const cm_spec* spec, char* buf, size_t len, size_t* needed);
+
+/* ---- online descriptor construction (sections 3.3, 3.3.1) ---------------------------------- */
+
+/* Byte sizes of the descriptor buffers, in the order itab_f, bm_f, itab_b, bm_b, sched_f,
+ * sched_b, status.  tile must be 128. */
+CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, int S, int tile,
+                               size_t sizes[7]);
+
+/* Queue the preprocess kernels that evaluate both specs against `meta` and fill `desc`.
+ * desc->B, S, tile, ni_f, ni_b must match the specs and sizes; its pointers must be set.
+ * Clears desc->status first.  Asynchronous on `stream`. */
+CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_meta* meta,
+                               int B, int S, cm_descriptor* desc, void* stream);
+
+/* ---- descriptor-guided attention (section 3.3.2) -------------------------------------------- */
+
+/* Forward: o = softmax(scale * q k^T masked by desc) v; lse = natural-log row sums.
+ * q, k, v, o: device bf16 [B][H][S][d]; lse: device fp32 [B][H][S].  The mask is shared by
+ * all heads of a sample.  A row with no visible key gets o = 0 and lse = -inf. */
+CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
+                       void* o, float* lse, int B, int H, int S, int d, float scale,
+                       void* stream);
+
+/* Workspace bytes cm_attn_bwd needs (fp32 dQ accumulator and per-row D = rowsum(dO * O)). */
+CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes);
+
+/* Backward: dq, dk, dv (device bf16 [B][H][S][d]) of sum(o * dO) given the forward's o and lse.
+ * Uses the forward descriptor's itab_f/bm_f for nothing but validation and the backward half
+ * (itab_b, bm_b, sched_b) to traverse key tiles.  `workspace` (device, >= the size above,
+ * 16-byte aligned) is overwritten. */
+CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
+                       const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
+                       int d, float scale, void* stream);
+
+/* ---- status --------------------------------------------------------------------------------- */
+
+/* Wait for `stream`, then read desc->status: CM_OK, CM_ERR_TIMEOUT or CM_ERR_DEVICE_CHECK
+ * (CM_ERR_CUDA if the wait or copy itself failed). */
+CM_API int cm_get_status(const cm_descriptor* desc, void* stream);
+
+/* Static description of a CM_* code. */
+CM_API const char* cm_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CM_H_ */

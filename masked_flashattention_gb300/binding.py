@@ -1,0 +1,267 @@
+"""Thin ctypes binding of libcm.so, with the same names as the C ABI (include/cm.h).
+
+Argument marshalling only: every step of the hot path runs in the library's CUDA kernels.
+PyTorch supplies device memory (tensor data pointers) and streams; nothing here computes a
+descriptor or an attention value, and there is no fallback when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcm.so")
+
+CM_OK = 0
+CM_ERR_PARSE = -1
+CM_ERR_INVALID_ARG = -2
+CM_ERR_UNSUPPORTED = -3
+CM_ERR_CUDA = -4
+CM_ERR_TIMEOUT = -5
+CM_ERR_DEVICE_CHECK = -6
+
+TILE = 128
+
+
+class CMError(RuntimeError):
+    def __init__(self, code: int, what: str, detail: str = ""):
+        self.code = code
+        msg = f"{what}: {cm_error_string(code)} ({code})"
+        super().__init__(msg + (f": {detail}" if detail else ""))
+
+
+class cm_meta(ctypes.Structure):
+    _fields_ = [("seg", ctypes.c_void_p), ("nseg", ctypes.c_void_p), ("nseg_max", ctypes.c_int32)]
+
+
+class cm_descriptor(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("tile", ctypes.c_int32),
+                ("ni_f", ctypes.c_int32), ("ni_b", ctypes.c_int32),
+                ("itab_f", ctypes.c_void_p), ("bm_f", ctypes.c_void_p),
+                ("itab_b", ctypes.c_void_p), ("bm_b", ctypes.c_void_p),
+                ("sched_f", ctypes.c_void_p), ("sched_b", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (there is no other code path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "masked_flashattention_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.cm_compile_spec.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp), ctypes.c_char_p, sz]
+        L.cm_spec_free.argtypes = [vp]
+        L.cm_spec_free.restype = None
+        L.cm_spec_num_intervals.argtypes = [vp, ctypes.POINTER(i32)]
+        L.cm_spec_describe.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
+        L.cm_descriptor_sizes.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(sz)]
+        L.cm_build_descriptor.argtypes = [vp, vp, ctypes.POINTER(cm_meta), i32, i32,
+                                          ctypes.POINTER(cm_descriptor), vp]
+        L.cm_attn_fwd.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp,
+                                  i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
+        L.cm_attn_bwd.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp, vp,
+                                  vp, vp, sz, i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_get_status.argtypes = [ctypes.POINTER(cm_descriptor), vp]
+        L.cm_error_string.argtypes = [i32]
+        L.cm_error_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def cm_error_string(code: int) -> str:
+    try:
+        return lib().cm_error_string(code).decode()
+    except RuntimeError:
+        return f"error {code}"
+
+
+def _check(rc: int, what: str, detail: str = "") -> None:
+    if rc != CM_OK:
+        raise CMError(rc, what, detail)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ------------------------------------------------------------------------------------------------
+# compiler
+# ------------------------------------------------------------------------------------------------
+class Spec:
+    """Owns a compiled MaskSpec (host memory inside the library)."""
+
+    def __init__(self, handle: int, text: str):
+        self.handle = ctypes.c_void_p(handle)
+        self.text = text
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None and self.handle.value:
+            _lib.cm_spec_free(self.handle)
+            self.handle = ctypes.c_void_p(0)
+
+
+def cm_compile_spec(text: str) -> Spec:
+    out = ctypes.c_void_p()
+    err = ctypes.create_string_buffer(512)
+    rc = lib().cm_compile_spec(text.encode(), ctypes.byref(out), err, 512)
+    _check(rc, "cm_compile_spec", err.value.decode())
+    return Spec(out.value, text)
+
+
+def cm_spec_num_intervals(spec: Spec) -> int:
+    n = ctypes.c_int()
+    _check(lib().cm_spec_num_intervals(spec.handle, ctypes.byref(n)), "cm_spec_num_intervals")
+    return n.value
+
+
+def cm_spec_describe(spec: Spec) -> str:
+    need = ctypes.c_size_t()
+    _check(lib().cm_spec_describe(spec.handle, None, 0, ctypes.byref(need)), "cm_spec_describe")
+    buf = ctypes.create_string_buffer(need.value)
+    _check(lib().cm_spec_describe(spec.handle, buf, need.value, None), "cm_spec_describe")
+    return buf.value.decode()
+
+
+def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE) -> list[int]:
+    sizes = (ctypes.c_size_t * 7)()
+    _check(lib().cm_descriptor_sizes(fwd.handle, bwd.handle, B, S, tile, sizes),
+           "cm_descriptor_sizes")
+    return list(sizes)
+
+
+# ------------------------------------------------------------------------------------------------
+# descriptor
+# ------------------------------------------------------------------------------------------------
+class Descriptor:
+    """Device buffers of an Execution Descriptor, allocated with torch on ``device``."""
+
+    def __init__(self, fwd: Spec, bwd: Spec, B: int, S: int, device="cuda"):
+        sizes = cm_descriptor_sizes(fwd, bwd, B, S)
+        self.fwd, self.bwd, self.B, self.S = fwd, bwd, B, S
+        self.ni_f, self.ni_b = cm_spec_num_intervals(fwd), cm_spec_num_intervals(bwd)
+        self.NT = S // TILE
+        self.W = (self.NT + 15) // 16
+        self.itab_f = torch.empty(sizes[0] // 4, dtype=torch.int32, device=device)
+        self.bm_f = torch.empty(sizes[1] // 4, dtype=torch.int32, device=device)
+        self.itab_b = torch.empty(sizes[2] // 4, dtype=torch.int32, device=device)
+        self.bm_b = torch.empty(sizes[3] // 4, dtype=torch.int32, device=device)
+        self.sched_f = torch.empty(sizes[4] // 4, dtype=torch.int32, device=device)
+        self.sched_b = torch.empty(sizes[5] // 4, dtype=torch.int32, device=device)
+        self.status = torch.zeros(4, dtype=torch.int32, device=device)
+        self.c = cm_descriptor(B, S, TILE, self.ni_f, self.ni_b,
+                               self.itab_f.data_ptr(), self.bm_f.data_ptr(),
+                               self.itab_b.data_ptr(), self.bm_b.data_ptr(),
+                               self.sched_f.data_ptr(), self.sched_b.data_ptr(),
+                               self.status.data_ptr())
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * 4 for t in (self.itab_f, self.bm_f, self.itab_b, self.bm_b,
+                                           self.sched_f, self.sched_b)) + 4
+
+    # host views for checking
+    def interval_table_fwd(self):
+        return self.itab_f.view(self.B, self.ni_f, self.S, 2).cpu().numpy()
+
+    def interval_table_bwd(self):
+        return self.itab_b.view(self.B, self.ni_b, self.S, 2).cpu().numpy()
+
+    def bitmap_fwd(self):
+        return self.bm_f.view(self.B, self.NT, self.W).cpu().numpy().view("uint32")
+
+    def bitmap_bwd(self):
+        return self.bm_b.view(self.B, self.NT, self.W).cpu().numpy().view("uint32")
+
+
+def cm_build_descriptor(fwd: Spec, bwd: Spec, seg: torch.Tensor, nseg: torch.Tensor,
+                        desc: Descriptor, stream=None) -> None:
+    """seg: device int32 [B, nseg_max + 1]; nseg: device int32 [B]."""
+    for t in (seg, nseg):
+        if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+            raise ValueError("metadata must be contiguous int32 CUDA tensors")
+    meta = cm_meta(seg.data_ptr(), nseg.data_ptr(), seg.shape[1] - 1)
+    _check(lib().cm_build_descriptor(fwd.handle, bwd.handle, ctypes.byref(meta), desc.B, desc.S,
+                                     ctypes.byref(desc.c), _stream(stream)),
+           "cm_build_descriptor")
+
+
+def cm_get_status(desc: Descriptor, stream=None) -> int:
+    return lib().cm_get_status(ctypes.byref(desc.c), _stream(stream))
+
+
+# ------------------------------------------------------------------------------------------------
+# attention
+# ------------------------------------------------------------------------------------------------
+def _bhsd(t: torch.Tensor, name: str):
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, H, S, d]")
+    return t.shape
+
+
+def cm_attn_fwd(desc: Descriptor, q, k, v, o, lse, scale: float | None = None,
+                stream=None) -> None:
+    B, H, S, d = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o")):
+        if _bhsd(t, n) != (B, H, S, d):
+            raise ValueError(f"{n} shape mismatch")
+    if not (lse.is_cuda and lse.dtype == torch.float32 and lse.shape == (B, H, S)):
+        raise ValueError("lse must be fp32 CUDA [B, H, S]")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(lib().cm_attn_fwd(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             o.data_ptr(), lse.data_ptr(), B, H, S, d, scale, _stream(stream)),
+           "cm_attn_fwd")
+
+
+def cm_attn_bwd_workspace_size(B: int, H: int, S: int, d: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().cm_attn_bwd_workspace_size(B, H, S, d, ctypes.byref(n)),
+           "cm_attn_bwd_workspace_size")
+    return n.value
+
+
+def cm_attn_bwd(desc: Descriptor, q, k, v, o, lse, d_o, dq, dk, dv, workspace: torch.Tensor,
+                scale: float | None = None, stream=None) -> None:
+    B, H, S, d = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (d_o, "dO"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        if _bhsd(t, n) != (B, H, S, d):
+            raise ValueError(f"{n} shape mismatch")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().cm_attn_bwd(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             o.data_ptr(), lse.data_ptr(), d_o.data_ptr(), dq.data_ptr(),
+                             dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes,
+                             B, H, S, d, scale, _stream(stream)),
+           "cm_attn_bwd")
+
+
+# ------------------------------------------------------------------------------------------------
+# convenience: one call for each pass, allocating outputs with torch
+# ------------------------------------------------------------------------------------------------
+def attention_forward(desc: Descriptor, q, k, v, scale=None, stream=None):
+    B, H, S, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device)
+    cm_attn_fwd(desc, q, k, v, o, lse, scale, stream)
+    return o, lse
+
+
+def attention_backward(desc: Descriptor, q, k, v, o, lse, d_o, scale=None, stream=None,
+                       workspace=None):
+    B, H, S, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(cm_attn_bwd_workspace_size(B, H, S, d), dtype=torch.uint8,
+                                device=q.device)
+    cm_attn_bwd(desc, q, k, v, o, lse, d_o, dq, dk, dv, workspace, scale, stream)
+    return dq, dk, dv

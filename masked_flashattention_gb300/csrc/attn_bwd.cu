@@ -1,0 +1,434 @@
+// Descriptor-guided attention, backward (CompileMask sections 3.2.2 / 3.3 / 3.3.2), for sm_103a.
+//
+// The backward pass traverses key tiles, so it uses the backward descriptor: per key column j,
+// the visible query intervals, and per (key tile, query tile) the 2-bit state.  One CTA owns one
+// 128-key tile of one (sample, head) and walks the non-empty query tiles of its bitmap row:
+//
+//   S^T  = K Q^T            (tcgen05, TMEM)        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
+//   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
+//   dV  += P^T dO           (TMEM accumulator)     dK  += dS^T Q   (TMEM accumulator)
+//   dQ_part = dS K          (TMEM) -> fp32 atomics into the dQ accumulator
+//
+// Partial tiles check each query index against the key column's intervals with the unsigned
+// test of section 4.4 and zero P there (the -inf of the forward).  Empty tiles are never visited.
+//
+// Warp roles (192 threads): warps 0-3 compute (thread t owns key row t = TMEM lane t for S^T/dP^T,
+// and query row t for dQ_part), warp 4 TMA producer, warp 5 MMA issuer.
+// TMEM (512 columns): dV [0, d), dK [128, 128 + d), S^T and later dQ_part [256, 384),
+// dP^T [384, 512).
+// Shared memory: K, V (once), Q, dO (one stage), P^T and dS^T (bf16, 128-byte swizzle), LSE, D.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace cm {
+
+namespace bwd {
+
+constexpr int kThreads = 192;
+constexpr int kMaxTiles = 1024;
+
+template <int D>
+struct Smem {
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kTileBytes;
+  static constexpr uint32_t kQ = 2 * kTileBytes;
+  static constexpr uint32_t kdO = 3 * kTileBytes;
+  static constexpr uint32_t kPt = 4 * kTileBytes;
+  static constexpr uint32_t kdSt = kPt + 32768u;
+  static constexpr uint32_t kLse = kdSt + 32768u;  // 128 floats
+  static constexpr uint32_t kDelta = kLse + 512u;  // 128 floats
+  static constexpr uint32_t kBar = kDelta + 512u;
+  static constexpr uint32_t kList = kBar + 256u;
+  static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
+  static constexpr uint32_t kAlloc = kTotal + 1024u;
+};
+
+enum {
+  B_KV = 0,      // K and V loaded
+  B_QFULL = 1,   // Q, dO, LSE, D of the current query tile loaded
+  B_QEMPTY = 2,  // all MMAs reading Q / dO / P^T / dS^T of the current tile are done
+  B_SFULL = 3,   // S^T and dP^T computed
+  B_PDS = 4,     // compute warps wrote P^T and dS^T (4 arrivals)
+  B_DQFULL = 5,  // dQ_part computed (and dV, dK updates done)
+  B_DQREAD = 6,  // compute warps read dQ_part (4 arrivals)
+  B_COUNT = 7
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int NI>
+__device__ __forceinline__ uint32_t visible_bits(int i0, const int (&st)[4], const uint32_t (&len)[4]) {
+  // bit c set iff query i0 + c (c < 32) lies in one of the column's intervals
+  uint32_t bits = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    bool vis = false;
+#pragma unroll
+    for (int n = 0; n < NI; ++n)
+      vis |= (static_cast<uint32_t>(i0 - st[n]) + static_cast<uint32_t>(c)) < len[n];
+    bits |= vis ? (1u << c) : 0u;
+  }
+  return bits;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ BwdParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
+  int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
+  const float* s_delta = reinterpret_cast<const float*>(smem + L::kDelta);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = p.sched[blockIdx.x / p.H];
+  const int h = blockIdx.x % p.H;
+  const int b = item >> 16;
+  const int kt = item & 0xFFFF;
+  const int bh = b * p.H + h;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_KV), 1);
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_PDS), 4);
+    mbar_init(bar(B_DQFULL), 1);
+    mbar_init(bar(B_DQREAD), 4);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + kt) * p.W;
+    int base = 0;
+    for (int c0 = 0; c0 < p.NT; c0 += 32) {
+      const int c = c0 + lane;
+      uint32_t code = 0;
+      if (c < p.NT) code = (row[c >> 4] >> (2 * (c & 15))) & 3u;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, code != 0);
+      if (code != 0)
+        list[base + __popc(m & ((1u << lane) - 1u))] =
+            static_cast<uint16_t>(c | (code == 2u ? 0x8000 : 0));
+      base += __popc(m);
+    }
+    if (lane == 0) *s_ntiles = base;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nt = *s_ntiles;
+  const uint32_t tdV = tmem, tdK = tmem + 128, tS = tmem + 256, tdP = tmem + 384;
+  const int row0 = bh * p.S;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(B_KV), 2 * L::kTileBytes);
+      for (int x = 0; x < D / 64; ++x) {
+        tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
+        tma_load_2d(sbase + L::kV + x * 16384u, &tmV, x * 64, row0 + kt * 128, bar(B_KV));
+      }
+      for (int m = 0; m < nt; ++m) {
+        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x201)) break;
+        const int qt = list[m] & 0x3FFF;
+        mbar_arrive_expect_tx(bar(B_QFULL), 2 * L::kTileBytes + 1024u);
+        for (int x = 0; x < D / 64; ++x) {
+          tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QFULL));
+          tma_load_2d(sbase + L::kdO + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_QFULL));
+        }
+        bulk_load(sbase + L::kLse, p.lse + static_cast<size_t>(row0) + qt * 128, 512u, bar(B_QFULL));
+        bulk_load(sbase + L::kDelta, p.delta + static_cast<size_t>(row0) + qt * 128, 512u, bar(B_QFULL));
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dV, dK
+      constexpr uint32_t idMM = make_idesc_bf16(128, D, 1, 1);    // dQ_part
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ,
+                     sdO = sbase + L::kdO, sPt = sbase + L::kPt, sdSt = sbase + L::kdSt;
+      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202);
+      for (int m = 0; ok && m < nt; ++m) {
+        if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x203)) break;
+        if (m >= 1 && !mbar_wait(bar(B_DQREAD), (m - 1) & 1, abort_flag, p.status, 0x204)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tS, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQ, kk, 16384u), idSS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tdP, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL));
+        if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tdV, sdesc_kmajor(sPt, kk, 16384u), sdesc_mnmajor(sdO, kk, 16384u), idKM,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tdK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tS, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_DQFULL));
+        umma_commit(bar(B_QEMPTY));
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps 0-3
+    const int r = threadIdx.x;
+    const int j = kt * 128 + r;  // key column owned by this thread
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    int st[4];
+    uint32_t len[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      st[n] = 0;
+      len[n] = 0;
+      if (n < p.NI) {
+        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + j];
+        st[n] = iv.x;
+        len[n] = static_cast<uint32_t>(iv.y - iv.x);
+      }
+    }
+    const float sl2 = p.scale_log2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    bool ok = true;
+    for (int m = 0; m < nt; ++m) {
+      const int entry = list[m];
+      const int qt = entry & 0x3FFF;
+      const bool full = (entry & 0x8000) != 0;
+      if (!mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206)) { ok = false; break; }
+      if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x207)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32], dpr[32];
+        tmem_ld32(tS + lane_off + ch * 32, sr);
+        tmem_ld32(tdP + lane_off + ch * 32, dpr);
+        tmem_wait_ld();
+        uint32_t vis = 0xFFFFFFFFu;
+        if (!full) {
+          const int i0 = qt * 128 + ch * 32;
+          switch (p.NI) {
+            case 1: vis = visible_bits<1>(i0, st, len); break;
+            case 2: vis = visible_bits<2>(i0, st, len); break;
+            case 3: vis = visible_bits<3>(i0, st, len); break;
+            default: vis = visible_bits<4>(i0, st, len); break;
+          }
+        }
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = ch * 32 + c + e;
+            const float lse = s_lse[q];
+            // a query row that sees nothing has lse = -inf: its P is 0
+            const float off = lse == -INFINITY ? INFINITY : lse * kLog2e;
+            float pr = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -off));
+            pr = ((vis >> (c + e)) & 1u) ? pr : 0.f;
+            pv[e] = pr;
+            dv[e] = pr * (__uint_as_float(dpr[c + e]) - s_delta[q]);
+          }
+          pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
+          dd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+        }
+        // rows = keys, 32 queries of chunk ch = 4 16-byte chunks in box ch/2
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t chunk = (ch & 1) * 4 + q4;
+          const uint32_t off = (ch >> 1) * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
+          st_shared_v4(sbase + L::kPt + off, pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+          st_shared_v4(sbase + L::kdSt + off, dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PDS));
+
+      // dQ_part (query row r of this query tile) -> fp32 accumulator
+      if (!mbar_wait(bar(B_DQFULL), m & 1, abort_flag, p.status, 0x208)) { ok = false; break; }
+      tc_fence_after();
+      float* dst = p.dq_acc + (static_cast<size_t>(row0) + qt * 128 + r) * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tS + lane_off + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; q += 4)
+          atomicAdd(reinterpret_cast<float4*>(dst + c + q),
+                    make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3])));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DQREAD));
+    }
+
+    // ---- epilogue: dV, dK (scaled) -> bf16 ----
+    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D;
+    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D;
+    if (nt > 0 && ok) {
+      // the last DQFULL wait above guarantees every MMA of this CTA has completed
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t a[32], k2[32];
+        tmem_ld32(tdV + lane_off + c, a);
+        tmem_ld32(tdK + lane_off + c, k2);
+        tmem_wait_ld();
+        uint4* dva = reinterpret_cast<uint4*>(dvrow + c);
+        uint4* dka = reinterpret_cast<uint4*>(dkrow + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 x, y;
+          x.x = pack_bf16x2(__uint_as_float(a[8 * q + 0]), __uint_as_float(a[8 * q + 1]));
+          x.y = pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3]));
+          x.z = pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5]));
+          x.w = pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7]));
+          const float sc = p.scale;
+          y.x = pack_bf16x2(__uint_as_float(k2[8 * q + 0]) * sc, __uint_as_float(k2[8 * q + 1]) * sc);
+          y.y = pack_bf16x2(__uint_as_float(k2[8 * q + 2]) * sc, __uint_as_float(k2[8 * q + 3]) * sc);
+          y.z = pack_bf16x2(__uint_as_float(k2[8 * q + 4]) * sc, __uint_as_float(k2[8 * q + 5]) * sc);
+          y.w = pack_bf16x2(__uint_as_float(k2[8 * q + 6]) * sc, __uint_as_float(k2[8 * q + 7]) * sc);
+          dva[q] = x;
+          dka[q] = y;
+        }
+      }
+    } else {
+      uint4* dva = reinterpret_cast<uint4*>(dvrow);
+      uint4* dka = reinterpret_cast<uint4*>(dkrow);
+      for (int q = 0; q < D / 8; ++q) {
+        dva[q] = make_uint4(0, 0, 0, 0);
+        dka[q] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// D_i = sum_c dO[i][c] * O[i][c] (fp32) and zero the dQ accumulator row.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* o,
+                                                           const __nv_bfloat16* d_o, float* delta,
+                                                           float* dq_acc, size_t rows) {
+  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int kPer = D / 32;  // elements per lane (2 or 4)
+  const __nv_bfloat16* a = o + row * D + lane * kPer;
+  const __nv_bfloat16* g = d_o + row * D + lane * kPer;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc += __bfloat162float(a[e]) * __bfloat162float(g[e]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) delta[row] = acc;
+  float* z = dq_acc + row * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) z[e] = 0.f;
+}
+
+// dQ = bf16(scale * dQ_acc), 8 elements per thread
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* dq_acc, __nv_bfloat16* dq,
+                                                         size_t n8, float scale) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
+  const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
+  uint4 v;
+  v.x = pack_bf16x2(a.x * scale, a.y * scale);
+  v.y = pack_bf16x2(a.z * scale, a.w * scale);
+  v.z = pack_bf16x2(c.x * scale, c.y * scale);
+  v.w = pack_bf16x2(c.z * scale, c.w * scale);
+  reinterpret_cast<uint4*>(dq)[t] = v;
+}
+
+}  // namespace bwd
+
+int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
+                    const void* o, const void* d_o, void* dq, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
+  // prologue: D and zeroed accumulator
+  {
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (d == 128)
+      bwd::bwd_prologue_kernel<128><<<blocks, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o),
+          const_cast<float*>(p.delta), p.dq_acc, rows);
+    else
+      bwd::bwd_prologue_kernel<64><<<blocks, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o),
+          const_cast<float*>(p.delta), p.dq_acc, rows);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+  }
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
+      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
+    return -1;
+  const dim3 grid(p.B * p.NT * p.H);
+  if (d == 128) {
+    const uint32_t smem = bwd::Smem<128>::kAlloc;
+    if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  } else {
+    const uint32_t smem = bwd::Smem<64>::kAlloc;
+    if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  }
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  const size_t n8 = rows * d / 8;
+  bwd::dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, p.scale);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace cm

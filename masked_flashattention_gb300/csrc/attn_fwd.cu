@@ -1,0 +1,390 @@
+// Descriptor-guided attention, forward (CompileMask section 3.3.2), for sm_103a.
+//
+// One CTA computes one 128-row query tile of one (sample, head).  The Tile-State Bitmap row of
+// that query tile lists the key tiles to visit: empty tiles are skipped, full tiles run without
+// any mask, and partial tiles check every score against the row's visible intervals with one
+// unsigned subtraction and one comparison per interval (section 4.4), replacing invisible scores
+// with -inf before the online softmax.
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t); reads S from TMEM,
+//              masks, runs the online softmax in the log2 domain, writes P (bf16) to shared
+//              memory in the 128-byte-swizzled K-major layout, rescales O in TMEM when needed,
+//              and finally normalises O and writes O and the LSE
+//   warp 4     TMA producer: Q once, then K and V of each visited key tile (2-stage ring)
+//   warp 5     MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers, then
+//              O += P V into the TMEM O accumulator; completion is signalled with tcgen05.commit
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + d).
+// The running max is refreshed lazily: O and l are rescaled only when the row max grows by more
+// than 2^8, which keeps P <= 256 and the result exact because O, l and the LSE use the same max.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace cm {
+
+namespace fwd {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr int kMaxTiles = 1024;  // S <= 131072
+
+template <int D>
+struct Smem {
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kTileBytes;
+  static constexpr uint32_t kV = kK + kStages * kTileBytes;
+  static constexpr uint32_t kP = kV + kStages * kTileBytes;
+  static constexpr uint32_t kBar = kP + 32768u;
+  static constexpr uint32_t kList = kBar + 256u;
+  static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
+  static constexpr uint32_t kAlloc = kTotal + 1024u;  // slack for 1024-byte alignment
+};
+
+// barrier slots (8 bytes each) inside the barrier area
+enum {
+  B_Q = 0,
+  B_KFULL = 1,   // +stage
+  B_VFULL = 3,   // +stage
+  B_KVEMPTY = 5, // +stage
+  B_SFULL = 7,   // +buffer
+  B_SFREE = 9,   // +buffer
+  B_PFULL = 11,
+  B_ODONE = 12,
+  B_COUNT = 13
+};
+
+// Replace invisible scores of a partial tile by -inf: key j is visible to the row iff for some
+// interval (start, end): (u32)(j - start) < (u32)(end - start).
+template <int NI>
+__device__ __forceinline__ void mask_partial(float (&s)[128], int j0, const int (&st)[4],
+                                             const uint32_t (&len)[4]) {
+  uint32_t base[NI];
+#pragma unroll
+  for (int n = 0; n < NI; ++n) base[n] = static_cast<uint32_t>(j0 - st[n]);
+#pragma unroll
+  for (int c = 0; c < 128; ++c) {
+    bool vis = false;
+#pragma unroll
+    for (int n = 0; n < NI; ++n) vis |= (base[n] + static_cast<uint32_t>(c)) < len[n];
+    s[c] = vis ? s[c] : -INFINITY;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
+  int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = p.sched[blockIdx.x / p.H];
+  const int h = blockIdx.x % p.H;
+  const int b = item >> 16;
+  const int qt = item & 0xFFFF;
+  const int bh = b * p.H + h;
+
+  // ---- set-up: barriers, tile list, TMEM ----------------------------------------------------
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_KVEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_SFREE + s), 4);
+    }
+    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_ODONE), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + qt) * p.W;
+    int base = 0;
+    for (int c0 = 0; c0 < p.NT; c0 += 32) {
+      const int c = c0 + lane;
+      uint32_t code = 0;
+      if (c < p.NT) code = (row[c >> 4] >> (2 * (c & 15))) & 3u;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, code != 0);
+      if (code != 0)
+        list[base + __popc(m & ((1u << lane) - 1u))] =
+            static_cast<uint16_t>(c | (code == 2u ? 0x8000 : 0));
+      base += __popc(m);
+    }
+    if (lane == 0) *s_ntiles = base;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nt = *s_ntiles;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int row0 = bh * p.S;
+      mbar_arrive_expect_tx(bar(B_Q), L::kTileBytes);
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_Q));
+      for (int n = 0; n < nt; ++n) {
+        const int st = n % kStages;
+        if (n >= kStages &&
+            !mbar_wait(bar(B_KVEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
+          break;
+        const int kt = list[n] & 0x3FFF;
+        mbar_arrive_expect_tx(bar(B_KFULL + st), L::kTileBytes);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kK + st * L::kTileBytes + x * 16384u, &tmK, x * 64,
+                      row0 + kt * 128, bar(B_KFULL + st));
+        mbar_arrive_expect_tx(bar(B_VFULL + st), L::kTileBytes);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kV + st * L::kTileBytes + x * 16384u, &tmV, x * 64,
+                      row0 + kt * 128, bar(B_VFULL + st));
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idO = make_idesc_bf16(128, D, 0, 1);
+      const uint32_t tO = tmem + 256;
+      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, 0x102);
+      auto issue_pv = [&](int m) -> bool {
+        const int st = m % kStages;
+        if (!mbar_wait(bar(B_PFULL), m & 1, abort_flag, p.status, 0x103)) return false;
+        if (!mbar_wait(bar(B_VFULL + st), (m / kStages) & 1, abort_flag, p.status, 0x104))
+          return false;
+        tc_fence_after();
+        const uint32_t sV = sbase + L::kV + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tO, sdesc_kmajor(sbase + L::kP, kk, 16384u), sdesc_mnmajor(sV, kk, 16384u), idO,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_ODONE));
+        umma_commit(bar(B_KVEMPTY + st));
+        return true;
+      };
+      for (int n = 0; ok && n < nt; ++n) {
+        const int st = n % kStages;
+        const int sb = n & 1;
+        if (!mbar_wait(bar(B_KFULL + st), (n / kStages) & 1, abort_flag, p.status, 0x105)) break;
+        if (n >= 2 && !mbar_wait(bar(B_SFREE + sb), ((n >> 1) - 1) & 1, abort_flag, p.status, 0x106))
+          break;
+        tc_fence_after();
+        const uint32_t sK = sbase + L::kK + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + sb * 128, sdesc_kmajor(sbase + L::kQ, kk, 16384u),
+                  sdesc_kmajor(sK, kk, 16384u), idS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL + sb));
+        if (n >= 1) ok = issue_pv(n - 1);
+      }
+      if (ok) issue_pv(nt - 1);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax warps 0-3
+    const int r = threadIdx.x;  // row within the tile == TMEM lane
+    const int i = qt * 128 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    int st[4];
+    uint32_t len[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      st[n] = 0;
+      len[n] = 0;
+      if (n < p.NI) {
+        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + i];
+        st[n] = iv.x;
+        len[n] = static_cast<uint32_t>(iv.y - iv.x);
+      }
+    }
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < nt; ++n) {
+      const int sb = n & 1;
+      if (!mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x107)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t t0[32], t1[32], t2[32], t3[32];
+        tmem_ld32(tmem + lane_off + sb * 128 + 0, t0);
+        tmem_ld32(tmem + lane_off + sb * 128 + 32, t1);
+        tmem_ld32(tmem + lane_off + sb * 128 + 64, t2);
+        tmem_ld32(tmem + lane_off + sb * 128 + 96, t3);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(t0[c]);
+          s[32 + c] = __uint_as_float(t1[c]);
+          s[64 + c] = __uint_as_float(t2[c]);
+          s[96 + c] = __uint_as_float(t3[c]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SFREE + sb));
+
+      const int entry = list[n];
+      if (!(entry & 0x8000)) {
+        const int j0 = (entry & 0x3FFF) * 128;
+        switch (p.NI) {
+          case 1: mask_partial<1>(s, j0, st, len); break;
+          case 2: mask_partial<2>(s, j0, st, len); break;
+          case 3: mask_partial<3>(s, j0, st, len); break;
+          default: mask_partial<4>(s, j0, st, len); break;
+        }
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      float alpha = 1.f;
+      if (m_tile > m_run + 8.f) {  // also true when m_run = -inf and the tile has a visible key
+        alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
+        m_run = m_tile;
+      }
+      const float moff = (m_run == -INFINITY) ? 0.f : m_run;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        const float p0 = ex2_approx(fmaf(s[c], sl2, -moff));
+        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -moff));
+        const float p2 = ex2_approx(fmaf(s[c + 2], sl2, -moff));
+        const float p3 = ex2_approx(fmaf(s[c + 3], sl2, -moff));
+        l0 += p0;
+        l1 += p1;
+        l2 += p2;
+        l3 += p3;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+        pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+      }
+      l_run = l_run * alpha + ((l0 + l1) + (l2 + l3));
+
+      if (n >= 1) {
+        // PV of the previous tile must be complete: O is stable and the P buffer is free
+        if (!mbar_wait(bar(B_ODONE), (n - 1) & 1, abort_flag, p.status, 0x108)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + 256 + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st32(tmem + lane_off + 256 + c, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row -> shared memory, K-major with the 128-byte swizzle (two 64-key boxes)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t box = q >> 3, chunk = q & 7;
+        const uint32_t addr = sbase + L::kP + box * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+    }
+
+    // ---- epilogue: O / l -> bf16, LSE (natural log) ----
+    __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.S + i) * D;
+    if (nt > 0 && ok && mbar_wait(bar(B_ODONE), (nt - 1) & 1, abort_flag, p.status, 0x109)) {
+      tc_fence_after();
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + 256 + c, o);
+        tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+          dst[q] = v;
+        }
+      }
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+      for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+      l_run = 0.f;
+    }
+    p.lse[static_cast<size_t>(bh) * p.S + i] =
+        l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace fwd
+
+int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
+                    cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.S;
+  if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
+      !make_bf16_tile_map(&mv, v, rows, d))
+    return -1;
+  const dim3 grid(p.B * p.NT * p.H);
+  if (d == 128) {
+    const uint32_t smem = fwd::Smem<128>::kAlloc;
+    if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    fwd::attn_fwd_kernel<128><<<grid, fwd::kThreads, smem, stream>>>(mq, mk, mv, p);
+  } else {
+    const uint32_t smem = fwd::Smem<64>::kAlloc;
+    if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    fwd::attn_fwd_kernel<64><<<grid, fwd::kThreads, smem, stream>>>(mq, mk, mv, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace cm

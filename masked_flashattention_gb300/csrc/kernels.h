@@ -1,0 +1,50 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "program.h"
+
+struct cm_spec;
+
+namespace cm {
+
+const DevProg* spec_program(const cm_spec* s);
+
+struct FwdParams {
+  const int32_t* itab;   // forward Interval Table [B][NI][S][2]
+  const uint32_t* bm;    // forward bitmaps [B][NT][W]
+  const int32_t* sched;  // (b << 16 | q_tile), longest first
+  int32_t* status;
+  __nv_bfloat16* o;
+  float* lse;
+  int B, H, S, NT, W, NI;
+  float scale_log2;      // softmax scale * log2(e)
+};
+
+struct BwdParams {
+  const int32_t* itab;   // backward Interval Table [B][NI][S][2]
+  const uint32_t* bm;    // backward bitmaps [B][NT][W]
+  const int32_t* sched;  // (b << 16 | k_tile), longest first
+  int32_t* status;
+  const float* lse;      // [B][H][S] natural log
+  const float* delta;    // [B][H][S] rowsum(dO * O)
+  float* dq_acc;         // [B][H][S][d] fp32
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, H, S, NT, W, NI;
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e)
+};
+
+int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const int32_t* seg,
+                      const int32_t* nseg, int nseg_max, int B, int S, int32_t* itab_f,
+                      uint32_t* bm_f, int32_t* itab_b, uint32_t* bm_b, int32_t* sched_f,
+                      int32_t* sched_b, int32_t* status, cudaStream_t stream);
+int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
+                    cudaStream_t stream);
+int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
+                    const void* o, const void* d_o, void* dq, cudaStream_t stream);
+
+}  // namespace cm

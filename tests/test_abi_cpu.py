@@ -1,0 +1,147 @@
+"""CPU checks of the C ABI: the library loads and exports every declared symbol, the offline
+compiler lowers MaskSpecs as the paper describes (section 3.2.2), and host-side validation
+rejects bad arguments before anything reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from masked_flashattention_gb300 import build as bld
+    bld.build()
+    from masked_flashattention_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "cm.h")).read()
+    return re.findall(r"CM_API\s+[\w\s\*]+?\b(cm_\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(B):
+    names = declared_symbols()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_region_c_lowering(B):
+    """The paper's Region C: the response rule keeps [0, b) and [s(i), i + 1) as two slots."""
+    from masked_flashattention_gb300 import specs
+    s = B.cm_compile_spec(specs.FWD[3])
+    text = B.cm_spec_describe(s)
+    assert B.cm_spec_num_intervals(s) == 2
+    region1 = text.split("region 1")[1]
+    assert "slot 0: [0, seg_end_at(0))" in region1
+    assert "slot 1: [seg_start(i), i + 1)" in region1
+
+
+@pytest.mark.parametrize("wid,nif,nib", [(1, 1, 1), (2, 1, 1), (3, 2, 1), (4, 2, 1), (5, 3, 2)])
+def test_interval_counts(B, wid, nif, nib):
+    from masked_flashattention_gb300 import specs
+    from oracle import masks as M
+    assert (nif, nib) == M.num_intervals(wid)
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(specs.FWD[wid])) == nif
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(specs.BWD[wid])) == nib
+
+
+@pytest.mark.parametrize("rule,slots", [
+    ("j <= i", ["[0, i + 1)"]),
+    ("!(j > i)", ["[0, i + 1)"]),
+    ("j != i", ["[0, i)", "[i + 1, S)"]),
+    ("i >= j && j >= i - 3", ["[i - 3, i + 1)"]),
+    ("j == i || j == i", ["[i, i + 1)"]),
+    ("j < 0", []),
+    ("j >= i + 1 && j <= i", []),
+    ("(j < 10 || j >= 20) && j < 30", ["[0, 10)", "[20, 30)"]),
+    ("2 * i - j >= 0 - i", ["[0, 3*i + 1)"]),
+    ("j - seg_start(i) < 64 && j >= seg_start(i)", ["[seg_start(i), seg_start(i) + 64)"]),
+])
+def test_dnf_and_interval_extraction(B, rule, slots):
+    s = B.cm_compile_spec(f"region all : {rule}")
+    got = [line.split(": ", 1)[1].split(" if ")[0]
+           for line in B.cm_spec_describe(s).splitlines() if line.strip().startswith("slot")]
+    assert got == slots
+
+
+def test_conditions_without_j_become_slot_conditions(B):
+    s = B.cm_compile_spec("region all : j <= i || (i < 100 && j == 200)")
+    text = B.cm_spec_describe(s)
+    assert "slot 1: [200, 201) if i - 100 < 0" in text
+
+
+@pytest.mark.parametrize("bad", [
+    "region all j <= i",            # missing ':'
+    "region j < 3 : j <= i",        # j in a guard
+    "region all : 2 * j <= i",      # coefficient 2
+    "region all : min(j, i) <= 3",  # j inside min
+    "region all : j <= i * i",      # non-constant product
+    "region all : j <= foo(i)",     # unknown name
+    "region all : j < i < 3",       # chained comparison
+    "",                             # no region
+])
+def test_parse_errors(B, bad):
+    with pytest.raises(B.CMError) as e:
+        B.cm_compile_spec(bad)
+    assert e.value.code == B.CM_ERR_PARSE
+
+
+def test_descriptor_sizes(B):
+    from masked_flashattention_gb300 import specs
+    f, b = B.cm_compile_spec(specs.FWD[5]), B.cm_compile_spec(specs.BWD[5])
+    sizes = B.cm_descriptor_sizes(f, b, 2, 32768)
+    NT = 256
+    assert sizes == [2 * 3 * 32768 * 8, 2 * NT * 16 * 4, 2 * 2 * 32768 * 8, 2 * NT * 16 * 4,
+                     2 * NT * 4, 2 * NT * 4, 4]
+    with pytest.raises(B.CMError):
+        B.cm_descriptor_sizes(f, b, 2, 1000)   # S not a multiple of 128
+    with pytest.raises(B.CMError):
+        B.cm_descriptor_sizes(f, b, 2, 32768, tile=64)
+
+
+def _fake_desc(B, Bn, S, ni_f=1, ni_b=1):
+    p = 1 << 20  # never dereferenced: validation fails first
+    return B.cm_descriptor(Bn, S, 128, ni_f, ni_b, p, p, p, p, p, p, p)
+
+
+def test_attention_argument_validation_happens_on_the_host(B):
+    L = B.lib()
+    p = ctypes.c_void_p(1 << 20)
+    d = _fake_desc(B, 1, 256)
+    # unsupported head dim
+    assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 1, 2, 256, 96, 0.1, None) == B.CM_ERR_UNSUPPORTED
+    # S not a multiple of the tile
+    d2 = _fake_desc(B, 1, 200)
+    assert L.cm_attn_fwd(ctypes.byref(d2), p, p, p, p, p, 1, 2, 200, 64, 0.1, None) == B.CM_ERR_UNSUPPORTED
+    # descriptor built for another shape
+    assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 2, 2, 256, 64, 0.1, None) == B.CM_ERR_INVALID_ARG
+    # null tensor
+    assert L.cm_attn_fwd(ctypes.byref(d), None, p, p, p, p, 1, 2, 256, 64, 0.1, None) == B.CM_ERR_INVALID_ARG
+    # misaligned tensor
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert L.cm_attn_fwd(ctypes.byref(d), odd, p, p, p, p, 1, 2, 256, 64, 0.1, None) == B.CM_ERR_INVALID_ARG
+    # non-finite scale
+    assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 1, 2, 256, 64, float("nan"), None) == B.CM_ERR_INVALID_ARG
+    # backward: workspace too small
+    need = B.cm_attn_bwd_workspace_size(1, 2, 256, 64)
+    assert need == 1 * 2 * 256 * 4 + 1 * 2 * 256 * 64 * 4
+    assert L.cm_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, need - 1, 1, 2, 256, 64,
+                         0.1, None) == B.CM_ERR_INVALID_ARG
+    # metadata pointer missing
+    from masked_flashattention_gb300 import specs
+    f, b = B.cm_compile_spec(specs.FWD[1]), B.cm_compile_spec(specs.BWD[1])
+    meta = B.cm_meta(None, None, 3)
+    assert L.cm_build_descriptor(f.handle, b.handle, ctypes.byref(meta), 1, 256, ctypes.byref(d),
+                                 None) == B.CM_ERR_INVALID_ARG
+
+
+def test_error_strings(B):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert B.cm_error_string(code)
