@@ -63,7 +63,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -220,6 +220,8 @@ def run_gpu(args):
 
     Bd.lib()
     w = W.WORKLOADS[args.config]
+    if args.heads:
+        w = W.Workload(w.id, f"{w.name}@H{args.heads}", w.B, args.heads, w.S, w.d)
     Bn, H, S, d = w.B, w.H, w.S, w.d
     scale = 1.0 / math.sqrt(d)
     seg_np, nseg_np = W.segments(w.id, Bn, S)
@@ -331,8 +333,14 @@ def run_gpu(args):
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
+        import hashlib
         with open(tp) as f:
-            traffic = json.load(f).get(f"attn_bwd@{w.name}")
+            rec = json.load(f).get(f"attn_bwd@{w.name}")
+        src = os.path.join(ROOT, "masked_flashattention_gb300", "csrc", "attn_bwd.cu")
+        with open(src, "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+        if rec and rec.get("source_sha1") == sha:  # counters only count for the kernel they measured
+            traffic = rec["bytes"]
 
     if rank == 0:
         line = {
@@ -358,7 +366,7 @@ def run_gpu(args):
             "clocks": clk,
         }
         if world == 1 and not args.no_cpu_baseline:
-            dt, pr, cores, sdesc = oracle_sample(w.id, args.ref_rows)
+            dt, pr, cores, sdesc = oracle_sample(args.config, args.ref_rows)
             line["cpu_baseline"] = {"value": FLOPS_PER_PAIR_PER_D * d * pr / dt / 1e12,
                                     "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": sdesc}
@@ -371,11 +379,13 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=3, help="workload 1..5 (default: 3, RM 32K)")
     ap.add_argument("--impl", default="cm", choices=["cm", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=8192)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the head count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
