@@ -145,6 +145,30 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
                        void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
                        int d, float scale, void* stream);
 
+/* ---- backward without a workspace (no counterpart in the paper) ---------------------------- */
+
+/* Size of the library's built-in backward scratch array (32 MiB per GPU that loads libcm.so). */
+#define CM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Same computation and arguments as cm_attn_bwd, minus the workspace, for callers that cannot
+ * allocate device memory themselves: plugins whose host framework owns all device memory, or
+ * latency-critical threads that must not call cudaMalloc (it can synchronise the device).  The
+ * scratch comes from a fixed file-scope device array inside the library instead, so this call
+ * allocates nothing.
+ *   - Limit: the workspace cm_attn_bwd_workspace_size reports must fit CM_NOALLOC_SCRATCH_BYTES
+ *     (e.g. B*H*S <= 65027 rows at d = 128); larger problems return CM_ERR_UNSUPPORTED and queue
+ *     nothing.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call on each
+ *     device, with that device current; make that first call before any stream capture.
+ *   - The array is held by every GPU that loads the library until the process exits.
+ *   - All calls share the one array per device, and it keeps the previous call's contents (each
+ *     call re-initialises what must start at zero).  Calls whose work overlaps on the GPU, e.g.
+ *     on two streams, race on it: order them on one stream. */
+CM_API int cm_attn_bwd_noalloc(const cm_descriptor* desc, const void* q, const void* k,
+                               const void* v, const void* o, const float* lse, const void* d_o,
+                               void* dq, void* dk, void* dv, int B, int H, int S, int d,
+                               float scale, void* stream);
+
 /* ---- status --------------------------------------------------------------------------------- */
 
 /* Wait for `stream`, then read desc->status: CM_OK, CM_ERR_TIMEOUT or CM_ERR_DEVICE_CHECK

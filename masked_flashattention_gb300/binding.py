@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.cm_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
         L.cm_attn_bwd.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, sz, i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_attn_bwd_noalloc.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp,
+                                          vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
         L.cm_get_status.argtypes = [ctypes.POINTER(cm_descriptor), vp]
         L.cm_error_string.argtypes = [i32]
         L.cm_error_string.restype = ctypes.c_char_p
@@ -243,6 +245,27 @@ def cm_attn_bwd(desc: Descriptor, q, k, v, o, lse, d_o, dq, dk, dv, workspace: t
                              dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes,
                              B, H, S, d, scale, _stream(stream)),
            "cm_attn_bwd")
+
+
+def cm_attn_bwd_noalloc(desc: Descriptor, q, k, v, o, lse, d_o, dq, dk, dv,
+                        scale: float | None = None, stream=None) -> None:
+    """cm_attn_bwd without a workspace, for callers that cannot allocate device memory.
+
+    The library's fixed scratch array (CM_NOALLOC_SCRATCH_BYTES per GPU) stands in for the
+    workspace; see include/cm.h for its limit and for the rule that overlapping calls race."""
+    B, H, S, d = _bhsd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (d_o, "dO"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        if _bhsd(t, n) != (B, H, S, d):
+            raise ValueError(f"{n} shape mismatch")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(lib().cm_attn_bwd_noalloc(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(),
+                                     v.data_ptr(), o.data_ptr(), lse.data_ptr(), d_o.data_ptr(),
+                                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, d,
+                                     scale, _stream(stream)),
+           "cm_attn_bwd_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 # ------------------------------------------------------------------------------------------------

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcm.so")
 
-SOURCES = ["compiler.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "api.cu"]
+SOURCES = ["compiler.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "api.cu",
+           "attn_bwd_noalloc.cu"]
 HEADERS = ["program.h", "kernels.h", "ptx.cuh", "tma_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
