@@ -204,6 +204,32 @@ def visible_pairs(desc, B: int, S: int):
     return [int(x) for x in total.sum(dim=1).tolist()]
 
 
+def preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev, target_mb=64.0, reps=20):
+    """Descriptor build replicated over a batch large enough that the descriptor (>= 64 MB)
+    exceeds what launch latency hides: achieved HBM GB/s of the preprocess kernels."""
+    import numpy as np
+    import torch
+    per_sample = sum(Bd.cm_descriptor_sizes(fwd, bwd, 1, S))
+    nt = S // 128
+    Bs = max(1, min(32768 // nt, math.ceil(target_mb * 2**20 / per_sample)))
+    rep = math.ceil(Bs / seg_np.shape[0])
+    seg = torch.from_numpy(np.tile(seg_np, (rep, 1))[:Bs].copy()).to(dev)
+    nseg = torch.from_numpy(np.tile(nseg_np, rep)[:Bs].copy()).to(dev)
+    desc = Bd.Descriptor(fwd, bwd, Bs, S, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        Bd.cm_build_descriptor(fwd, bwd, seg, nseg, desc, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        Bd.cm_build_descriptor(fwd, bwd, seg, nseg, desc, stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    us = a.elapsed_time(b) * 1e3 / reps
+    nbytes = seg.numel() * 4 + nseg.numel() * 4 + desc.nbytes()
+    return {"B": Bs, "MB": nbytes / 2**20, "us": us, "gbs": nbytes / (us * 1e-6) / 1e9}
+
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -330,6 +356,9 @@ def run_gpu(args):
     fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
     meta_bytes = seg.numel() * 4 + nseg.numel() * 4
     prep_bytes = meta_bytes + desc.nbytes()
+    sweep = preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev)
+    if sweep is not None:
+        sweep["pct_hbm"] = 100.0 * sweep["gbs"] / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -356,6 +385,7 @@ def run_gpu(args):
                        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "build_ms": build_ms,
                        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
                        "preprocess_gbs": prep_bytes / (build_ms / 1e3) / 1e9,
+                       "preprocess_sweep": sweep,
                        "peak_source": f"{peak_src} bf16_tflops_sustained"},
             "roofline": {"bound": "tensor", "kernel": "attention backward (prologue + main + dQ convert)",
                          "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",

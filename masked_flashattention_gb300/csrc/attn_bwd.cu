@@ -6,17 +6,27 @@
 //
 //   S^T  = K Q^T            (tcgen05, TMEM)        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
 //   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
-//   dV  += P^T dO           (TMEM accumulator)     dK  += dS^T Q   (TMEM accumulator)
-//   dQ_part = dS K          (TMEM) -> fp32 atomics into the dQ accumulator
+//   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
+//   dK  += dS^T Q           (TMEM accumulator)
+//   dQ_part = dS K          (TMEM) -> shared memory -> TMA bulk add into the fp32 dQ accumulator
 //
 // Partial tiles check each query index against the key column's intervals with the unsigned
 // test of section 4.4 and zero P there (the -inf of the forward).  Empty tiles are never visited.
 //
-// Warp roles (192 threads): warps 0-3 compute (thread t owns key row t = TMEM lane t for S^T/dP^T,
-// and query row t for dQ_part), warp 4 TMA producer, warp 5 MMA issuer.
-// TMEM (512 columns): dV [0, d), dK [128, 128 + d), S^T and later dQ_part [256, 384),
-// dP^T [384, 512).
-// Shared memory: K, V (once), Q, dO (one stage), P^T and dS^T (bf16, 128-byte swizzle), LSE, D.
+// Warp roles (320 threads):
+//   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
+//              half w / 4: queries [64*half, +64) of S^T / dP^T, and head-dim columns
+//              [half*d/2, +d/2) of dQ_part, dV and dK.
+//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE by bulk copy) into one slot and
+//              dO (+ D) into two slots, so the next tile's dO is in flight during this tile.
+//   warp 9     MMA issuer (one thread).  Per query tile: S^T, dP^T; then dK first (its
+//              completion frees Q for the next tile), dV, and dQ_part.
+// TMEM (512 columns): dV [0, d), dK [128, 128+d), R1 [256, 384) = S^T, overwritten in place by
+// the bf16 P^T pairs (each warp writes only columns it has already read), R2 [384, 512) = dP^T,
+// then dQ_part.
+// Shared memory: K, V, Q, dO x2 (bf16, 128-byte swizzle); the dS^T tile, whose box h also serves
+// as column half h's fp32 staging tile for the dQ bulk add once the MMAs reading dS^T are done;
+// LSE and D x2 of the query tiles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -29,8 +39,16 @@ namespace cm {
 
 namespace bwd {
 
-constexpr int kThreads = 192;
+constexpr int kComputeWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kMaxTiles = 1024;
+
+constexpr uint32_t kColDV = 0;
+constexpr uint32_t kColDK = 128;
+constexpr uint32_t kColR1 = 256;
+constexpr uint32_t kColR2 = 384;
 
 template <int D>
 struct Smem {
@@ -38,26 +56,31 @@ struct Smem {
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTileBytes;
   static constexpr uint32_t kQ = 2 * kTileBytes;
-  static constexpr uint32_t kdO = 3 * kTileBytes;
-  static constexpr uint32_t kPt = 4 * kTileBytes;
-  static constexpr uint32_t kdSt = kPt + 32768u;
-  static constexpr uint32_t kLse = kdSt + 32768u;  // 128 floats
-  static constexpr uint32_t kDelta = kLse + 512u;  // 128 floats
-  static constexpr uint32_t kBar = kDelta + 512u;
+  static constexpr uint32_t kdO = 3 * kTileBytes;   // two slots
+  // dS^T [2 boxes][128 keys][64 queries] bf16; once the MMAs that read it are done, box h is the
+  // fp32 [128 rows][32 cols] staging tile of column half h for the dQ bulk add
+  static constexpr uint32_t kdSt = 5 * kTileBytes;
+  static constexpr uint32_t kLse = kdSt + 32768u;   // 128 floats (with Q)
+  static constexpr uint32_t kDelta = kLse + 512u;   // two slots of 128 floats (with dO)
+  static constexpr uint32_t kBar = kDelta + 1024u;
   static constexpr uint32_t kList = kBar + 256u;
   static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
   static constexpr uint32_t kAlloc = kTotal + 1024u;
 };
 
 enum {
-  B_KV = 0,      // K and V loaded
-  B_QFULL = 1,   // Q, dO, LSE, D of the current query tile loaded
-  B_QEMPTY = 2,  // all MMAs reading Q / dO / P^T / dS^T of the current tile are done
-  B_SFULL = 3,   // S^T and dP^T computed
-  B_PDS = 4,     // compute warps wrote P^T and dS^T (4 arrivals)
-  B_DQFULL = 5,  // dQ_part computed (and dV, dK updates done)
-  B_DQREAD = 6,  // compute warps read dQ_part (4 arrivals)
-  B_COUNT = 7
+  B_KV = 0,       // K and V loaded
+  B_QFULL = 1,    // Q and LSE of the current query tile loaded
+  B_QEMPTY = 2,   // the dK MMA (last reader of Q) of the current tile is done
+  B_DOFULL = 3,   // +slot: dO and D of a query tile loaded
+  B_DOEMPTY = 5,  // +slot: the dV MMA (last reader of the dO slot) is done
+  B_SFULL = 7,    // S^T and dP^T computed
+  B_PDS = 8,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
+  B_DQFULL = 9,   // dQ_part computed (and every MMA of the tile done)
+  B_DQREAD = 10,  // compute warps read dQ_part from TMEM (8 arrivals)
+  B_STGFREE = 11, // +half: the half's box of the dS^T buffer may be written (leader, 1 arrival)
+  B_STGFULL = 13, // +half: the half's 4 warps wrote their staging rows (4 arrivals)
+  B_COUNT = 15
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -87,8 +110,10 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const __grid_constant__ BwdParams p) {
+                const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ BwdParams p) {
   using L = Smem<D>;
+  constexpr int kHalf = D / 2;           // head-dim columns per compute warp
+  constexpr int kChunks = kHalf / 32;    // 32-column dQ chunks per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -115,10 +140,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_KV), 1);
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(bar(B_DOFULL + sl), 1);
+      mbar_init(bar(B_DOEMPTY + sl), 1);
+    }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_PDS), 4);
+    mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQREAD), 4);
+    mbar_init(bar(B_DQREAD), kComputeWarps);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(bar(B_STGFREE + hh), 1);
+      mbar_init(bar(B_STGFULL + hh), 4);
+    }
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -136,7 +169,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     if (lane == 0) *s_ntiles = base;
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -145,76 +178,97 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nt = *s_ntiles;
-  const uint32_t tdV = tmem, tdK = tmem + 128, tS = tmem + 256, tdP = tmem + 384;
   const int row0 = bh * p.S;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
+      tma_prefetch_desc(&tmdQ);
       mbar_arrive_expect_tx(bar(B_KV), 2 * L::kTileBytes);
       for (int x = 0; x < D / 64; ++x) {
         tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
         tma_load_2d(sbase + L::kV + x * 16384u, &tmV, x * 64, row0 + kt * 128, bar(B_KV));
       }
       for (int m = 0; m < nt; ++m) {
-        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x201)) break;
         const int qt = list[m] & 0x3FFF;
-        mbar_arrive_expect_tx(bar(B_QFULL), 2 * L::kTileBytes + 1024u);
-        for (int x = 0; x < D / 64; ++x) {
+        const int ds = m & 1;
+        // dO and D: two slots, so the next tile's are in flight while this tile computes
+        if (m >= 2 && !mbar_wait(bar(B_DOEMPTY + ds), ((m >> 1) - 1) & 1, abort_flag, p.status, 0x201))
+          break;
+        mbar_arrive_expect_tx(bar(B_DOFULL + ds), L::kTileBytes + 512u);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kdO + ds * L::kTileBytes + x * 16384u, &tmdO, x * 64,
+                      row0 + qt * 128, bar(B_DOFULL + ds));
+        bulk_load(sbase + L::kDelta + ds * 512u, p.delta + static_cast<size_t>(row0) + qt * 128,
+                  512u, bar(B_DOFULL + ds));
+        // Q and LSE: one slot, refilled as soon as the dK MMA of the previous tile is done
+        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x20b)) break;
+        mbar_arrive_expect_tx(bar(B_QFULL), L::kTileBytes + 512u);
+        for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QFULL));
-          tma_load_2d(sbase + L::kdO + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_QFULL));
-        }
         bulk_load(sbase + L::kLse, p.lse + static_cast<size_t>(row0) + qt * 128, 512u, bar(B_QFULL));
-        bulk_load(sbase + L::kDelta, p.delta + static_cast<size_t>(row0) + qt * 128, 512u, bar(B_QFULL));
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dV, dK
+      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dV (TS), dK
       constexpr uint32_t idMM = make_idesc_bf16(128, D, 1, 1);    // dQ_part
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ,
-                     sdO = sbase + L::kdO, sPt = sbase + L::kPt, sdSt = sbase + L::kdSt;
+                     sdSt = sbase + L::kdSt;
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202);
       for (int m = 0; ok && m < nt; ++m) {
+        const int ds = m & 1;
+        const uint32_t sdO = sbase + L::kdO + ds * L::kTileBytes;
         if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x203)) break;
+        if (!mbar_wait(bar(B_DOFULL + ds), (m >> 1) & 1, abort_flag, p.status, 0x20c)) break;
+        // dQ_part of the previous tile has been read out of R2, which also means every MMA of the
+        // previous tile (including the dV that read P^T from R1) has completed
         if (m >= 1 && !mbar_wait(bar(B_DQREAD), (m - 1) & 1, abort_flag, p.status, 0x204)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tS, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQ, kk, 16384u), idSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColR1, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQ, kk, 16384u), idSS,
+                  kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tdP, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColR2, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
+                  kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL));
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tdV, sdesc_kmajor(sPt, kk, 16384u), sdesc_mnmajor(sdO, kk, 16384u), idKM,
+          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
                   (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_QEMPTY));  // Q may be refilled once dK is done
+        // P^T pairs: queries [0,64) at R1 columns [0,32), queries [64,128) at [64,96)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tdK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
-                  (m > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + kColDV, tmem + kColR1 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_DOEMPTY + ds));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tS, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
+          umma_ss(tmem + kColR2, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
                   kk > 0 ? 1u : 0u);
         umma_commit(bar(B_DQFULL));
-        umma_commit(bar(B_QEMPTY));
       }
     }
   } else {
-    // ---------------------------------------------------------------- compute warps 0-3
-    const int r = threadIdx.x;
-    const int j = kt * 128 + r;  // key column owned by this thread
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------------------------------------------------------- compute warps 0-7
+    const int quarter = warp & 3;
+    const int hf = warp >> 2;
+    const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_part)
+    const int j = kt * 128 + r;         // key column owned for S^T / dP^T
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool leader = (quarter == 0 && lane == 0);           // issues this half's bulk adds
+    const uint32_t stage = sbase + L::kdSt + hf * 16384u;  // this half's dS^T box / dQ staging
     int st[4];
     uint32_t len[4];
 #pragma unroll
@@ -230,22 +284,37 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float sl2 = p.scale_log2;
     constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;
-    for (int m = 0; m < nt; ++m) {
+    for (int m = 0; ok && m < nt; ++m) {
       const int entry = list[m];
       const int qt = entry & 0x3FFF;
       const bool full = (entry & 0x8000) != 0;
-      if (!mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206)) { ok = false; break; }
-      if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x207)) { ok = false; break; }
+      const int ds = m & 1;
+      const float* s_dlt = s_delta + ds * 128;
+      bool ready = mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206) &&
+                   mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x207) &&
+                   mbar_wait(bar(B_DOFULL + ds), (m >> 1) & 1, abort_flag, p.status, 0x20d);
+      // this half's dS^T box is also the staging tile of the previous tile's dQ bulk adds: wait
+      // until those have stopped reading it (use uf of the box)
+      const int uf0 = m * (1 + kChunks);
+      if (leader) {
+        bulk_wait_read_all();
+        mbar_arrive(bar(B_STGFREE + hf));
+      }
+      ready = mbar_wait(bar(B_STGFREE + hf), uf0 & 1, abort_flag, p.status, 0x20e) && ready;
+      __syncwarp();
+      if (!ready) { ok = false; break; }
       tc_fence_after();
+      // this warp's 64 queries, in two chunks of 32
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int q0 = 64 * hf + 32 * ch;  // first query of the chunk within the tile
         uint32_t sr[32], dpr[32];
-        tmem_ld32(tS + lane_off + ch * 32, sr);
-        tmem_ld32(tdP + lane_off + ch * 32, dpr);
+        tmem_ld32(tmem + lane_off + kColR1 + q0, sr);
+        tmem_ld32(tmem + lane_off + kColR2 + q0, dpr);
         tmem_wait_ld();
         uint32_t vis = 0xFFFFFFFFu;
         if (!full) {
-          const int i0 = qt * 128 + ch * 32;
+          const int i0 = qt * 128 + q0;
           switch (p.NI) {
             case 1: vis = visible_bits<1>(i0, st, len); break;
             case 2: vis = visible_bits<2>(i0, st, len); break;
@@ -259,65 +328,95 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           float pv[2], dv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int q = ch * 32 + c + e;
+            const int q = q0 + c + e;
             const float lse = s_lse[q];
             // a query row that sees nothing has lse = -inf: its P is 0
             const float off = lse == -INFINITY ? INFINITY : lse * kLog2e;
             float pr = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -off));
             pr = ((vis >> (c + e)) & 1u) ? pr : 0.f;
             pv[e] = pr;
-            dv[e] = pr * (__uint_as_float(dpr[c + e]) - s_delta[q]);
+            dv[e] = pr * (__uint_as_float(dpr[c + e]) - s_dlt[q]);
           }
           pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
           dd[c / 2] = pack_bf16x2(dv[0], dv[1]);
         }
-        // rows = keys, 32 queries of chunk ch = 4 16-byte chunks in box ch/2
+        // P^T pairs into R1 columns this warp has already read: hf * 64 + ch * 16
+        tmem_st16(tmem + lane_off + kColR1 + hf * 64 + ch * 16, pp);
+        // dS^T row r, queries q0..q0+31 = four 16-byte chunks of box hf
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = (ch & 1) * 4 + q4;
-          const uint32_t off = (ch >> 1) * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
-          st_shared_v4(sbase + L::kPt + off, pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+          const uint32_t chunk = ch * 4 + q4;
+          const uint32_t off = hf * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
           st_shared_v4(sbase + L::kdSt + off, dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
         }
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PDS));
 
-      // dQ_part (query row r of this query tile) -> fp32 accumulator
-      if (!mbar_wait(bar(B_DQFULL), m & 1, abort_flag, p.status, 0x208)) { ok = false; break; }
-      tc_fence_after();
-      float* dst = p.dq_acc + (static_cast<size_t>(row0) + qt * 128 + r) * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tS + lane_off + c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; q += 4)
-          atomicAdd(reinterpret_cast<float4*>(dst + c + q),
-                    make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
-                                __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3])));
-      }
-      tc_fence_before();
+      // dQ_part: query row r of this tile, head-dim columns [hf * kHalf, +kHalf)
+      ready = mbar_wait(bar(B_DQFULL), m & 1, abort_flag, p.status, 0x208);
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DQREAD));
+      if (!ready) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < kChunks; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + kColR2 + hf * kHalf + cc * 32, v);
+        tmem_wait_ld();
+        if (cc == kChunks - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DQREAD));  // R2 may be overwritten now
+        }
+        // use uf of this half's box: wait until the previous bulk add stopped reading it
+        const int uf = uf0 + 1 + cc;
+        const int u = m * kChunks + cc;
+        if (leader) {
+          bulk_wait_read_all();
+          mbar_arrive(bar(B_STGFREE + hf));
+        }
+        const bool free_ok = mbar_wait(bar(B_STGFREE + hf), uf & 1, abort_flag, p.status, 0x209);
+        __syncwarp();
+        if (!free_ok) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(stage + r * 128u + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4), v[4 * c],
+                       v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STGFULL + hf));
+        bool full_ok = true;
+        if (leader) {
+          full_ok = mbar_wait(bar(B_STGFULL + hf), u & 1, abort_flag, p.status, 0x20a);
+          if (full_ok) {
+            tma_reduce_add_2d(&tmdQ, hf * kHalf + cc * 32, row0 + qt * 128, stage);
+            bulk_commit_group();
+          }
+        }
+        full_ok = __shfl_sync(0xFFFFFFFFu, full_ok, 0);
+        if (!full_ok) { ok = false; break; }
+      }
     }
+    if (leader) bulk_wait_all();
+    __syncwarp();
 
-    // ---- epilogue: dV, dK (scaled) -> bf16 ----
-    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D;
-    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D;
+    // ---- epilogue: dV, dK (scaled) -> bf16, this warp's half of the head dim ----
+    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
+    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
     if (nt > 0 && ok) {
       // the last DQFULL wait above guarantees every MMA of this CTA has completed
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < kHalf; c += 32) {
         uint32_t a[32], k2[32];
-        tmem_ld32(tdV + lane_off + c, a);
-        tmem_ld32(tdK + lane_off + c, k2);
+        tmem_ld32(tmem + lane_off + kColDV + hf * kHalf + c, a);
+        tmem_ld32(tmem + lane_off + kColDK + hf * kHalf + c, k2);
         tmem_wait_ld();
         uint4* dva = reinterpret_cast<uint4*>(dvrow + c);
         uint4* dka = reinterpret_cast<uint4*>(dkrow + c);
+        const float sc = p.scale;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 x, y;
@@ -325,7 +424,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           x.y = pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3]));
           x.z = pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5]));
           x.w = pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7]));
-          const float sc = p.scale;
           y.x = pack_bf16x2(__uint_as_float(k2[8 * q + 0]) * sc, __uint_as_float(k2[8 * q + 1]) * sc);
           y.y = pack_bf16x2(__uint_as_float(k2[8 * q + 2]) * sc, __uint_as_float(k2[8 * q + 3]) * sc);
           y.z = pack_bf16x2(__uint_as_float(k2[8 * q + 4]) * sc, __uint_as_float(k2[8 * q + 5]) * sc);
@@ -337,7 +435,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
       uint4* dva = reinterpret_cast<uint4*>(dvrow);
       uint4* dka = reinterpret_cast<uint4*>(dkrow);
-      for (int q = 0; q < D / 8; ++q) {
+      for (int q = 0; q < kHalf / 8; ++q) {
         dva[q] = make_uint4(0, 0, 0, 0);
         dka[q] = make_uint4(0, 0, 0, 0);
       }
@@ -348,7 +446,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // D_i = sum_c dO[i][c] * O[i][c] (fp32) and zero the dQ accumulator row.  One warp per row.
@@ -406,9 +504,10 @@ int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, con
           const_cast<float*>(p.delta), p.dq_acc, rows);
     if (cudaGetLastError() != cudaSuccess) return -1;
   }
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
-      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
+      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d) ||
+      !make_f32_tile_map(&mdq, p.dq_acc, rows, d))
     return -1;
   const dim3 grid(p.B * p.NT * p.H);
   if (d == 128) {
@@ -416,13 +515,13 @@ int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, con
     if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return -1;
-    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
   } else {
     const uint32_t smem = bwd::Smem<64>::kAlloc;
     if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return -1;
-    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
   }
   if (cudaGetLastError() != cudaSuccess) return -1;
   const size_t n8 = rows * d / 8;

@@ -6,15 +6,19 @@
 // unsigned subtraction and one comparison per interval (section 4.4), replacing invisible scores
 // with -inf before the online softmax.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t); reads S from TMEM,
-//              masks, runs the online softmax in the log2 domain, writes P (bf16) to shared
-//              memory in the 128-byte-swizzled K-major layout, rescales O in TMEM when needed,
-//              and finally normalises O and writes O and the LSE
-//   warp 4     TMA producer: Q once, then K and V of each visited key tile (2-stage ring)
-//   warp 5     MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers, then
-//              O += P V into the TMEM O accumulator; completion is signalled with tcgen05.commit
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + d).
+// Warp roles (320 threads):
+//   warps 0-7  softmax.  Warp w serves TMEM lane quarter w % 4 (query rows 32*(w%4) ..) and
+//              column half w / 4 of each 128-key S tile, so every query row is handled by a pair
+//              of warps that exchange their partial row maxima through shared memory.  They read
+//              S from TMEM, mask partial tiles, run the online softmax in the log2 domain, write
+//              P (bf16 pairs) back into TMEM, rescale O in TMEM when needed, and finally
+//              normalise O and write O and the LSE.
+//   warp 8     TMA producer: Q once, then K and V of each visited key tile through two 3-slot
+//              rings (a K slot frees when its S MMA completes, a V slot when its PV completes).
+//   warp 9     MMA issuer (one thread): S = Q K^T and O += P V, both with the A operand (Q, P)
+//              read from TMEM and the B operand (K, V) from shared memory, so shared memory
+//              carries only K and V.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+d), P [384, 448), Q [448, 448+d/2).
 // The running max is refreshed lazily: O and l are rescaled only when the row max grows by more
 // than 2^8, which keeps P <= 256 and the result exact because O, l and the LSE use the same max.
 #include <cuda_bf16.h>
@@ -26,49 +30,59 @@
 #include "tma_host.h"
 
 namespace cm {
-
 namespace fwd {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kStages = 3;  // K ring and V ring depth
 constexpr int kMaxTiles = 1024;  // S <= 131072
+
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
+constexpr uint32_t kColQ = 448;
 
 template <int D>
 struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kTileBytes;
+  static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kStages * kTileBytes;
-  static constexpr uint32_t kP = kV + kStages * kTileBytes;
-  static constexpr uint32_t kBar = kP + 32768u;
+  // Q is staged in K slot 2 (first needed by the third key tile, after Q has moved into TMEM)
+  static constexpr uint32_t kQ = kK + 2 * kTileBytes;
+  static constexpr uint32_t kRed = kV + kStages * kTileBytes;  // float [2][2][128]
+  static constexpr uint32_t kBar = kRed + 2048u;
   static constexpr uint32_t kList = kBar + 256u;
   static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
   static constexpr uint32_t kAlloc = kTotal + 1024u;  // slack for 1024-byte alignment
 };
 
-// barrier slots (8 bytes each) inside the barrier area
 enum {
-  B_Q = 0,
-  B_KFULL = 1,   // +stage
-  B_VFULL = 3,   // +stage
-  B_KVEMPTY = 5, // +stage
-  B_SFULL = 7,   // +buffer
-  B_SFREE = 9,   // +buffer
-  B_PFULL = 11,
-  B_ODONE = 12,
-  B_COUNT = 13
+  B_Q = 0,        // Q tile in shared memory (TMA)
+  B_QT = 1,       // Q copied into TMEM (8 softmax warps)
+  B_KFULL = 2,    // +stage
+  B_VFULL = 5,    // +stage
+  B_KEMPTY = 8,   // +stage: the S MMA that read the K slot has completed
+  B_VEMPTY = 11,  // +stage: the PV MMA that read the V slot has completed
+  B_SFULL = 14,   // +buffer
+  B_SFREE = 16,   // +buffer (8 arrivals)
+  B_PFULL = 18,   // P in TMEM and O rescaled (8 arrivals)
+  B_ODONE = 19,
+  B_PAIR = 20,    // +2*quarter+parity: row-max / row-sum exchange of a warp pair (2 arrivals)
+  B_COUNT = 28
 };
 
-// Replace invisible scores of a partial tile by -inf: key j is visible to the row iff for some
-// interval (start, end): (u32)(j - start) < (u32)(end - start).
-template <int NI>
-__device__ __forceinline__ void mask_partial(float (&s)[128], int j0, const int (&st)[4],
-                                             const uint32_t (&len)[4]) {
+// Replace invisible scores by -inf: key j0 + c is visible to the row iff for some interval
+// (start, end): (u32)(j0 + c - start) < (u32)(end - start).
+template <int NI, int N>
+__device__ __forceinline__ void mask_cols(float (&s)[N], int j0, const int (&st)[4],
+                                          const uint32_t (&len)[4]) {
   uint32_t base[NI];
 #pragma unroll
   for (int n = 0; n < NI; ++n) base[n] = static_cast<uint32_t>(j0 - st[n]);
 #pragma unroll
-  for (int c = 0; c < 128; ++c) {
+  for (int c = 0; c < N; ++c) {
     bool vis = false;
 #pragma unroll
     for (int n = 0; n < NI; ++n) vis |= (base[n] + static_cast<uint32_t>(c)) < len[n];
@@ -81,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
+  constexpr int kHalf = D / 2;  // O columns per softmax warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -90,6 +105,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -104,17 +120,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_Q), 1);
+    mbar_init(bar(B_QT), kSoftmaxWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SFREE + s), 4);
+      mbar_init(bar(B_SFREE + s), kSoftmaxWarps);
     }
-    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_PFULL), kSoftmaxWarps);
     mbar_init(bar(B_ODONE), 1);
+    for (int s = 0; s < 8; ++s) mbar_init(bar(B_PAIR + s), 2);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -132,7 +151,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     if (lane == 0) *s_ntiles = base;
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -142,7 +161,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   const int nt = *s_ntiles;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nt > 0) {
       tma_prefetch_desc(&tmQ);
@@ -155,26 +174,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int n = 0; n < nt; ++n) {
         const int st = n % kStages;
         if (n >= kStages &&
-            !mbar_wait(bar(B_KVEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
+            !mbar_wait(bar(B_KEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
           break;
+        // K slot 2 holds Q until the softmax warps have copied it into TMEM
+        if (n == 2 && !mbar_wait(bar(B_QT), 0, abort_flag, p.status, 0x10c)) break;
         const int kt = list[n] & 0x3FFF;
         mbar_arrive_expect_tx(bar(B_KFULL + st), L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kK + st * L::kTileBytes + x * 16384u, &tmK, x * 64,
                       row0 + kt * 128, bar(B_KFULL + st));
+        if (n >= kStages &&
+            !mbar_wait(bar(B_VEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x10d))
+          break;
         mbar_arrive_expect_tx(bar(B_VFULL + st), L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kV + st * L::kTileBytes + x * 16384u, &tmV, x * 64,
                       row0 + kt * 128, bar(B_VFULL + st));
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idO = make_idesc_bf16(128, D, 0, 1);
-      const uint32_t tO = tmem + 256;
-      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, 0x102);
+      bool ok = mbar_wait(bar(B_QT), 0, abort_flag, p.status, 0x102);
       auto issue_pv = [&](int m) -> bool {
         const int st = m % kStages;
         if (!mbar_wait(bar(B_PFULL), m & 1, abort_flag, p.status, 0x103)) return false;
@@ -184,10 +207,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sV = sbase + L::kV + st * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tO, sdesc_kmajor(sbase + L::kP, kk, 16384u), sdesc_mnmajor(sV, kk, 16384u), idO,
+          umma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_mnmajor(sV, kk, 16384u), idO,
                   (m > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_ODONE));
-        umma_commit(bar(B_KVEMPTY + st));
+        umma_commit(bar(B_VEMPTY + st));
         return true;
       };
       for (int n = 0; ok && n < nt; ++n) {
@@ -200,18 +223,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sK = sbase + L::kK + st * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + sb * 128, sdesc_kmajor(sbase + L::kQ, kk, 16384u),
-                  sdesc_kmajor(sK, kk, 16384u), idS, kk > 0 ? 1u : 0u);
+          umma_ts(tmem + kColS + sb * 128, tmem + kColQ + kk * 8, sdesc_kmajor(sK, kk, 16384u),
+                  idS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL + sb));
+        umma_commit(bar(B_KEMPTY + st));
         if (n >= 1) ok = issue_pv(n - 1);
       }
       if (ok) issue_pv(nt - 1);
     }
   } else {
-    // ---------------------------------------------------------------- softmax warps 0-3
-    const int r = threadIdx.x;  // row within the tile == TMEM lane
+    // ---------------------------------------------------------------- softmax warps 0-7
+    const int quarter = warp & 3;
+    const int hf = warp >> 2;           // column half of S (keys) and of O (head dim)
+    const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
     const int i = qt * 128 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // exchange slot k (k-th use) of this warp pair: write own value, meet the partner, read its
+    auto pair_exchange = [&](int k, float mine, float* other) -> bool {
+      float* slot = red + (k & 1) * 256;
+      slot[hf * 128 + r] = mine;
+      __syncwarp();
+      const uint32_t pb = bar(B_PAIR + 2 * quarter + (k & 1));
+      if (lane == 0) mbar_arrive(pb);
+      const bool got = mbar_wait(pb, (k >> 1) & 1, abort_flag, p.status, 0x10b);
+      __syncwarp();
+      if (got) *other = slot[(hf ^ 1) * 128 + r];
+      return got;
+    };
     int st[4];
     uint32_t len[4];
 #pragma unroll
@@ -224,28 +262,56 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         len[n] = static_cast<uint32_t>(iv.y - iv.x);
       }
     }
+    bool ok = nt > 0;
+    // Q (this warp's half of the row) -> TMEM as bf16 pairs, the A operand of S = Q K^T
+    const bool q_ready = ok && mbar_wait(bar(B_Q), 0, abort_flag, p.status, 0x10a);
+    __syncwarp();
+    if (q_ready) {
+      if (D == 128) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = ld_shared_v4(sbase + L::kQ + hf * 16384u + r * 128u + ((c ^ (r & 7)) << 4));
+          qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kColQ + 32 * hf, qv);
+      } else {
+        uint32_t qv[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t chunk = static_cast<uint32_t>(4 * hf + c);
+          const uint4 v = ld_shared_v4(sbase + L::kQ + r * 128u + ((chunk ^ (r & 7)) << 4));
+          qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
+        }
+        tmem_st16(tmem + lane_off + kColQ + 16 * hf, qv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QT));
+    } else {
+      ok = false;
+    }
+
     float m_run = -INFINITY;
-    float l_run = 0.f;
+    float l_half = 0.f;
     const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int n = 0; n < nt; ++n) {
+    for (int n = 0; ok && n < nt; ++n) {
       const int sb = n & 1;
-      if (!mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x107)) { ok = false; break; }
+      const bool s_ready = mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x107);
+      __syncwarp();
+      if (!s_ready) { ok = false; break; }
       tc_fence_after();
-      float s[128];
+      float s[64];
       {
-        uint32_t t0[32], t1[32], t2[32], t3[32];
-        tmem_ld32(tmem + lane_off + sb * 128 + 0, t0);
-        tmem_ld32(tmem + lane_off + sb * 128 + 32, t1);
-        tmem_ld32(tmem + lane_off + sb * 128 + 64, t2);
-        tmem_ld32(tmem + lane_off + sb * 128 + 96, t3);
+        uint32_t t0[32], t1[32];
+        tmem_ld32(tmem + lane_off + kColS + sb * 128 + 64 * hf, t0);
+        tmem_ld32(tmem + lane_off + kColS + sb * 128 + 64 * hf + 32, t1);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           s[c] = __uint_as_float(t0[c]);
           s[32 + c] = __uint_as_float(t1[c]);
-          s[64 + c] = __uint_as_float(t2[c]);
-          s[96 + c] = __uint_as_float(t3[c]);
         }
       }
       tc_fence_before();
@@ -254,23 +320,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
       const int entry = list[n];
       if (!(entry & 0x8000)) {
-        const int j0 = (entry & 0x3FFF) * 128;
+        const int j0 = (entry & 0x3FFF) * 128 + 64 * hf;
         switch (p.NI) {
-          case 1: mask_partial<1>(s, j0, st, len); break;
-          case 2: mask_partial<2>(s, j0, st, len); break;
-          case 3: mask_partial<3>(s, j0, st, len); break;
-          default: mask_partial<4>(s, j0, st, len); break;
+          case 1: mask_cols<1>(s, j0, st, len); break;
+          case 2: mask_cols<2>(s, j0, st, len); break;
+          case 3: mask_cols<3>(s, j0, st, len); break;
+          default: mask_cols<4>(s, j0, st, len); break;
         }
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
+      for (int c = 4; c < 64; c += 4) {
         mx0 = fmaxf(mx0, s[c]);
         mx1 = fmaxf(mx1, s[c + 1]);
         mx2 = fmaxf(mx2, s[c + 2]);
         mx3 = fmaxf(mx3, s[c + 3]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      // combine with the partner warp (the other column half of the same rows)
+      float mx_other;
+      if (!pair_exchange(n, mx, &mx_other)) { ok = false; break; }
+      mx = fmaxf(mx, mx_other);
+      const float m_tile = mx * sl2;
       float alpha = 1.f;
       if (m_tile > m_run + 8.f) {  // also true when m_run = -inf and the tile has a visible key
         alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
@@ -278,9 +349,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       const float moff = (m_run == -INFINITY) ? 0.f : m_run;
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
+      for (int c = 0; c < 64; c += 4) {
         const float p0 = ex2_approx(fmaf(s[c], sl2, -moff));
         const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -moff));
         const float p2 = ex2_approx(fmaf(s[c + 2], sl2, -moff));
@@ -292,47 +363,48 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         pk[c / 2] = pack_bf16x2(p0, p1);
         pk[c / 2 + 1] = pack_bf16x2(p2, p3);
       }
-      l_run = l_run * alpha + ((l0 + l1) + (l2 + l3));
+      l_half = l_half * alpha + ((l0 + l1) + (l2 + l3));
 
       if (n >= 1) {
-        // PV of the previous tile must be complete: O is stable and the P buffer is free
-        if (!mbar_wait(bar(B_ODONE), (n - 1) & 1, abort_flag, p.status, 0x108)) { ok = false; break; }
+        // PV of the previous tile must be complete: O is stable and the P columns are free
+        const bool o_ready = mbar_wait(bar(B_ODONE), (n - 1) & 1, abort_flag, p.status, 0x108);
+        __syncwarp();
+        if (!o_ready) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < kHalf; c += 32) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + 256 + c, o);
+            tmem_ld32(tmem + lane_off + kColO + hf * kHalf + c, o);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-            tmem_st32(tmem + lane_off + 256 + c, o);
+            tmem_st32(tmem + lane_off + kColO + hf * kHalf + c, o);
           }
-          tmem_wait_st();
         }
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle (two 64-key boxes)
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint32_t box = q >> 3, chunk = q & 7;
-        const uint32_t addr = sbase + L::kP + box * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_st32(tmem + lane_off + kColP + 32 * hf, pk);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
     }
 
     // ---- epilogue: O / l -> bf16, LSE (natural log) ----
-    __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.S + i) * D;
-    if (nt > 0 && ok && mbar_wait(bar(B_ODONE), (nt - 1) & 1, abort_flag, p.status, 0x109)) {
+    __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.S + i) * D + hf * kHalf;
+    float l_tot = 0.f;
+    float l_other = 0.f;
+    bool o_final = ok && mbar_wait(bar(B_ODONE), (nt - 1) & 1, abort_flag, p.status, 0x109);
+    __syncwarp();
+    if (o_final) o_final = pair_exchange(nt, l_half, &l_other);
+    if (o_final) {
+      l_tot = l_half + l_other;
       tc_fence_after();
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < kHalf; c += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + 256 + c, o);
+        tmem_ld32(tmem + lane_off + kColO + hf * kHalf + c, o);
         tmem_wait_ld();
         uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
@@ -347,18 +419,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
     } else {
       uint4* dst = reinterpret_cast<uint4*>(orow);
-      for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
-      l_run = 0.f;
+      for (int q = 0; q < kHalf / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
     }
-    p.lse[static_cast<size_t>(bh) * p.S + i] =
-        l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    if (hf == 0)
+      p.lse[static_cast<size_t>(bh) * p.S + i] =
+          l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace fwd

@@ -234,31 +234,62 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
   }
 }
 
-// Longest-first order of tile rows: rank = #rows with more non-empty tiles, ties by index.
+// Longest-first order of tile rows by counting sort on the number of non-empty tiles (0..NT):
+// histogram, descending exclusive scan, then placement.  Rows with equal counts may come in any
+// order.  One block of 1024 threads per direction; NT <= 1024.
+__device__ __forceinline__ int row_tile_count(const uint32_t* bm, int it, int W) {
+  int c = 0;
+  for (int w = 0; w < W; ++w) {
+    const uint32_t x = bm[static_cast<size_t>(it) * W + w];
+    c += __popc((x | (x >> 1)) & 0x55555555u);
+  }
+  return c;
+}
+
 __global__ void __launch_bounds__(1024) schedule_kernel(const uint32_t* bm_f, const uint32_t* bm_b,
                                                         int32_t* sched_f, int32_t* sched_b, int B,
                                                         int NT, int W) {
-  extern __shared__ int cnt[];
+  __shared__ int hist[1025];
+  __shared__ int wsum[32];
   const uint32_t* bm = blockIdx.x == 0 ? bm_f : bm_b;
   int32_t* sched = blockIdx.x == 0 ? sched_f : sched_b;
   const int n = B * NT;
-  for (int it = threadIdx.x; it < n; it += blockDim.x) {
-    int c = 0;
-    for (int w = 0; w < W; ++w) {
-      const uint32_t x = bm[static_cast<size_t>(it) * W + w];
-      c += __popc((x | (x >> 1)) & 0x55555555u);
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  for (int c = t; c <= NT; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  for (int it = t; it < n; it += blockDim.x) atomicAdd(&hist[row_tile_count(bm, it, W)], 1);
+  __syncthreads();
+  // thread t owns count NT - t (t < NT): inclusive scan in descending count order
+  const int c = NT - t;
+  const int v = t < NT ? hist[c] : 0;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+    int e = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, e, o);
+      if (lane >= o) e += y;
     }
-    cnt[it] = c;
+    wsum[lane] = e - w;  // exclusive prefix of the warp totals
   }
   __syncthreads();
-  for (int it = threadIdx.x; it < n; it += blockDim.x) {
-    const int c = cnt[it];
-    int rank = 0;
-    for (int j = 0; j < n; ++j) {
-      const int cj = cnt[j];
-      rank += (cj > c) || (cj == c && j < it);
-    }
-    sched[rank] = ((it / NT) << 16) | (it % NT);
+  const int incl = x + wsum[warp];
+  __syncthreads();
+  if (t < NT) hist[c] = incl - v;  // first slot of count c
+  if (t == NT - 1) hist[0] = incl;  // rows without tiles go last
+  __syncthreads();
+  for (int it = t; it < n; it += blockDim.x) {
+    const int pos = atomicAdd(&hist[row_tile_count(bm, it, W)], 1);
+    sched[pos] = ((it / NT) << 16) | (it % NT);
   }
 }
 
@@ -291,13 +322,8 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const int32_t* seg
   }
   descriptor_kernel<<<2 * B * p.NT, kTile, smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  const size_t smem2 = static_cast<size_t>(B) * p.NT * 4;
-  if (smem2 > 48 * 1024) {
-    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem2)) != cudaSuccess)
-      return -1;
-  }
-  schedule_kernel<<<2, 1024, smem2, stream>>>(bm_f, bm_b, sched_f, sched_b, B, p.NT, p.W);
+  if (p.NT > 1024) return -1;
+  schedule_kernel<<<2, 1024, 0, stream>>>(bm_f, bm_b, sched_f, sched_b, B, p.NT, p.W);
   if (cudaGetLastError() != cudaSuccess) return -1;
   return 0;
 }
