@@ -133,7 +133,8 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
                        void* o, float* lse, int B, int H, int S, int d, float scale,
                        void* stream);
 
-/* Workspace bytes cm_attn_bwd needs (fp32 dQ accumulator and per-row D = rowsum(dO * O)). */
+/* Workspace bytes cm_attn_bwd needs: per-row D = rowsum(dO * O) and LSE * log2(e) (fp32), and the
+ * fp32 dQ accumulator. */
 CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes);
 
 /* Backward: dq, dk, dv (device bf16 [B][H][S][d]) of sum(o * dO) given the forward's o and lse.
@@ -156,7 +157,7 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
  * scratch comes from a fixed file-scope device array inside the library instead, so this call
  * allocates nothing.
  *   - Limit: the workspace cm_attn_bwd_workspace_size reports must fit CM_NOALLOC_SCRATCH_BYTES
- *     (e.g. B*H*S <= 65027 rows at d = 128); larger problems return CM_ERR_UNSUPPORTED and queue
+ *     (e.g. B*H*S <= 64527 rows at d = 128); larger problems return CM_ERR_UNSUPPORTED and queue
  *     nothing.
  *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call on each
  *     device, with that device current; make that first call before any stream capture.

@@ -125,8 +125,8 @@ CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes)
   if (!bytes || B < 1 || H < 1 || S < 1) return CM_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
   const size_t rows = static_cast<size_t>(B) * H * S;
-  const size_t delta = (rows * 4 + 255) / 256 * 256;
-  *bytes = delta + rows * d * 4;
+  const size_t row_floats = (rows * 4 + 255) / 256 * 256;  // D, then LSE * log2(e)
+  *bytes = 2 * row_floats + rows * d * 4;
   return CM_OK;
 }
 
@@ -150,15 +150,16 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   if (workspace_bytes < need) return CM_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return CM_ERR_INVALID_ARG;
   const size_t rows = static_cast<size_t>(B) * H * S;
-  const size_t delta_bytes = (rows * 4 + 255) / 256 * 256;
+  const size_t row_floats = (rows * 4 + 255) / 256 * 256;
   cm::BwdParams p;
   p.itab = desc->itab_b;
   p.bm = desc->bm_b;
   p.sched = desc->sched_b;
   p.status = desc->status;
   p.lse = lse;
-  p.delta = static_cast<const float*>(workspace);
-  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes);
+  p.delta = static_cast<float*>(workspace);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + row_floats);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * row_floats);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.B = B;

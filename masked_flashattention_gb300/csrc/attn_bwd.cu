@@ -6,27 +6,26 @@
 //
 //   S^T  = K Q^T            (tcgen05, TMEM)        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
 //   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
-//   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
 //   dK  += dS^T Q           (TMEM accumulator)
+//   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
 //   dQ_part = dS K          (TMEM) -> shared memory -> TMA bulk add into the fp32 dQ accumulator
 //
 // Partial tiles check each query index against the key column's intervals with the unsigned
-// test of section 4.4 and zero P there (the -inf of the forward).  Empty tiles are never visited.
+// test of section 4.4 and zero P there (the -inf of the forward); full tiles skip the check.
+// Empty tiles are never visited.
 //
 // Warp roles (320 threads):
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
 //              half w / 4: queries [64*half, +64) of S^T / dP^T, and head-dim columns
 //              [half*d/2, +d/2) of dQ_part, dV and dK.
-//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE by bulk copy) into one slot and
-//              dO (+ D) into two slots, so the next tile's dO is in flight during this tile.
-//   warp 9     MMA issuer (one thread).  Per query tile: S^T, dP^T; then dK first (its
-//              completion frees Q for the next tile), dV, and dQ_part.
+//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) and dO (+ D).
+//   warp 9     MMA issuer (one thread).  Per query tile: S^T, dP^T; then dK (its completion
+//              frees Q for the next tile), dV (frees dO), and dQ_part.
 // TMEM (512 columns): dV [0, d), dK [128, 128+d), R1 [256, 384) = S^T, overwritten in place by
 // the bf16 P^T pairs (each warp writes only columns it has already read), R2 [384, 512) = dP^T,
 // then dQ_part.
-// Shared memory: K, V, Q, dO x2 (bf16, 128-byte swizzle); the dS^T tile, whose box h also serves
-// as column half h's fp32 staging tile for the dQ bulk add once the MMAs reading dS^T are done;
-// LSE and D x2 of the query tiles.
+// Shared memory: K, V, Q, dO, dS^T (bf16, 128-byte swizzle), one 16 KB fp32 staging tile per
+// column half for the dQ bulk add, LSE*log2e and D of the current query tile.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -50,19 +49,20 @@ constexpr uint32_t kColDK = 128;
 constexpr uint32_t kColR1 = 256;
 constexpr uint32_t kColR2 = 384;
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 template <int D>
 struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTileBytes;
   static constexpr uint32_t kQ = 2 * kTileBytes;
-  static constexpr uint32_t kdO = 3 * kTileBytes;   // two slots
-  // dS^T [2 boxes][128 keys][64 queries] bf16; once the MMAs that read it are done, box h is the
-  // fp32 [128 rows][32 cols] staging tile of column half h for the dQ bulk add
-  static constexpr uint32_t kdSt = 5 * kTileBytes;
-  static constexpr uint32_t kLse = kdSt + 32768u;   // 128 floats (with Q)
-  static constexpr uint32_t kDelta = kLse + 512u;   // two slots of 128 floats (with dO)
-  static constexpr uint32_t kBar = kDelta + 1024u;
+  static constexpr uint32_t kdO = 3 * kTileBytes;
+  static constexpr uint32_t kdSt = 4 * kTileBytes;   // [2 boxes][128 keys][64 queries] bf16
+  static constexpr uint32_t kStage = kdSt + 32768u;  // fp32 [2 halves][128 rows][32 cols]
+  static constexpr uint32_t kLse2 = kStage + 32768u; // 128 floats: -LSE * log2(e)
+  static constexpr uint32_t kDelta = kLse2 + 512u;   // 128 floats: -D
+  static constexpr uint32_t kBar = kDelta + 512u;
   static constexpr uint32_t kList = kBar + 256u;
   static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
   static constexpr uint32_t kAlloc = kTotal + 1024u;
@@ -70,17 +70,17 @@ struct Smem {
 
 enum {
   B_KV = 0,       // K and V loaded
-  B_QFULL = 1,    // Q and LSE of the current query tile loaded
+  B_QFULL = 1,    // Q and LSE*log2e of the current query tile loaded
   B_QEMPTY = 2,   // the dK MMA (last reader of Q) of the current tile is done
-  B_DOFULL = 3,   // +slot: dO and D of a query tile loaded
-  B_DOEMPTY = 5,  // +slot: the dV MMA (last reader of the dO slot) is done
-  B_SFULL = 7,    // S^T and dP^T computed
-  B_PDS = 8,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
-  B_DQFULL = 9,   // dQ_part computed (and every MMA of the tile done)
-  B_DQREAD = 10,  // compute warps read dQ_part from TMEM (8 arrivals)
-  B_STGFREE = 11, // +half: the half's box of the dS^T buffer may be written (leader, 1 arrival)
-  B_STGFULL = 13, // +half: the half's 4 warps wrote their staging rows (4 arrivals)
-  B_COUNT = 15
+  B_DOFULL = 3,   // dO and D of the current query tile loaded
+  B_DOEMPTY = 4,  // the dV MMA (last reader of dO) of the current tile is done
+  B_SFULL = 5,    // S^T and dP^T computed
+  B_PDS = 6,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
+  B_DQFULL = 7,   // dQ_part computed (and every MMA of the tile done)
+  B_DQREAD = 8,   // compute warps read dQ_part from TMEM (8 arrivals)
+  B_STGFREE = 9,  // +half: the half's staging tile may be written (its leader, 1 arrival)
+  B_STGFULL = 11, // +half: the half's 4 warps wrote their staging rows (4 arrivals)
+  B_COUNT = 13
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -89,6 +89,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 template <int NI>
@@ -104,6 +112,44 @@ __device__ __forceinline__ uint32_t visible_bits(int i0, const int (&st)[4], con
     bits |= vis ? (1u << c) : 0u;
   }
   return bits;
+}
+
+// P^T and dS^T of 32 queries of this key row.  For a full tile every query is visible; for a
+// partial tile `vis` holds the visibility bits.
+template <bool FULL>
+__device__ __forceinline__ void chunk_p_ds(const uint32_t (&sr)[32], const uint32_t (&dpr)[32],
+                                           uint32_t lse2_addr, uint32_t delta_addr, float sl2,
+                                           uint32_t vis, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+  // shared memory holds -LSE*log2e and -D per query, so both steps are paired FMAs / adds:
+  // x = s * scale*log2e + (-lse2),  p = exp2(x),  g = dp + (-D),  ds = p * g
+  const float2 scale2 = make_float2(sl2, sl2);
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 l4 = ld_shared_f4(lse2_addr + c * 4u);
+    const float4 d4 = ld_shared_f4(delta_addr + c * 4u);
+    const float2 xa = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2,
+                           make_float2(l4.x, l4.y));
+    const float2 xb = fma2(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
+                           scale2, make_float2(l4.z, l4.w));
+    float2 pa = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+    float2 pb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
+    if (!FULL) {
+      pa.x = ((vis >> c) & 1u) ? pa.x : 0.f;
+      pa.y = ((vis >> (c + 1)) & 1u) ? pa.y : 0.f;
+      pb.x = ((vis >> (c + 2)) & 1u) ? pb.x : 0.f;
+      pb.y = ((vis >> (c + 3)) & 1u) ? pb.y : 0.f;
+    }
+    const float2 ga = add2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])),
+                           make_float2(d4.x, d4.y));
+    const float2 gb = add2(make_float2(__uint_as_float(dpr[c + 2]), __uint_as_float(dpr[c + 3])),
+                           make_float2(d4.z, d4.w));
+    const float2 dsa = mul2(pa, ga);
+    const float2 dsb = mul2(pb, gb);
+    pp[c / 2] = pack_bf16x2(pa.x, pa.y);
+    pp[c / 2 + 1] = pack_bf16x2(pb.x, pb.y);
+    dd[c / 2] = pack_bf16x2(dsa.x, dsa.y);
+    dd[c / 2 + 1] = pack_bf16x2(dsb.x, dsb.y);
+  }
 }
 
 template <int D>
@@ -123,8 +169,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
-  const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
-  const float* s_delta = reinterpret_cast<const float*>(smem + L::kDelta);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -140,10 +184,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_KV), 1);
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    for (int sl = 0; sl < 2; ++sl) {
-      mbar_init(bar(B_DOFULL + sl), 1);
-      mbar_init(bar(B_DOEMPTY + sl), 1);
-    }
+    mbar_init(bar(B_DOFULL), 1);
+    mbar_init(bar(B_DOEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DQFULL), 1);
@@ -195,38 +237,32 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       for (int m = 0; m < nt; ++m) {
         const int qt = list[m] & 0x3FFF;
-        const int ds = m & 1;
-        // dO and D: two slots, so the next tile's are in flight while this tile computes
-        if (m >= 2 && !mbar_wait(bar(B_DOEMPTY + ds), ((m >> 1) - 1) & 1, abort_flag, p.status, 0x201))
-          break;
-        mbar_arrive_expect_tx(bar(B_DOFULL + ds), L::kTileBytes + 512u);
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kdO + ds * L::kTileBytes + x * 16384u, &tmdO, x * 64,
-                      row0 + qt * 128, bar(B_DOFULL + ds));
-        bulk_load(sbase + L::kDelta + ds * 512u, p.delta + static_cast<size_t>(row0) + qt * 128,
-                  512u, bar(B_DOFULL + ds));
-        // Q and LSE: one slot, refilled as soon as the dK MMA of the previous tile is done
-        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x20b)) break;
+        const size_t r = static_cast<size_t>(row0) + qt * 128;
+        // Q is free once the previous tile's dK MMA is done, dO once its dV MMA is done
+        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x201)) break;
         mbar_arrive_expect_tx(bar(B_QFULL), L::kTileBytes + 512u);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QFULL));
-        bulk_load(sbase + L::kLse, p.lse + static_cast<size_t>(row0) + qt * 128, 512u, bar(B_QFULL));
+        bulk_load(sbase + L::kLse2, p.lse2 + r, 512u, bar(B_QFULL));
+        if (m >= 1 && !mbar_wait(bar(B_DOEMPTY), (m - 1) & 1, abort_flag, p.status, 0x20b)) break;
+        mbar_arrive_expect_tx(bar(B_DOFULL), L::kTileBytes + 512u);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kdO + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_DOFULL));
+        bulk_load(sbase + L::kDelta, p.delta + r, 512u, bar(B_DOFULL));
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dV (TS), dK
+      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV (TS)
       constexpr uint32_t idMM = make_idesc_bf16(128, D, 1, 1);    // dQ_part
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ,
-                     sdSt = sbase + L::kdSt;
+                     sdO = sbase + L::kdO, sdSt = sbase + L::kdSt;
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202);
       for (int m = 0; ok && m < nt; ++m) {
-        const int ds = m & 1;
-        const uint32_t sdO = sbase + L::kdO + ds * L::kTileBytes;
         if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x203)) break;
-        if (!mbar_wait(bar(B_DOFULL + ds), (m >> 1) & 1, abort_flag, p.status, 0x20c)) break;
+        if (!mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20c)) break;
         // dQ_part of the previous tile has been read out of R2, which also means every MMA of the
         // previous tile (including the dV that read P^T from R1) has completed
         if (m >= 1 && !mbar_wait(bar(B_DQREAD), (m - 1) & 1, abort_flag, p.status, 0x204)) break;
@@ -246,13 +282,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
                   (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY));  // Q may be refilled once dK is done
+        umma_commit(bar(B_QEMPTY));
         // P^T pairs: queries [0,64) at R1 columns [0,32), queries [64,128) at [64,96)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + kColDV, tmem + kColR1 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                   sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DOEMPTY + ds));
+        umma_commit(bar(B_DOEMPTY));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + kColR2, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
@@ -267,8 +303,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_part)
     const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool leader = (quarter == 0 && lane == 0);           // issues this half's bulk adds
-    const uint32_t stage = sbase + L::kdSt + hf * 16384u;  // this half's dS^T box / dQ staging
+    const bool leader = (quarter == 0 && lane == 0);  // issues this half's bulk adds
+    const uint32_t stage = sbase + L::kStage + hf * 16384u;
     int st[4];
     uint32_t len[4];
 #pragma unroll
@@ -282,25 +318,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
     }
     const float sl2 = p.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;
     for (int m = 0; ok && m < nt; ++m) {
       const int entry = list[m];
       const int qt = entry & 0x3FFF;
       const bool full = (entry & 0x8000) != 0;
-      const int ds = m & 1;
-      const float* s_dlt = s_delta + ds * 128;
       bool ready = mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206) &&
                    mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x207) &&
-                   mbar_wait(bar(B_DOFULL + ds), (m >> 1) & 1, abort_flag, p.status, 0x20d);
-      // this half's dS^T box is also the staging tile of the previous tile's dQ bulk adds: wait
-      // until those have stopped reading it (use uf of the box)
-      const int uf0 = m * (1 + kChunks);
-      if (leader) {
-        bulk_wait_read_all();
-        mbar_arrive(bar(B_STGFREE + hf));
-      }
-      ready = mbar_wait(bar(B_STGFREE + hf), uf0 & 1, abort_flag, p.status, 0x20e) && ready;
+                   mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20d);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -312,33 +337,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_ld32(tmem + lane_off + kColR1 + q0, sr);
         tmem_ld32(tmem + lane_off + kColR2 + q0, dpr);
         tmem_wait_ld();
-        uint32_t vis = 0xFFFFFFFFu;
-        if (!full) {
+        uint32_t pp[16], dd[16];
+        const uint32_t la = sbase + L::kLse2 + q0 * 4u, da = sbase + L::kDelta + q0 * 4u;
+        if (full) {
+          chunk_p_ds<true>(sr, dpr, la, da, sl2, 0u, pp, dd);
+        } else {
           const int i0 = qt * 128 + q0;
+          uint32_t vis;
           switch (p.NI) {
             case 1: vis = visible_bits<1>(i0, st, len); break;
             case 2: vis = visible_bits<2>(i0, st, len); break;
             case 3: vis = visible_bits<3>(i0, st, len); break;
             default: vis = visible_bits<4>(i0, st, len); break;
           }
-        }
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = q0 + c + e;
-            const float lse = s_lse[q];
-            // a query row that sees nothing has lse = -inf: its P is 0
-            const float off = lse == -INFINITY ? INFINITY : lse * kLog2e;
-            float pr = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -off));
-            pr = ((vis >> (c + e)) & 1u) ? pr : 0.f;
-            pv[e] = pr;
-            dv[e] = pr * (__uint_as_float(dpr[c + e]) - s_dlt[q]);
-          }
-          pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
-          dd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+          chunk_p_ds<false>(sr, dpr, la, da, sl2, vis, pp, dd);
         }
         // P^T pairs into R1 columns this warp has already read: hf * 64 + ch * 16
         tmem_st16(tmem + lane_off + kColR1 + hf * 64 + ch * 16, pp);
@@ -371,14 +383,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_DQREAD));  // R2 may be overwritten now
         }
-        // use uf of this half's box: wait until the previous bulk add stopped reading it
-        const int uf = uf0 + 1 + cc;
+        // use u of this half's staging tile: wait until the previous bulk add stopped reading it
         const int u = m * kChunks + cc;
         if (leader) {
           bulk_wait_read_all();
           mbar_arrive(bar(B_STGFREE + hf));
         }
-        const bool free_ok = mbar_wait(bar(B_STGFREE + hf), uf & 1, abort_flag, p.status, 0x209);
+        const bool free_ok = mbar_wait(bar(B_STGFREE + hf), u & 1, abort_flag, p.status, 0x209);
         __syncwarp();
         if (!free_ok) { ok = false; break; }
 #pragma unroll
@@ -449,11 +460,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// D_i = sum_c dO[i][c] * O[i][c] (fp32) and zero the dQ accumulator row.  One warp per row.
+// Per row, negated for the main kernel's paired FMAs: -D = -sum_c dO[c] * O[c] (fp32) and
+// -LSE * log2(e) (-inf for a row that sees nothing, so that its P is exp2(-inf) = 0); and a zeroed
+// dQ accumulator row.  One warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* o,
-                                                           const __nv_bfloat16* d_o, float* delta,
-                                                           float* dq_acc, size_t rows) {
+                                                           const __nv_bfloat16* d_o,
+                                                           const float* lse, float* delta,
+                                                           float* lse2, float* dq_acc,
+                                                           size_t rows) {
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -465,7 +480,11 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* 
   for (int e = 0; e < kPer; ++e) acc += __bfloat162float(a[e]) * __bfloat162float(g[e]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  if (lane == 0) delta[row] = acc;
+  if (lane == 0) {
+    delta[row] = -acc;
+    const float l = lse[row];
+    lse2[row] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+  }
   float* z = dq_acc + row * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) z[e] = 0.f;
@@ -491,17 +510,17 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* dq_acc, __
 int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
                     const void* o, const void* d_o, void* dq, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
-  // prologue: D and zeroed accumulator
+  // prologue: D, LSE * log2(e) and the zeroed accumulator
   {
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
     if (d == 128)
       bwd::bwd_prologue_kernel<128><<<blocks, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o),
-          const_cast<float*>(p.delta), p.dq_acc, rows);
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
+          p.delta, p.lse2, p.dq_acc, rows);
     else
       bwd::bwd_prologue_kernel<64><<<blocks, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o),
-          const_cast<float*>(p.delta), p.dq_acc, rows);
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
+          p.delta, p.lse2, p.dq_acc, rows);
     if (cudaGetLastError() != cudaSuccess) return -1;
   }
   CUtensorMap mq, mk, mv, mdo, mdq;

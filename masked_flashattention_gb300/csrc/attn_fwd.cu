@@ -328,15 +328,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           default: mask_cols<4>(s, j0, st, len); break;
         }
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[32], s[33]);
 #pragma unroll
-      for (int c = 4; c < 64; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 2; c < 32; c += 2) {
+        mx0 = max3f(mx0, s[c], s[c + 1]);
+        mx1 = max3f(mx1, s[32 + c], s[33 + c]);
       }
-      float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      float mx = fmaxf(mx0, mx1);
       // combine with the partner warp (the other column half of the same rows)
       float mx_other;
       if (!pair_exchange(n, mx, &mx_other)) { ok = false; break; }
@@ -348,22 +346,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m_run = m_tile;
       }
       const float moff = (m_run == -INFINITY) ? 0.f : m_run;
-      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      // p = exp2(s * scale * log2e - m), two scores per paired FMA; row sums in paired adds
+      const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-moff, -moff);
+      float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float p0 = ex2_approx(fmaf(s[c], sl2, -moff));
-        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -moff));
-        const float p2 = ex2_approx(fmaf(s[c + 2], sl2, -moff));
-        const float p3 = ex2_approx(fmaf(s[c + 3], sl2, -moff));
-        l0 += p0;
-        l1 += p1;
-        l2 += p2;
-        l3 += p3;
-        pk[c / 2] = pack_bf16x2(p0, p1);
-        pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+        const float2 xa = fma2(make_float2(s[c], s[c + 1]), scale2, neg_m2);
+        const float2 xb = fma2(make_float2(s[c + 2], s[c + 3]), scale2, neg_m2);
+        const float2 pa = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+        const float2 pb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
+        lsa = add2(lsa, pa);
+        lsb = add2(lsb, pb);
+        pk[c / 2] = pack_bf16x2(pa.x, pa.y);
+        pk[c / 2 + 1] = pack_bf16x2(pb.x, pb.y);
       }
-      l_half = l_half * alpha + ((l0 + l1) + (l2 + l3));
+      l_half = l_half * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
       if (n >= 1) {
         // PV of the previous tile must be complete: O is stable and the P columns are free

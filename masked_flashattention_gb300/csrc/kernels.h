@@ -28,8 +28,9 @@ struct BwdParams {
   const uint32_t* bm;    // backward bitmaps [B][NT][W]
   const int32_t* sched;  // (b << 16 | k_tile), longest first
   int32_t* status;
-  const float* lse;      // [B][H][S] natural log
-  const float* delta;    // [B][H][S] rowsum(dO * O)
+  const float* lse;      // [B][H][S] natural log (forward output)
+  float* delta;          // [B][H][S] -rowsum(dO * O), written by the prologue
+  float* lse2;           // [B][H][S] -LSE * log2(e) (-inf for rows that see nothing), prologue
   float* dq_acc;         // [B][H][S][d] fp32
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
