@@ -157,7 +157,9 @@ def run_reference(args):
         return 0
     from masked_flashattention_gb300 import workloads as W
     w = W.WORKLOADS[args.config]
-    rows = args.ref_rows
+    # each step is a bounded sample: about 8192 rows x 33 steps of CPU work in total (a few
+    # minutes on the GB300 host), whatever K and W are
+    rows = args.ref_rows or max(256, min(w.S, (8192 * 33) // max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(args.config, rows)
     times, pairs, cores, desc = [], 0, 0, ""
@@ -396,7 +398,7 @@ def run_gpu(args):
             "clocks": clk,
         }
         if world == 1 and not args.no_cpu_baseline:
-            dt, pr, cores, sdesc = oracle_sample(args.config, args.ref_rows)
+            dt, pr, cores, sdesc = oracle_sample(args.config, args.ref_rows or 8192)
             line["cpu_baseline"] = {"value": FLOPS_PER_PAIR_PER_D * d * pr / dt / 1e12,
                                     "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": sdesc}
@@ -413,7 +415,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=3, help="workload 1..5 (default: 3, RM 32K)")
     ap.add_argument("--impl", default="cm", choices=["cm", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=8192)
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="query rows of the oracle sample (default: sized to the run length)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

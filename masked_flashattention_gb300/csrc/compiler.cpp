@@ -626,7 +626,19 @@ struct Emitter {
       case EK::Nseg: op(OP_NSEG); break;
       case EK::Min: lin(a.args[0]); lin(a.args[1]); op(OP_MIN); break;
       case EK::Max: lin(a.args[0]); lin(a.args[1]); op(OP_MAX); break;
-      case EK::SegIdx: lin(a.args[0]); op(OP_SEG_IDX); break;
+      case EK::SegIdx: {
+        // seg_idx(i) is the common case: the evaluator computes it once per row
+        const Lin& x = a.args[0];
+        const bool row_itself = x.c == 0 && x.t.size() == 1 && x.t.begin()->second.first == 1 &&
+                                x.t.begin()->second.second->kind == EK::I;
+        if (row_itself) {
+          op(OP_SEG_IDX_I);
+        } else {
+          lin(x);
+          op(OP_SEG_IDX);
+        }
+        break;
+      }
       case EK::SegStartAt: lin(a.args[0]); op(OP_SEG_START_AT); break;
       case EK::SegEndAt: lin(a.args[0]); op(OP_SEG_END_AT); break;
       default: throw CompileError("internal: j in an endpoint");
@@ -665,7 +677,7 @@ int max_depth(const std::vector<int32_t>& code, int start) {
     switch (code[p]) {
       case OP_END: return m;
       case OP_CONST: ++d; ++p; break;
-      case OP_I: case OP_S: case OP_NSEG: ++d; break;
+      case OP_I: case OP_S: case OP_NSEG: case OP_SEG_IDX_I: ++d; break;
       case OP_ADD: case OP_SUB: case OP_MIN: case OP_MAX: case OP_AND: case OP_OR: --d; break;
       case OP_CMP: --d; ++p; break;
       case OP_MULC: ++p; break;

@@ -8,11 +8,11 @@
 //      endpoints (stack programs from the compiler), clamps them to [0, S] and stores every slot
 //      as (start, end), writing (0, 0) for padding, failed conditions and empty intervals;
 //      stores are 8-byte and coalesced (slot-major layout [b][slot][row]);
-//   3. tile states: each row marks the other-index tiles its intervals touch ("any") and the
-//      tiles its merged intervals cover completely ("all"); warp OR/AND reductions and a
-//      4-warp merge in shared memory give, per tile, empty (no row touches it), full (every row
-//      covers it) or partial.  A union of adjacent or overlapping slots counts as covering, so
-//      the states equal those of the dense mask exactly.
+//   3. tile states: each row adds its touched tile ranges ("any") and the tile ranges its merged
+//      intervals cover completely ("all") to two shared-memory difference arrays; a prefix sum
+//      over the tiles gives, per tile, empty (no row touches it), full (all 128 rows cover it)
+//      or partial.  A union of adjacent or overlapping slots counts as covering, so the states
+//      equal those of the dense mask exactly.
 // A second small launch orders the tile rows longest first (LPT) for the attention kernels.
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -34,7 +34,6 @@ struct PrepParams {
   int32_t* status;
   int nseg_max;
   int B, S, NT, W;  // NT tiles per row; W = ceil(NT / 16) bitmap words per tile row
-  int NW32;         // ceil(NT / 32) words of the per-row tile bitsets
 };
 
 __device__ __forceinline__ int seg_index(const int* seg_s, int nseg, int e) {
@@ -51,7 +50,8 @@ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 
 // Evaluate one endpoint program.  Arithmetic wraps (unsigned) instead of overflowing.
-__device__ int eval_prog(const int32_t* code, int pc, int row, const int* seg_s, int nseg, int S) {
+__device__ int eval_prog(const int32_t* code, int pc, int row, int row_seg, const int* seg_s,
+                         int nseg, int S) {
   int st[kMaxStack];
   int sp = 0;
 #define PUSH(x)                          \
@@ -67,6 +67,7 @@ __device__ int eval_prog(const int32_t* code, int pc, int row, const int* seg_s,
       case OP_I: PUSH(row); break;
       case OP_S: PUSH(S); break;
       case OP_NSEG: PUSH(nseg); break;
+      case OP_SEG_IDX_I: PUSH(row_seg); break;
       case OP_MULC: TOP = static_cast<int>(static_cast<unsigned>(TOP) * static_cast<unsigned>(code[pc])); ++pc; break;
       case OP_NEG: TOP = static_cast<int>(0u - static_cast<unsigned>(TOP)); break;
       case OP_NOT: TOP = (TOP == 0); break;
@@ -106,15 +107,6 @@ __device__ int eval_prog(const int32_t* code, int pc, int row, const int* seg_s,
   return 0;
 }
 
-// bits of tiles [a, b) that fall in 32-tile word w
-__device__ __forceinline__ uint32_t range_bits(int a, int b, int w) {
-  const int lo = imax(a - 32 * w, 0);
-  const int hi = imin(b - 32 * w, 32);
-  if (hi <= lo) return 0u;
-  const uint32_t upper = hi == 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
-  return upper & ~((1u << lo) - 1u);
-}
-
 __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant__ PrepParams p) {
   extern __shared__ int smem_i[];
   const int per_dir = p.B * p.NT;
@@ -124,16 +116,19 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
   const int tile = rem % p.NT;
   const DevProg& prog = p.prog[dir];
 
-  int* seg_s = smem_i;                                   // [nseg_max + 1]
-  uint32_t* s_any = reinterpret_cast<uint32_t*>(smem_i + p.nseg_max + 1);  // [4][NW32]
-  uint32_t* s_all = s_any + 4 * p.NW32;                  // [4][NW32]
+  int* seg_s = smem_i;                         // [nseg_max + 1]
+  int* cnt_any = smem_i + p.nseg_max + 1;      // [NT + 1] difference array: rows touching tile
+  int* cnt_all = cnt_any + p.NT + 1;           // [NT + 1] difference array: rows covering tile
+  uint8_t* code = reinterpret_cast<uint8_t*>(cnt_all + p.NT + 1);  // [NT] 2-bit state per tile
   __shared__ int s_bad;
+  __shared__ int s_wtot[2][kTile / 32];
 
   const int t = threadIdx.x;
   int nseg = p.nseg[b];
   if (t == 0) s_bad = (nseg < 1 || nseg > p.nseg_max);
   nseg = imin(imax(nseg, 1), p.nseg_max);
   for (int k = t; k <= p.nseg_max; k += blockDim.x) seg_s[k] = p.seg[b * (p.nseg_max + 1) + k];
+  for (int k = t; k < 2 * (p.NT + 1); k += blockDim.x) cnt_any[k] = 0;
   __syncthreads();
   // metadata validation: seg[0] = 0, strictly increasing, seg[nseg] = S
   bool bad = false;
@@ -145,9 +140,10 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
 
   // --- 1. endpoints -------------------------------------------------------------------------
   const int row = tile * kTile + t;
+  const int row_seg = seg_index(seg_s, nseg, row);
   int region = -1;
   for (int r = 0; r < prog.nreg; ++r) {
-    if (eval_prog(prog.code, prog.guard[r], row, seg_s, nseg, p.S) != 0) {
+    if (eval_prog(prog.code, prog.guard[r], row, row_seg, seg_s, nseg, p.S) != 0) {
       region = r;
       break;
     }
@@ -159,9 +155,9 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
     hi[n] = 0;
     if (n < prog.ni && region >= 0 && n < prog.nslot[region]) {
       const int c = prog.cond[region][n];
-      if (c < 0 || eval_prog(prog.code, c, row, seg_s, nseg, p.S) != 0) {
-        int a = eval_prog(prog.code, prog.lo[region][n], row, seg_s, nseg, p.S);
-        int e = eval_prog(prog.code, prog.hi[region][n], row, seg_s, nseg, p.S);
+      if (c < 0 || eval_prog(prog.code, c, row, row_seg, seg_s, nseg, p.S) != 0) {
+        int a = eval_prog(prog.code, prog.lo[region][n], row, row_seg, seg_s, nseg, p.S);
+        int e = eval_prog(prog.code, prog.hi[region][n], row, row_seg, seg_s, nseg, p.S);
         a = imin(imax(a, 0), p.S);
         e = imin(imax(e, 0), p.S);
         if (e > a) {
@@ -200,21 +196,59 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
     }
   }
 
-  // --- 3. tile states -----------------------------------------------------------------------
-  const int warp = t >> 5;
-  for (int w = 0; w < p.NW32; ++w) {
-    uint32_t any_b = 0, all_b = 0;
+  // --- 3. tile states ---------------------------------------------------------------------
+  // Each row adds +1 / -1 at the ends of its touched tile ranges (any slot) and of its fully
+  // covered tile ranges (merged intervals, which are disjoint, so a row counts once per tile).
+  // After a prefix sum, a tile is touched by some row iff its "any" count is > 0, and full iff
+  // its "all" count equals the 128 rows of the tile.
 #pragma unroll
-    for (int n = 0; n < kMaxSlots; ++n) {
-      if (hi[n] > lo[n]) any_b |= range_bits(lo[n] / kTile, (hi[n] - 1) / kTile + 1, w);
-      if (ms[n] != 0x7FFFFFFF) all_b |= range_bits((ms[n] + kTile - 1) / kTile, me[n] / kTile, w);
+  for (int n = 0; n < kMaxSlots; ++n) {
+    if (hi[n] > lo[n]) {
+      atomicAdd(&cnt_any[lo[n] / kTile], 1);
+      atomicAdd(&cnt_any[(hi[n] - 1) / kTile + 1], -1);
     }
-    any_b = __reduce_or_sync(0xFFFFFFFFu, any_b);
-    all_b = __reduce_and_sync(0xFFFFFFFFu, all_b);
-    if ((t & 31) == 0) {
-      s_any[warp * p.NW32 + w] = any_b;
-      s_all[warp * p.NW32 + w] = all_b;
+    if (ms[n] != 0x7FFFFFFF) {
+      const int a = (ms[n] + kTile - 1) / kTile, e = me[n] / kTile;
+      if (e > a) {
+        atomicAdd(&cnt_all[a], 1);
+        atomicAdd(&cnt_all[e], -1);
+      }
     }
+  }
+  __syncthreads();
+  // block prefix sum: thread t owns tiles [t * per, (t + 1) * per)
+  const int per = (p.NT + kTile - 1) / kTile;
+  const int c0 = t * per;
+  int sa = 0, sf = 0;
+  for (int c = c0; c < c0 + per && c < p.NT; ++c) {
+    sa += cnt_any[c];
+    sf += cnt_all[c];
+  }
+  const int lane = t & 31, warp = t >> 5;
+  int ia = sa, iff = sf;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xFFFFFFFFu, ia, o);
+    const int yf = __shfl_up_sync(0xFFFFFFFFu, iff, o);
+    if (lane >= o) {
+      ia += ya;
+      iff += yf;
+    }
+  }
+  if (lane == 31) {
+    s_wtot[0][warp] = ia;
+    s_wtot[1][warp] = iff;
+  }
+  __syncthreads();
+  int run_a = ia - sa, run_f = iff - sf;  // exclusive prefix within the warp
+  for (int w = 0; w < warp; ++w) {
+    run_a += s_wtot[0][w];
+    run_f += s_wtot[1][w];
+  }
+  for (int c = c0; c < c0 + per && c < p.NT; ++c) {
+    run_a += cnt_any[c];
+    run_f += cnt_all[c];
+    code[c] = run_a > 0 ? (run_f == kTile ? 2 : 1) : 0;
   }
   __syncthreads();
   uint32_t* out = p.bm[dir] + (static_cast<size_t>(b) * p.NT + tile) * p.W;
@@ -223,12 +257,7 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
     for (int q = 0; q < 16; ++q) {
       const int c = ow * 16 + q;
       if (c >= p.NT) break;
-      const int w = c >> 5;
-      const uint32_t bit = 1u << (c & 31);
-      const uint32_t a = (s_any[w] | s_any[p.NW32 + w] | s_any[2 * p.NW32 + w] | s_any[3 * p.NW32 + w]) & bit;
-      const uint32_t f = (s_all[w] & s_all[p.NW32 + w] & s_all[2 * p.NW32 + w] & s_all[3 * p.NW32 + w]) & bit;
-      const uint32_t code = a ? (f ? 2u : 1u) : 0u;
-      word |= code << (2 * q);
+      word |= static_cast<uint32_t>(code[c]) << (2 * q);
     }
     out[ow] = word;
   }
@@ -312,8 +341,8 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const int32_t* seg
   p.S = S;
   p.NT = S / kTile;
   p.W = (p.NT + 15) / 16;
-  p.NW32 = (p.NT + 31) / 32;
-  const size_t smem = static_cast<size_t>(nseg_max + 1) * 4 + static_cast<size_t>(8) * p.NW32 * 4;
+  const size_t smem = static_cast<size_t>(nseg_max + 1) * 4 + static_cast<size_t>(2) * (p.NT + 1) * 4 +
+                      static_cast<size_t>(p.NT) + 16;
   if (smem > 200 * 1024) return -1;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(descriptor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -69,3 +69,22 @@ def test_visible_pairs_union_matches_oracle_counts():
         got = bench.visible_pairs(d, 2, S)
         want = [int(M.dense_mask(wid, seg[b], int(nseg[b]), S).sum()) for b in range(2)]
         assert got == want
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the CPU oracle and prints one JSON line."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--config", "1", "--steps", "1", "--warmup", "3", "--ref-rows", "64"],
+                         capture_output=True, text=True, timeout=300, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
