@@ -111,12 +111,39 @@ CM_API int cm_spec_num_intervals(const cm_spec* spec, int* ni_max);
  * NUL-terminated string; *needed (if not NULL) receives the full length + 1.  Host only. */
 CM_API int cm_spec_describe(const cm_spec* spec, char* buf, size_t len, size_t* needed);
 
+/* CUDA C++ source of the spec's mask-specific preprocess kernel (section 3.1: the compiler
+ * generates a mask-specific preprocess kernel), written to buf as a NUL-terminated string;
+ * *needed (if not NULL) receives the full length + 1.  The source includes the shared kernel body
+ * "descriptor_core.cuh", which the library carries in itself.  Host only. */
+CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed);
+
+/* Whether the spec's generated kernel can run.  load = 0: compile it with NVRTC only (host only,
+ * no GPU needed).  load = 1: compile it and load it into the current device context, which is
+ * what cm_build_descriptor does on its first call with the spec (the result, good or bad, is
+ * kept per spec; compiling takes a few tenths of a second).  Returns CM_OK on success,
+ * CM_ERR_UNSUPPORTED when NVRTC (libnvrtc.so.13) cannot be opened, CM_ERR_CUDA when compiling or
+ * loading failed.  The NVRTC log or the failing step goes to log as a NUL-terminated string (log
+ * may be NULL). */
+CM_API int cm_spec_kernel_status(const cm_spec* spec, int load, char* log, size_t log_len);
+
 /* ---- online descriptor construction (sections 3.3, 3.3.1) ---------------------------------- */
 
 /* Byte sizes of the descriptor buffers, in the order itab_f, bm_f, itab_b, bm_b, sched_f,
  * sched_b, status.  tile must be 128. */
 CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, int S, int tile,
                                size_t sizes[7]);
+
+/* Which descriptor kernels cm_build_descriptor runs, for the whole process:
+ * CM_PREPROCESS_GENERATED (default): the specs' generated kernels, one launch per direction; if
+ *   either spec's kernel cannot be compiled or loaded (see cm_spec_kernel_status), the generic
+ *   kernel runs instead;
+ * CM_PREPROCESS_GENERIC: the generic kernel, which interprets the compiled endpoint programs and
+ *   builds both directions in one launch.
+ * Both are GPU kernels and build identical descriptors.  Returns CM_ERR_INVALID_ARG for any other
+ * mode.  Not synchronised with builds in flight on other host threads. */
+#define CM_PREPROCESS_GENERATED 0
+#define CM_PREPROCESS_GENERIC 1
+CM_API int cm_set_preprocess_mode(int mode);
 
 /* Queue the preprocess kernels that evaluate both specs against `meta` and fill `desc`.
  * desc->B, S, tile, ni_f, ni_b must match the specs and sizes; its pointers must be set.

@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.cm_spec_free.restype = None
         L.cm_spec_num_intervals.argtypes = [vp, ctypes.POINTER(i32)]
         L.cm_spec_describe.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
+        L.cm_spec_kernel_source.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
+        L.cm_spec_kernel_status.argtypes = [vp, i32, ctypes.c_char_p, sz]
+        L.cm_set_preprocess_mode.argtypes = [i32]
         L.cm_descriptor_sizes.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(sz)]
         L.cm_build_descriptor.argtypes = [vp, vp, ctypes.POINTER(cm_meta), i32, i32,
                                           ctypes.POINTER(cm_descriptor), vp]
@@ -134,6 +137,33 @@ def cm_spec_describe(spec: Spec) -> str:
     buf = ctypes.create_string_buffer(need.value)
     _check(lib().cm_spec_describe(spec.handle, buf, need.value, None), "cm_spec_describe")
     return buf.value.decode()
+
+
+def cm_spec_kernel_source(spec: Spec) -> str:
+    """CUDA C++ source of the spec's mask-specific preprocess kernel."""
+    need = ctypes.c_size_t()
+    _check(lib().cm_spec_kernel_source(spec.handle, None, 0, ctypes.byref(need)),
+           "cm_spec_kernel_source")
+    buf = ctypes.create_string_buffer(need.value)
+    _check(lib().cm_spec_kernel_source(spec.handle, buf, need.value, None), "cm_spec_kernel_source")
+    return buf.value.decode()
+
+
+def cm_spec_kernel_status(spec: Spec, load: bool = True) -> tuple[int, str]:
+    """(code, log): CM_OK when the spec's generated preprocess kernel compiles (load=False, host
+    only) or compiles and loads on the current GPU (load=True); otherwise the code and the reason."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    rc = lib().cm_spec_kernel_status(spec.handle, 1 if load else 0, buf, len(buf))
+    return rc, buf.value.decode(errors="replace")
+
+
+CM_PREPROCESS_GENERATED = 0
+CM_PREPROCESS_GENERIC = 1
+
+
+def cm_set_preprocess_mode(mode: int) -> None:
+    """Process-wide choice of descriptor kernels: generated per spec (default) or generic."""
+    _check(lib().cm_set_preprocess_mode(mode), "cm_set_preprocess_mode")
 
 
 def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE) -> list[int]:

@@ -16,9 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcm.so")
 
-SOURCES = ["compiler.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "api.cu",
+SOURCES = ["compiler.cpp", "codegen.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "api.cu",
            "attn_bwd_noalloc.cu"]
-HEADERS = ["program.h", "kernels.h", "ptx.cuh", "tma_host.h"]
+HEADERS = ["program.h", "kernels.h", "ptx.cuh", "tma_host.h", "descriptor_core.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,7 +31,21 @@ def _nvcc() -> str:
 
 def _flags() -> list[str]:
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-                   "-I", os.path.join(ROOT, "include")]
+                   "-I", os.path.join(ROOT, "include"), "-I", BUILD]
+
+
+def _embed_core_source() -> None:
+    """Write the shared preprocess kernel body as a C++ string literal for codegen.cpp, which hands
+    it to NVRTC as the header of every generated kernel."""
+    with open(os.path.join(CSRC, "descriptor_core.cuh")) as f:
+        text = f.read()
+    delim = "cmcore_src"
+    assert ")" + delim + '"' not in text
+    out = os.path.join(BUILD, "descriptor_core_src.inc")
+    body = 'R"' + delim + "(" + text + ")" + delim + '"\n'
+    if not os.path.exists(out) or open(out).read() != body:
+        with open(out, "w") as f:
+            f.write(body)
 
 
 def _stale() -> bool:
@@ -47,6 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    _embed_core_source()
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
@@ -64,7 +79,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)

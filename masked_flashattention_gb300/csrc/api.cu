@@ -1,6 +1,7 @@
 // C ABI of libcm.so: host-side validation and kernel launches (declarations in include/cm.h).
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <atomic>
 #include <cmath>
 
 #include "../../include/cm.h"
@@ -11,6 +12,9 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kMaxS = 131072;
+
+// which descriptor kernels cm_build_descriptor runs (cm_set_preprocess_mode)
+std::atomic<int> g_preprocess_mode{CM_PREPROCESS_GENERATED};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -69,6 +73,12 @@ CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, in
   return CM_OK;
 }
 
+CM_API int cm_set_preprocess_mode(int mode) {
+  if (mode != CM_PREPROCESS_GENERATED && mode != CM_PREPROCESS_GENERIC) return CM_ERR_INVALID_ARG;
+  g_preprocess_mode.store(mode);
+  return CM_OK;
+}
+
 CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_meta* meta, int B,
                                int S, cm_descriptor* desc, void* stream) {
   if (!fwd || !bwd || !meta || !meta->seg || !meta->nseg || meta->nseg_max < 1)
@@ -82,9 +92,16 @@ CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_
   if (meta->nseg_max > 16384) return CM_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(desc->status, 0, 4, st) != cudaSuccess) return CM_ERR_CUDA;
-  if (cm::launch_descriptor(*cm::spec_program(fwd), *cm::spec_program(bwd), meta->seg, meta->nseg,
-                            meta->nseg_max, B, S, desc->itab_f, desc->bm_f, desc->itab_b,
-                            desc->bm_b, desc->sched_f, desc->sched_b, desc->status, st) != 0)
+  const void* gen_f = nullptr;
+  const void* gen_b = nullptr;
+  if (g_preprocess_mode.load() == CM_PREPROCESS_GENERATED) {
+    gen_f = cm::spec_generated_kernel(fwd);
+    gen_b = gen_f != nullptr ? cm::spec_generated_kernel(bwd) : nullptr;
+  }
+  if (cm::launch_descriptor(*cm::spec_program(fwd), *cm::spec_program(bwd), gen_f, gen_b,
+                            meta->seg, meta->nseg, meta->nseg_max, B, S, desc->itab_f, desc->bm_f,
+                            desc->itab_b, desc->bm_b, desc->sched_f, desc->sched_b, desc->status,
+                            st) != 0)
     return CM_ERR_CUDA;
   return CM_OK;
 }

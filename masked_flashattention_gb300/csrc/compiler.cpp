@@ -17,7 +17,9 @@
 //             Two different slots are never merged: a merge must hold for every row of the
 //             Region, which the symbolic form cannot show for the rules used here (e.g. the
 //             Region C rule keeps [0, b) and [s(i), i + 1) as two slots).
-//  emit       stack programs (program.h) evaluated per row by the preprocess kernel
+//  emit       stack programs (program.h) evaluated per row by the generic preprocess kernel,
+//             and the same endpoints as CUDA C++: the row evaluator of the spec's own
+//             preprocess kernel, compiled at run time with NVRTC (codegen.cpp)
 #include <algorithm>
 #include <cctype>
 #include <climits>
@@ -25,6 +27,7 @@
 #include <cstring>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <sstream>
 #include <stdexcept>
 #include <string>
@@ -688,6 +691,61 @@ int max_depth(const std::vector<int32_t>& code, int start) {
   return m;
 }
 
+// ---- the same endpoints as CUDA C++ (the mask-specific kernel's row evaluator) --------------
+// Names in scope of the generated code: i (row), ki (= seg_idx(i)), seg (segment starts in shared
+// memory), nseg, S.  Sums and products wrap like the stack programs' arithmetic.
+std::string c_lin(const Lin& l);
+std::string c_atom(const Atom& a) {
+  switch (a.kind) {
+    case EK::I: return "i";
+    case EK::S: return "S";
+    case EK::Nseg: return "nseg";
+    case EK::Min: return "cmcore::imin(" + c_lin(a.args[0]) + ", " + c_lin(a.args[1]) + ")";
+    case EK::Max: return "cmcore::imax(" + c_lin(a.args[0]) + ", " + c_lin(a.args[1]) + ")";
+    case EK::SegIdx: {
+      const Lin& x = a.args[0];
+      const bool row_itself = x.c == 0 && x.t.size() == 1 && x.t.begin()->second.first == 1 &&
+                              x.t.begin()->second.second->kind == EK::I;
+      return row_itself ? "ki" : "cmcore::seg_index(seg, nseg, " + c_lin(x) + ")";
+    }
+    case EK::SegStartAt: return "cmcore::seg_start_at(seg, nseg, " + c_lin(a.args[0]) + ")";
+    case EK::SegEndAt: return "cmcore::seg_end_at(seg, nseg, " + c_lin(a.args[0]) + ")";
+    default: throw CompileError("internal: j in an endpoint");
+  }
+}
+std::string c_const(long long v) {
+  if (v < INT32_MIN || v > INT32_MAX) throw CompileError("constant out of int32 range");
+  return "(" + std::to_string(v) + ")";
+}
+std::string c_lin(const Lin& l) {
+  std::string acc;
+  for (const auto& kv : l.t) {
+    std::string term = c_atom(*kv.second.second);
+    if (kv.second.first != 1) term = "cmcore::wmul(" + term + ", " + c_const(kv.second.first) + ")";
+    acc = acc.empty() ? term : "cmcore::wadd(" + acc + ", " + term + ")";
+  }
+  if (acc.empty()) return c_const(l.c);
+  if (l.c != 0) acc = "cmcore::wadd(" + acc + ", " + c_const(l.c) + ")";
+  return acc;
+}
+const char* c_op(int op) {
+  static const char* s[] = {"<", "<=", ">", ">=", "==", "!="};
+  return s[op];
+}
+std::string c_bool(const BP& b) {
+  switch (b->k) {
+    case BK::True: return "true";
+    case BK::False: return "false";
+    case BK::Not: return "!(" + c_bool(b->a) + ")";
+    case BK::And: return "(" + c_bool(b->a) + " && " + c_bool(b->b) + ")";
+    case BK::Or: return "(" + c_bool(b->a) + " || " + c_bool(b->b) + ")";
+    case BK::Cmp:
+      return "(" + c_lin(lin_of(b->l, false)) + " " + c_op(b->op) + " " +
+             c_lin(lin_of(b->r, false)) + ")";
+  }
+  return "false";
+}
+
 std::string bstr(const BP& b) {
   switch (b->k) {
     case BK::True: return "all";
@@ -708,7 +766,13 @@ std::string bstr(const BP& b) {
 // ---------------------------------------------------------------------------------------------
 struct SpecImpl {
   DevProg prog;
-  std::string text;  // describe() output
+  std::string text;        // describe() output
+  std::string gen;         // CUDA C++ source of the mask-specific preprocess kernel
+  std::mutex mu;           // guards the four fields below
+  bool gen_tried = false;  // compiled and loaded once, on first use
+  const void* gen_kernel = nullptr;
+  int gen_rc = CM_OK;      // why gen_kernel is null, if it is
+  std::string gen_log;
 };
 
 static int compile(const char* text, SpecImpl& out) {
@@ -719,7 +783,7 @@ static int compile(const char* text, SpecImpl& out) {
   DevProg& P = out.prog;
   std::memset(&P, 0, sizeof(P));
   std::ostringstream desc;
-  std::vector<std::string> region_desc;
+  std::ostringstream gen;  // body of the generated row evaluator
   int ni = 0, nreg = 0;
   while (std::getline(in, line)) {
     ++lineno;
@@ -773,6 +837,7 @@ static int compile(const char* text, SpecImpl& out) {
     em.end();
     P.nslot[r] = static_cast<int16_t>(slots.size());
     desc << "region " << r << " when " << bstr(guard) << "\n";
+    gen << "    if (" << c_bool(guard) << ") {\n";
     for (size_t n = 0; n < slots.size(); ++n) {
       const Slot& s = slots[n];
       if (s.conds.empty()) {
@@ -804,11 +869,25 @@ static int compile(const char* text, SpecImpl& out) {
         hi_s = q ? "min(" + hi_s + ", " + s.highs[q].str() + ")" : s.highs[q].str();
       }
       em.end();
+      std::string lo_c = c_const(0), hi_c = "S", cond_c;
+      for (size_t q = 0; q < s.lows.size(); ++q)
+        lo_c = q ? "cmcore::imax(" + lo_c + ", " + c_lin(s.lows[q]) + ")" : c_lin(s.lows[q]);
+      for (size_t q = 0; q < s.highs.size(); ++q)
+        hi_c = q ? "cmcore::imin(" + hi_c + ", " + c_lin(s.highs[q]) + ")" : c_lin(s.highs[q]);
+      for (size_t q = 0; q < s.conds.size(); ++q)
+        cond_c += std::string(q ? " && " : "") + "(" + c_lin(s.conds[q].diff) + " " +
+                  c_op(s.conds[q].op) + " 0)";
+      const std::string ind = cond_c.empty() ? "      " : "        ";
+      if (!cond_c.empty()) gen << "      if (" << cond_c << ") {\n";
+      gen << ind << "lo[" << n << "] = " << lo_c << ";\n";
+      gen << ind << "hi[" << n << "] = " << hi_c << ";\n";
+      if (!cond_c.empty()) gen << "      }\n";
       desc << "  slot " << n << ": [" << lo_s << ", " << hi_s << ")";
       for (size_t q = 0; q < s.conds.size(); ++q)
         desc << (q ? " and " : " if ") << cmp_str(s.conds[q]);
       desc << "\n";
     }
+    gen << "      return;\n    }\n";
     if (em.code.size() > static_cast<size_t>(kMaxCode))
       throw CompileError("spec too large (endpoint programs exceed " + std::to_string(kMaxCode) +
                          " words)");
@@ -828,10 +907,28 @@ static int compile(const char* text, SpecImpl& out) {
   P.nreg = nreg;
   for (size_t q = 0; q < em.code.size(); ++q) P.code[q] = em.code[q];
   out.text = "intervals " + std::to_string(P.ni) + "\n" + desc.str();
+  out.gen =
+      "// Mask-specific preprocess kernel generated from a MaskSpec.\n"
+      "#include \"descriptor_core.cuh\"\n"
+      "struct GenEval {\n"
+      "  __device__ __forceinline__ void row(int i, int ki, const int* seg, int nseg, int S,\n"
+      "                                      int* lo, int* hi) const {\n"
+      "    (void)i; (void)ki; (void)seg; (void)nseg; (void)S;\n" +
+      gen.str() +
+      "  }\n"
+      "};\n"
+      "extern \"C\" __global__ void __launch_bounds__(128)\n"
+      "cm_generated_descriptor(const __grid_constant__ cmcore::DescCore p) {\n"
+      "  cmcore::descriptor_tile<" + std::to_string(P.ni) +
+      ">(p, blockIdx.x / p.NT, blockIdx.x % p.NT, GenEval());\n"
+      "}\n";
   return CM_OK;
 }
 
 const DevProg* spec_program(const cm_spec* s);
+const void* spec_generated_kernel(const cm_spec* s);
+int compile_generated_kernel(const std::string& source, std::vector<char>* cubin, std::string* log);
+int load_generated_kernel(const std::string& source, const void** kernel, std::string* log);
 
 }  // namespace cm
 
@@ -840,6 +937,16 @@ struct cm_spec {
 };
 
 const cm::DevProg* cm::spec_program(const cm_spec* s) { return &s->impl.prog; }
+
+const void* cm::spec_generated_kernel(const cm_spec* s) {
+  cm::SpecImpl& im = const_cast<cm_spec*>(s)->impl;
+  std::lock_guard<std::mutex> lock(im.mu);
+  if (!im.gen_tried) {
+    im.gen_tried = true;
+    im.gen_rc = cm::load_generated_kernel(im.gen, &im.gen_kernel, &im.gen_log);
+  }
+  return im.gen_kernel;
+}
 
 extern "C" {
 
@@ -865,6 +972,33 @@ CM_API int cm_spec_num_intervals(const cm_spec* spec, int* ni_max) {
   if (!spec || !ni_max) return CM_ERR_INVALID_ARG;
   *ni_max = spec->impl.prog.ni;
   return CM_OK;
+}
+
+CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed) {
+  if (!spec) return CM_ERR_INVALID_ARG;
+  const std::string& t = spec->impl.gen;
+  if (needed) *needed = t.size() + 1;
+  if (buf && len) std::snprintf(buf, len, "%s", t.c_str());
+  return CM_OK;
+}
+
+CM_API int cm_spec_kernel_status(const cm_spec* spec, int load, char* log, size_t log_len) {
+  if (log && log_len) log[0] = 0;
+  if (!spec) return CM_ERR_INVALID_ARG;
+  int rc;
+  std::string text;
+  if (load) {
+    cm::spec_generated_kernel(spec);
+    cm::SpecImpl& im = const_cast<cm_spec*>(spec)->impl;
+    std::lock_guard<std::mutex> lock(im.mu);
+    rc = im.gen_rc;
+    text = im.gen_log;
+  } else {
+    std::vector<char> cubin;
+    rc = cm::compile_generated_kernel(spec->impl.gen, &cubin, &text);
+  }
+  if (log && log_len) std::snprintf(log, log_len, "%s", text.c_str());
+  return rc;
 }
 
 CM_API int cm_spec_describe(const cm_spec* spec, char* buf, size_t len, size_t* needed) {

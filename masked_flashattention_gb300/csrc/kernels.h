@@ -11,6 +11,9 @@ struct cm_spec;
 namespace cm {
 
 const DevProg* spec_program(const cm_spec* s);
+// The spec's mask-specific preprocess kernel (a cudaKernel_t), compiled with NVRTC and loaded
+// into the current context on first use; nullptr where that is not possible.
+const void* spec_generated_kernel(const cm_spec* s);
 
 struct FwdParams {
   const int32_t* itab;   // forward Interval Table [B][NI][S][2]
@@ -39,10 +42,12 @@ struct BwdParams {
   float scale_log2;      // scale * log2(e)
 };
 
-int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const int32_t* seg,
-                      const int32_t* nseg, int nseg_max, int B, int S, int32_t* itab_f,
-                      uint32_t* bm_f, int32_t* itab_b, uint32_t* bm_b, int32_t* sched_f,
-                      int32_t* sched_b, int32_t* status, cudaStream_t stream);
+// Runs the generated kernels when both gen_fwd and gen_bwd are given, else the generic kernel.
+int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_fwd,
+                      const void* gen_bwd, const int32_t* seg, const int32_t* nseg, int nseg_max,
+                      int B, int S, int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b,
+                      uint32_t* bm_b, int32_t* sched_f, int32_t* sched_b, int32_t* status,
+                      cudaStream_t stream);
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream);
 int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,

@@ -145,3 +145,39 @@ def test_attention_argument_validation_happens_on_the_host(B):
 def test_error_strings(B):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert B.cm_error_string(code)
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_generated_preprocess_kernels_compile(B, wid):
+    """Each workload spec's mask-specific preprocess kernel (section 3.1) compiles with NVRTC for
+    sm_103a (host only; loading needs a GPU and is checked by the GPU tests)."""
+    from masked_flashattention_gb300 import specs
+    for text in (specs.FWD[wid], specs.BWD[wid]):
+        spec = B.cm_compile_spec(text)
+        src = B.cm_spec_kernel_source(spec)
+        assert 'extern "C" __global__' in src and "cm_generated_descriptor" in src
+        assert f"descriptor_tile<{B.cm_spec_num_intervals(spec)}>" in src
+        rc, log = B.cm_spec_kernel_status(spec, load=False)
+        if rc == B.CM_ERR_UNSUPPORTED:
+            pytest.skip("NVRTC is not available here: " + log)
+        assert rc == B.CM_OK, log
+
+
+def test_generated_source_follows_the_lowered_slots(B):
+    """The generated evaluator holds the Region C slots of the lowered form: [0, b) and
+    [s(i), i + 1) for response rows (seg_idx(i) >= 1), one causal slot for prompt rows."""
+    from masked_flashattention_gb300 import specs
+    src = B.cm_spec_kernel_source(B.cm_compile_spec(specs.FWD[3]))
+    assert "if ((ki == (0))) {" in src
+    assert "lo[0] = (0);\n      hi[0] = cmcore::wadd(i, (1));" in src
+    assert "hi[0] = cmcore::seg_end_at(seg, nseg, (0));" in src
+    assert "lo[1] = cmcore::seg_start_at(seg, nseg, ki);" in src
+
+
+def test_preprocess_mode_validation(B):
+    L = B.lib()
+    assert L.cm_set_preprocess_mode(7) == B.CM_ERR_INVALID_ARG
+    assert L.cm_set_preprocess_mode(-1) == B.CM_ERR_INVALID_ARG
+    B.cm_set_preprocess_mode(B.CM_PREPROCESS_GENERIC)
+    B.cm_set_preprocess_mode(B.CM_PREPROCESS_GENERATED)
+    assert L.cm_spec_kernel_status(None, 0, None, 0) == B.CM_ERR_INVALID_ARG

@@ -20,13 +20,25 @@ def _lib():
     return B
 
 
-def _build(B, wid, seg, nseg, S):
+MODES = ["generated", "generic"]
+
+
+def _set_mode(B, mode):
+    B.cm_set_preprocess_mode(B.CM_PREPROCESS_GENERIC if mode == "generic"
+                             else B.CM_PREPROCESS_GENERATED)
+
+
+def _build(B, wid, seg, nseg, S, mode="generated"):
     from masked_flashattention_gb300 import specs
+    _set_mode(B, mode)
     f = B.cm_compile_spec(specs.FWD[wid])
     b = B.cm_compile_spec(specs.BWD[wid])
     desc = B.Descriptor(f, b, seg.shape[0], S)
-    B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
-    torch.cuda.synchronize()
+    try:
+        B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
+        torch.cuda.synchronize()
+    finally:
+        _set_mode(B, "generated")
     assert B.cm_get_status(desc) == 0
     return desc
 
@@ -55,24 +67,26 @@ def _check(desc, wid, seg, nseg, S):
         assert (np.diff(counts) <= 0).all()
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
-def test_descriptor_full_size(wid):
+def test_descriptor_full_size(wid, mode):
     B = _lib()
     w = W.WORKLOADS[wid]
     seg, nseg = W.segments(wid, w.B, w.S)
-    desc = _build(B, wid, seg, nseg, w.S)
+    desc = _build(B, wid, seg, nseg, w.S, mode)
     _check(desc, wid, seg, nseg, w.S)
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("S", [128, 384, 1024, 2048])
-def test_descriptor_small_seeded(wid, S):
+def test_descriptor_small_seeded(wid, S, mode):
     B = _lib()
     for seed in range(4):
         if wid == 5 and S < 1024:
             continue  # the prefix/document rule needs room for documents
         seg, nseg = W.segments(wid, 3, S, seed=100 * seed + S + wid)
-        desc = _build(B, wid, seg, nseg, S)
+        desc = _build(B, wid, seg, nseg, S, mode)
         _check(desc, wid, seg, nseg, S)
 
 
@@ -91,3 +105,20 @@ def test_bad_metadata_is_reported_not_faulted():
     seg = np.array([[0, 100, 200, S]], dtype=np.int32)
     B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
     assert B.cm_get_status(desc) == B.CM_OK
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_generated_kernels_load_and_agree_with_the_generic_kernel(wid):
+    """The mask-specific kernels compile and load on this GPU (so the default mode really runs
+    them), and build the same bytes as the generic kernel on a batch of several samples."""
+    B = _lib()
+    from masked_flashattention_gb300 import specs
+    for text in (specs.FWD[wid], specs.BWD[wid]):
+        rc, log = B.cm_spec_kernel_status(B.cm_compile_spec(text), load=True)
+        assert rc == B.CM_OK, log
+    S = 4096
+    seg, nseg = W.segments(wid, 5, S, seed=11 + wid)
+    a = _build(B, wid, seg, nseg, S, "generated")
+    g = _build(B, wid, seg, nseg, S, "generic")
+    for x, y in ((a.itab_f, g.itab_f), (a.bm_f, g.bm_f), (a.itab_b, g.itab_b), (a.bm_b, g.bm_b)):
+        assert torch.equal(x, y)
