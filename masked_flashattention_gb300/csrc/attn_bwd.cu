@@ -18,14 +18,25 @@
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
 //              half w / 4: queries [64*half, +64) of S^T / dP^T, and head-dim columns
 //              [half*d/2, +d/2) of dQ_part, dV and dK.
-//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) and dO (+ D).
-//   warp 9     MMA issuer (one thread).  Per query tile: S^T, dP^T; then dK (its completion
-//              frees Q for the next tile), dV (frees dO), and dQ_part.
-// TMEM (512 columns): dV [0, d), dK [128, 128+d), R1 [256, 384) = S^T, overwritten in place by
-// the bf16 P^T pairs (each warp writes only columns it has already read), R2 [384, 512) = dP^T,
-// then dQ_part.
-// Shared memory: K, V, Q, dO, dS^T (bf16, 128-byte swizzle), one 16 KB fp32 staging tile per
-// column half for the dQ bulk add, LSE*log2e and D of the current query tile.
+//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) into one of
+//              two slots, and dO (+ D).
+//   warp 9     MMA issuer (one thread).
+// TMEM (512 columns): dV [0, d), dK [128, 128+d), and two 128-column regions RA [256, 384),
+// RB [384, 512) whose roles alternate between query tiles.  For tile m with X = RA (m even) or
+// RB (m odd) and Y the other one:
+//   S^T(m) -> X; the compute warps overwrite it in place with the bf16 P^T pairs (each warp
+//   writes only columns it has already read); dP^T(m) -> Y.
+//   After the compute warps hand over P^T and dS^T, the MMA issues dV(m) (reads P^T from X),
+//   dK(m), S^T(m+1) -> Y (free: dP^T(m) was consumed), dQ_part(m) -> X (after dV read P^T), and,
+//   once dQ_part(m) has been read out, dP^T(m+1) -> X.
+// So the next tile's S^T is computed while the compute warps wait for dQ_part, and its dP^T while
+// they stage dQ_part and compute P(m+1): the tensor pipe does not idle for the whole P/dS phase.
+// Shared memory: K, V, Q (two slots), dO, dS^T (bf16, 128-byte swizzle), one 16 KB fp32 staging
+// tile per column half for the dQ bulk adds, LSE*log2e (per Q slot) and D of the current tile, and
+// the CTA's row of the backward bitmap (the non-empty query tiles are found by scanning it).
+// dQ_part is read out of TMEM at once; each half stages its first 32-column chunk in its staging
+// tile and the second in its dS^T box (idle from the dQ_part MMA until the next tile's dS^T), so
+// the bulk adds of one tile overlap the next tile's P/dS work.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -42,12 +53,11 @@ constexpr int kComputeWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-constexpr int kMaxTiles = 1024;
 
 constexpr uint32_t kColDV = 0;
 constexpr uint32_t kColDK = 128;
-constexpr uint32_t kColR1 = 256;
-constexpr uint32_t kColR2 = 384;
+constexpr uint32_t kColRA = 256;
+constexpr uint32_t kColRB = 384;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -56,32 +66,50 @@ struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTileBytes;
-  static constexpr uint32_t kQ = 2 * kTileBytes;
-  static constexpr uint32_t kdO = 3 * kTileBytes;
-  static constexpr uint32_t kdSt = 4 * kTileBytes;   // [2 boxes][128 keys][64 queries] bf16
-  static constexpr uint32_t kStage = kdSt + 32768u;  // fp32 [2 halves][128 rows][32 cols]
-  static constexpr uint32_t kLse2 = kStage + 32768u; // 128 floats: -LSE * log2(e)
-  static constexpr uint32_t kDelta = kLse2 + 512u;   // 128 floats: -D
+  static constexpr uint32_t kQ = 2 * kTileBytes;      // two slots
+  static constexpr uint32_t kdO = 4 * kTileBytes;
+  static constexpr uint32_t kdSt = 5 * kTileBytes;    // [2 boxes][128 keys][64 queries] bf16
+  static constexpr uint32_t kStage = kdSt + 32768u;   // fp32 [2 halves][128 rows][32 cols]
+  static constexpr uint32_t kLse2 = kStage + 32768u;  // [2 slots][128 floats]: -LSE * log2(e)
+  static constexpr uint32_t kDelta = kLse2 + 1024u;   // 128 floats: -D
   static constexpr uint32_t kBar = kDelta + 512u;
-  static constexpr uint32_t kList = kBar + 256u;
-  static constexpr uint32_t kTotal = kList + 2u * kMaxTiles;
-  static constexpr uint32_t kAlloc = kTotal + 1024u;
+  static constexpr uint32_t kRow = kBar + 256u;       // bitmap row: at most 64 words (NT <= 1024)
+  static constexpr uint32_t kTotal = kRow + 256u;
+  static constexpr uint32_t kAlloc = kTotal + 1024u;  // + slack to align the base to 1024 bytes
 };
+static_assert(Smem<128>::kAlloc <= 232448, "backward shared memory exceeds 227 KB");
 
 enum {
-  B_KV = 0,       // K and V loaded
-  B_QFULL = 1,    // Q and LSE*log2e of the current query tile loaded
-  B_QEMPTY = 2,   // the dK MMA (last reader of Q) of the current tile is done
-  B_DOFULL = 3,   // dO and D of the current query tile loaded
-  B_DOEMPTY = 4,  // the dV MMA (last reader of dO) of the current tile is done
-  B_SFULL = 5,    // S^T and dP^T computed
-  B_PDS = 6,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
-  B_DQFULL = 7,   // dQ_part computed (and every MMA of the tile done)
-  B_DQREAD = 8,   // compute warps read dQ_part from TMEM (8 arrivals)
-  B_STGFREE = 9,  // +half: the half's staging tile may be written (its leader, 1 arrival)
-  B_STGFULL = 11, // +half: the half's 4 warps wrote their staging rows (4 arrivals)
-  B_COUNT = 13
+  B_KV = 0,        // K and V loaded
+  B_QFULL = 1,     // +slot: Q and LSE*log2e of a query tile loaded
+  B_QEMPTY = 3,    // +slot: the dK MMA (last reader of that Q slot) is done
+  B_DOFULL = 5,    // dO and D of the current query tile loaded
+  B_DOEMPTY = 6,   // the dV MMA (last reader of dO) of the current tile is done
+  B_SFULL = 7,     // S^T of the current tile computed
+  B_DPFULL = 8,    // dP^T of the current tile computed
+  B_PDS = 9,       // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
+  B_DQFULL = 10,   // dQ_part computed (and every earlier MMA done)
+  B_DQREAD = 11,   // compute warps read dQ_part from TMEM (8 arrivals)
+  B_STGFREE = 12,  // +2*half+buffer: the buffer may be written (the half's leader, 1 arrival)
+  B_STGFULL = 16,  // +2*half+buffer: the half's 4 warps wrote their rows (4 arrivals)
+  B_COUNT = 20
 };
+
+// first query tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
+__device__ __forceinline__ int next_tile(const uint32_t* row, int NT, int c) {
+  while (c < NT) {
+    const int w = c >> 4;
+    uint32_t x = row[w];
+    x = (x | (x >> 1)) & 0x55555555u;
+    x &= 0xFFFFFFFFu << (2 * (c & 15));
+    if (x != 0) return (w << 4) + ((__ffs(x) - 1) >> 1);
+    c = (w + 1) << 4;
+  }
+  return NT;
+}
+__device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
+  return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
+}
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -114,39 +142,45 @@ __device__ __forceinline__ uint32_t visible_bits(int i0, const int (&st)[4], con
   return bits;
 }
 
-// P^T and dS^T of 32 queries of this key row.  For a full tile every query is visible; for a
-// partial tile `vis` holds the visibility bits.
+// P^T of 32 queries of this key row: p = exp2(s * scale*log2e + (-LSE*log2e)) in fp32 (kept for
+// dS) and as bf16 pairs (the A operand of dV).  Shared memory holds -LSE*log2e per query, so the
+// exponent is one paired FMA.  For a partial tile, queries whose bit in `vis` is clear get p = 0.
 template <bool FULL>
-__device__ __forceinline__ void chunk_p_ds(const uint32_t (&sr)[32], const uint32_t (&dpr)[32],
-                                           uint32_t lse2_addr, uint32_t delta_addr, float sl2,
-                                           uint32_t vis, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
-  // shared memory holds -LSE*log2e and -D per query, so both steps are paired FMAs / adds:
-  // x = s * scale*log2e + (-lse2),  p = exp2(x),  g = dp + (-D),  ds = p * g
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[32], uint32_t lse2_addr, float sl2,
+                                        uint32_t vis, float (&pf)[32], uint32_t (&pp)[16]) {
   const float2 scale2 = make_float2(sl2, sl2);
 #pragma unroll
   for (int c = 0; c < 32; c += 4) {
     const float4 l4 = ld_shared_f4(lse2_addr + c * 4u);
-    const float4 d4 = ld_shared_f4(delta_addr + c * 4u);
     const float2 xa = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2,
                            make_float2(l4.x, l4.y));
     const float2 xb = fma2(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
                            scale2, make_float2(l4.z, l4.w));
-    float2 pa = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
-    float2 pb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
+    pf[c] = ex2_approx(xa.x);
+    pf[c + 1] = ex2_approx(xa.y);
+    pf[c + 2] = ex2_approx(xb.x);
+    pf[c + 3] = ex2_approx(xb.y);
     if (!FULL) {
-      pa.x = ((vis >> c) & 1u) ? pa.x : 0.f;
-      pa.y = ((vis >> (c + 1)) & 1u) ? pa.y : 0.f;
-      pb.x = ((vis >> (c + 2)) & 1u) ? pb.x : 0.f;
-      pb.y = ((vis >> (c + 3)) & 1u) ? pb.y : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pf[c + e] = ((vis >> (c + e)) & 1u) ? pf[c + e] : 0.f;
     }
+    pp[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
+    pp[c / 2 + 1] = pack_bf16x2(pf[c + 2], pf[c + 3]);
+  }
+}
+
+// dS^T of 32 queries: ds = p * (dp + (-D)), as bf16 pairs.
+__device__ __forceinline__ void ds_chunk(const float (&pf)[32], const uint32_t (&dpr)[32],
+                                         uint32_t delta_addr, uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 d4 = ld_shared_f4(delta_addr + c * 4u);
     const float2 ga = add2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])),
                            make_float2(d4.x, d4.y));
     const float2 gb = add2(make_float2(__uint_as_float(dpr[c + 2]), __uint_as_float(dpr[c + 3])),
                            make_float2(d4.z, d4.w));
-    const float2 dsa = mul2(pa, ga);
-    const float2 dsb = mul2(pb, gb);
-    pp[c / 2] = pack_bf16x2(pa.x, pa.y);
-    pp[c / 2 + 1] = pack_bf16x2(pb.x, pb.y);
+    const float2 dsa = mul2(make_float2(pf[c], pf[c + 1]), ga);
+    const float2 dsb = mul2(make_float2(pf[c + 2], pf[c + 3]), gb);
     dd[c / 2] = pack_bf16x2(dsa.x, dsa.y);
     dd[c / 2 + 1] = pack_bf16x2(dsb.x, dsb.y);
   }
@@ -168,7 +202,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
-  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+  uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -182,34 +216,34 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_KV), 1);
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QEMPTY), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(B_QFULL + x), 1);
+      mbar_init(bar(B_QEMPTY + x), 1);
+    }
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(bar(B_STGFREE + x), 1);
+      mbar_init(bar(B_STGFULL + x), 4);
+    }
     mbar_init(bar(B_DOFULL), 1);
     mbar_init(bar(B_DOEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQREAD), kComputeWarps);
-    for (int hh = 0; hh < 2; ++hh) {
-      mbar_init(bar(B_STGFREE + hh), 1);
-      mbar_init(bar(B_STGFULL + hh), 4);
-    }
     fence_barrier_init();
   }
   if (warp == 0) {
+    // this CTA's bitmap row (W <= 64 words) and its count of non-empty query tiles
     const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + kt) * p.W;
-    int base = 0;
-    for (int c0 = 0; c0 < p.NT; c0 += 32) {
-      const int c = c0 + lane;
-      uint32_t code = 0;
-      if (c < p.NT) code = (row[c >> 4] >> (2 * (c & 15))) & 3u;
-      const uint32_t m = __ballot_sync(0xFFFFFFFFu, code != 0);
-      if (code != 0)
-        list[base + __popc(m & ((1u << lane) - 1u))] =
-            static_cast<uint16_t>(c | (code == 2u ? 0x8000 : 0));
-      base += __popc(m);
+    int cnt = 0;
+    for (int w = lane; w < p.W; w += 32) {
+      const uint32_t x = row[w];
+      bmrow[w] = x;
+      cnt += __popc((x | (x >> 1)) & 0x55555555u);
     }
-    if (lane == 0) *s_ntiles = base;
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    if (lane == 0) *s_ntiles = cnt;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -235,15 +269,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
         tma_load_2d(sbase + L::kV + x * 16384u, &tmV, x * 64, row0 + kt * 128, bar(B_KV));
       }
-      for (int m = 0; m < nt; ++m) {
-        const int qt = list[m] & 0x3FFF;
+      int qt = next_tile(bmrow, p.NT, 0);
+      for (int m = 0; m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
+        const int slot = m & 1;
         const size_t r = static_cast<size_t>(row0) + qt * 128;
-        // Q is free once the previous tile's dK MMA is done, dO once its dV MMA is done
-        if (m >= 1 && !mbar_wait(bar(B_QEMPTY), (m - 1) & 1, abort_flag, p.status, 0x201)) break;
-        mbar_arrive_expect_tx(bar(B_QFULL), L::kTileBytes + 512u);
+        // a Q slot is free once the dK MMA of the tile two back is done; dO once the previous
+        // tile's dV MMA is done
+        if (m >= 2 && !mbar_wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x201))
+          break;
+        mbar_arrive_expect_tx(bar(B_QFULL + slot), L::kTileBytes + 512u);
         for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QFULL));
-        bulk_load(sbase + L::kLse2, p.lse2 + r, 512u, bar(B_QFULL));
+          tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
+                      row0 + qt * 128, bar(B_QFULL + slot));
+        bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, bar(B_QFULL + slot));
         if (m >= 1 && !mbar_wait(bar(B_DOEMPTY), (m - 1) & 1, abort_flag, p.status, 0x20b)) break;
         mbar_arrive_expect_tx(bar(B_DOFULL), L::kTileBytes + 512u);
         for (int x = 0; x < D / 64; ++x)
@@ -255,45 +293,77 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV (TS)
+      constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
       constexpr uint32_t idMM = make_idesc_bf16(128, D, 1, 1);    // dQ_part
-      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ,
-                     sdO = sbase + L::kdO, sdSt = sbase + L::kdSt;
-      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202);
-      for (int m = 0; ok && m < nt; ++m) {
-        if (!mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x203)) break;
-        if (!mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20c)) break;
-        // dQ_part of the previous tile has been read out of R2, which also means every MMA of the
-        // previous tile (including the dV that read P^T from R1) has completed
-        if (m >= 1 && !mbar_wait(bar(B_DQREAD), (m - 1) & 1, abort_flag, p.status, 0x204)) break;
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdO = sbase + L::kdO,
+                     sdSt = sbase + L::kdSt;
+      // tile 0: S^T -> RA, dP^T -> RB
+      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202) &&
+                mbar_wait(bar(B_QFULL), 0, abort_flag, p.status, 0x203);
+      if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColR1, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQ, kk, 16384u), idSS,
-                  kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColRA, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sbase + L::kQ, kk, 16384u),
+                  idSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL));
+        ok = mbar_wait(bar(B_DOFULL), 0, abort_flag, p.status, 0x20c);
+      }
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColR2, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
+          umma_ss(tmem + kColRB, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
                   kk > 0 ? 1u : 0u);
-        umma_commit(bar(B_SFULL));
+        umma_commit(bar(B_DPFULL));
+      }
+      for (int m = 0; ok && m < nt; ++m) {
+        const uint32_t X = (m & 1) ? kColRB : kColRA;
+        const uint32_t Y = (m & 1) ? kColRA : kColRB;
+        const uint32_t sQ = sbase + L::kQ + (m & 1) * L::kTileBytes;
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
+        // dV += P^T dO; P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_DOEMPTY));
+        // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
                   (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY));
-        // P^T pairs: queries [0,64) at R1 columns [0,32), queries [64,128) at [64,96)
+        umma_commit(bar(B_QEMPTY + (m & 1)));
+        if (m + 1 < nt) {
+          // S^T of the next tile into Y, whose dP^T the compute warps have consumed
+          const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
+          if (!mbar_wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x203))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + Y, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQn, kk, 16384u), idSS,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(B_SFULL));
+        }
+        // dQ_part = dS K into X, after the dV MMA above has read P^T from it
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDV, tmem + kColR1 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DOEMPTY));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kColR2, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
+          umma_ss(tmem + X, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
                   kk > 0 ? 1u : 0u);
         umma_commit(bar(B_DQFULL));
+        if (m + 1 < nt) {
+          // dP^T of the next tile into X once dQ_part has been read out of it
+          if (!mbar_wait(bar(B_DOFULL), (m + 1) & 1, abort_flag, p.status, 0x20c)) break;
+          if (!mbar_wait(bar(B_DQREAD), m & 1, abort_flag, p.status, 0x204)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(B_DPFULL));
+        }
       }
     }
   } else {
@@ -304,7 +374,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = (quarter == 0 && lane == 0);  // issues this half's bulk adds
-    const uint32_t stage = sbase + L::kStage + hf * 16384u;
+    // staging buffers of this half: chunk 0 in the staging tile, chunk 1 in the half's dS^T box,
+    // which nothing reads between the dQ_part MMA and the next tile's dS^T
+    const uint32_t stage_buf[2] = {sbase + L::kStage + hf * 16384u, sbase + L::kdSt + hf * 16384u};
     int st[4];
     uint32_t len[4];
 #pragma unroll
@@ -319,28 +391,34 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int m = 0; ok && m < nt; ++m) {
-      const int entry = list[m];
-      const int qt = entry & 0x3FFF;
-      const bool full = (entry & 0x8000) != 0;
+    int qt = next_tile(bmrow, p.NT, 0);
+    for (int m = 0; ok && m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
+      const bool full = tile_is_full(bmrow, qt);
+      const uint32_t X = (m & 1) ? kColRB : kColRA;
+      const uint32_t Y = (m & 1) ? kColRA : kColRB;
+
+      // the previous tile's chunk-0 bulk add has read the staging tile: free it for this tile
+      if (leader) {
+        if (kChunks == 2) bulk_wait_read_but1();  // the chunk-1 add may still be reading
+        else bulk_wait_read_all();
+        mbar_arrive(bar(B_STGFREE + 2 * hf));
+      }
+      // ---- P^T: S^T from X, written back in place as bf16 pairs; fp32 P kept for dS ----
       bool ready = mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206) &&
-                   mbar_wait(bar(B_QFULL), m & 1, abort_flag, p.status, 0x207) &&
-                   mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20d);
+                   mbar_wait(bar(B_QFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x207);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
-      // this warp's 64 queries, in two chunks of 32
+      float pf[2][32];
+      const uint32_t lse2_base = sbase + L::kLse2 + (m & 1) * 512u;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int q0 = 64 * hf + 32 * ch;  // first query of the chunk within the tile
-        uint32_t sr[32], dpr[32];
-        tmem_ld32(tmem + lane_off + kColR1 + q0, sr);
-        tmem_ld32(tmem + lane_off + kColR2 + q0, dpr);
+        uint32_t sr[32], pp[16];
+        tmem_ld32(tmem + lane_off + X + q0, sr);
         tmem_wait_ld();
-        uint32_t pp[16], dd[16];
-        const uint32_t la = sbase + L::kLse2 + q0 * 4u, da = sbase + L::kDelta + q0 * 4u;
         if (full) {
-          chunk_p_ds<true>(sr, dpr, la, da, sl2, 0u, pp, dd);
+          p_chunk<true>(sr, lse2_base + q0 * 4u, sl2, 0u, pf[ch], pp);
         } else {
           const int i0 = qt * 128 + q0;
           uint32_t vis;
@@ -350,10 +428,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             case 3: vis = visible_bits<3>(i0, st, len); break;
             default: vis = visible_bits<4>(i0, st, len); break;
           }
-          chunk_p_ds<false>(sr, dpr, la, da, sl2, vis, pp, dd);
+          p_chunk<false>(sr, lse2_base + q0 * 4u, sl2, vis, pf[ch], pp);
         }
-        // P^T pairs into R1 columns this warp has already read: hf * 64 + ch * 16
-        tmem_st16(tmem + lane_off + kColR1 + hf * 64 + ch * 16, pp);
+        // P^T pairs into X columns this warp has already read: hf * 64 + ch * 16
+        tmem_st16(tmem + lane_off + X + hf * 64 + ch * 16, pp);
+      }
+
+      // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T into this half's box ----
+      if (leader) {
+        // the previous tile's chunk-1 bulk add has read the dS^T box
+        bulk_wait_read_all();
+        mbar_arrive(bar(B_STGFREE + 2 * hf + 1));
+      }
+      ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e) &&
+              mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20d) &&
+              mbar_wait(bar(B_STGFREE + 2 * hf + 1), m & 1, abort_flag, p.status, 0x209);
+      __syncwarp();
+      if (!ready) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int q0 = 64 * hf + 32 * ch;
+        uint32_t dpr[32], dd[16];
+        tmem_ld32(tmem + lane_off + Y + q0, dpr);
+        tmem_wait_ld();
+        ds_chunk(pf[ch], dpr, sbase + L::kDelta + q0 * 4u, dd);
         // dS^T row r, queries q0..q0+31 = four 16-byte chunks of box hf
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -368,42 +467,39 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PDS));
 
-      // dQ_part: query row r of this tile, head-dim columns [hf * kHalf, +kHalf)
+      // ---- dQ_part from X: query row r, head-dim columns [hf * kHalf, +kHalf), read at once ----
       ready = mbar_wait(bar(B_DQFULL), m & 1, abort_flag, p.status, 0x208);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
+      uint32_t v[kChunks][32];
+#pragma unroll
+      for (int cc = 0; cc < kChunks; ++cc) tmem_ld32(tmem + lane_off + X + hf * kHalf + cc * 32, v[cc]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DQREAD));  // X may be overwritten now
 #pragma unroll
       for (int cc = 0; cc < kChunks; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColR2 + hf * kHalf + cc * 32, v);
-        tmem_wait_ld();
-        if (cc == kChunks - 1) {
-          tc_fence_before();
+        // chunk 0 waits for its staging tile; chunk 1 uses the dS^T box, free since DQFULL
+        if (cc == 0) {
+          const bool free_ok = mbar_wait(bar(B_STGFREE + 2 * hf), m & 1, abort_flag, p.status, 0x209);
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_DQREAD));  // R2 may be overwritten now
+          if (!free_ok) { ok = false; break; }
         }
-        // use u of this half's staging tile: wait until the previous bulk add stopped reading it
-        const int u = m * kChunks + cc;
-        if (leader) {
-          bulk_wait_read_all();
-          mbar_arrive(bar(B_STGFREE + hf));
-        }
-        const bool free_ok = mbar_wait(bar(B_STGFREE + hf), u & 1, abort_flag, p.status, 0x209);
-        __syncwarp();
-        if (!free_ok) { ok = false; break; }
+        const uint32_t buf = stage_buf[cc];
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          st_shared_v4(stage + r * 128u + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4), v[4 * c],
-                       v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          st_shared_v4(buf + r * 128u + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4), v[cc][4 * c],
+                       v[cc][4 * c + 1], v[cc][4 * c + 2], v[cc][4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STGFULL + hf));
+        if (lane == 0) mbar_arrive(bar(B_STGFULL + 2 * hf + cc));
         bool full_ok = true;
         if (leader) {
-          full_ok = mbar_wait(bar(B_STGFULL + hf), u & 1, abort_flag, p.status, 0x20a);
+          full_ok = mbar_wait(bar(B_STGFULL + 2 * hf + cc), m & 1, abort_flag, p.status, 0x20a);
           if (full_ok) {
-            tma_reduce_add_2d(&tmdQ, hf * kHalf + cc * 32, row0 + qt * 128, stage);
+            tma_reduce_add_2d(&tmdQ, hf * kHalf + cc * 32, row0 + qt * 128, buf);
             bulk_commit_group();
           }
         }

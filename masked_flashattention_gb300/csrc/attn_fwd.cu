@@ -11,14 +11,19 @@
 //              column half w / 4 of each 128-key S tile, so every query row is handled by a pair
 //              of warps that exchange their partial row maxima through shared memory.  They read
 //              S from TMEM, mask partial tiles, run the online softmax in the log2 domain, write
-//              P (bf16 pairs) back into TMEM, rescale O in TMEM when needed, and finally
-//              normalise O and write O and the LSE.
+//              P (bf16 pairs) back over the S columns they have read, rescale O in TMEM when the
+//              running max moved, and finally normalise O and write O and the LSE.
 //   warp 8     TMA producer: Q once, then K and V of each visited key tile through two 3-slot
 //              rings (a K slot frees when its S MMA completes, a V slot when its PV completes).
 //   warp 9     MMA issuer (one thread): S = Q K^T and O += P V, both with the A operand (Q, P)
 //              read from TMEM and the B operand (K, V) from shared memory, so shared memory
 //              carries only K and V.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+d), P [384, 448), Q [448, 448+d/2).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+d), Q [448, 448+d/2).  P of tile n
+// lives in S buffer n % 2: keys [0,64) in columns [0,32), keys [64,128) in [64,96).
+// Ordering without extra barriers: the MMA issues S(n+2) into a buffer only after it saw P(n) and
+// issued PV(n), which reads P(n) from that buffer; tcgen05 MMAs of one thread run in issue order.
+// The softmax warps wait for PV(n-1) only when they must rescale O: the completion of S(n), which
+// they wait for anyway, already covers every PV issued before it, i.e. up to PV(n-2).
 // The running max is refreshed lazily: O and l are rescaled only when the row max grows by more
 // than 2^8, which keeps P <= 256 and the result exact because O, l and the LSE use the same max.
 #include <cuda_bf16.h>
@@ -41,7 +46,6 @@ constexpr int kMaxTiles = 1024;  // S <= 131072
 
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;
 constexpr uint32_t kColQ = 448;
 
 template <int D>
@@ -66,7 +70,6 @@ enum {
   B_KEMPTY = 8,   // +stage: the S MMA that read the K slot has completed
   B_VEMPTY = 11,  // +stage: the PV MMA that read the V slot has completed
   B_SFULL = 14,   // +buffer
-  B_SFREE = 16,   // +buffer (8 arrivals)
   B_PFULL = 18,   // P in TMEM and O rescaled (8 arrivals)
   B_ODONE = 19,
   B_PAIR = 20,    // +2*quarter+parity: row-max / row-sum exchange of a warp pair (2 arrivals)
@@ -129,7 +132,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SFREE + s), kSoftmaxWarps);
     }
     mbar_init(bar(B_PFULL), kSoftmaxWarps);
     mbar_init(bar(B_ODONE), 1);
@@ -207,7 +209,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sV = sbase + L::kV + st * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_mnmajor(sV, kk, 16384u), idO,
+          umma_ts(tmem + kColO, tmem + kColS + (m & 1) * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sV, kk, 16384u), idO,
                   (m > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_ODONE));
         umma_commit(bar(B_VEMPTY + st));
@@ -217,8 +220,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int st = n % kStages;
         const int sb = n & 1;
         if (!mbar_wait(bar(B_KFULL + st), (n / kStages) & 1, abort_flag, p.status, 0x105)) break;
-        if (n >= 2 && !mbar_wait(bar(B_SFREE + sb), ((n >> 1) - 1) & 1, abort_flag, p.status, 0x106))
-          break;
         tc_fence_after();
         const uint32_t sK = sbase + L::kK + st * L::kTileBytes;
 #pragma unroll
@@ -314,9 +315,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           s[32 + c] = __uint_as_float(t1[c]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SFREE + sb));
 
       const int entry = list[n];
       if (!(entry & 0x8000)) {
@@ -363,13 +361,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       l_half = l_half * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
-      if (n >= 1) {
-        // PV of the previous tile must be complete: O is stable and the P columns are free
+      if (n >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // rescale O: PV(n-1) must be complete (PV(n-2) and earlier are, since S(n) is)
         const bool o_ready = mbar_wait(bar(B_ODONE), (n - 1) & 1, abort_flag, p.status, 0x108);
         __syncwarp();
         if (!o_ready) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        {
 #pragma unroll
           for (int c = 0; c < kHalf; c += 32) {
             uint32_t o[32];
@@ -381,7 +379,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
       }
-      tmem_st32(tmem + lane_off + kColP + 32 * hf, pk);
+      // P over the S columns this warp has read: keys [64*hf, +64) -> columns [64*hf, +32)
+      tmem_st32(tmem + lane_off + kColS + sb * 128 + 64 * hf, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

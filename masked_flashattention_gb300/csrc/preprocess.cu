@@ -116,9 +116,8 @@ __global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant
 
 // Longest-first order of tile rows by counting sort on the number of non-empty tiles (0..NT),
 // which the descriptor kernel left in the schedule array itself: the counts are staged in shared
-// memory, histogrammed, scanned in descending order, and each row is placed.  Lanes of a warp
-// with equal counts share one shared-memory atomic.  Rows with equal counts may come in any
-// order.  One block of 1024 threads per direction; NT <= 1024 and B * NT <= 32768.
+// memory, histogrammed, scanned in descending order, and each row is placed.  Rows with equal
+// counts may come in any order.  One block of 1024 threads per direction; NT <= 1024 and B * NT <= 32768.
 __global__ void __launch_bounds__(1024) schedule_kernel(int32_t* sched_f, int32_t* sched_b, int B,
                                                         int NT) {
   extern __shared__ uint16_t s_cnt[];  // [B * NT]
@@ -132,15 +131,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(int32_t* sched_f, int32_
   for (int c = t; c <= NT; c += blockDim.x) hist[c] = 0;
   for (int it = t; it < n; it += blockDim.x) s_cnt[it] = static_cast<uint16_t>(sched[it]);
   __syncthreads();
-  // whole rounds of blockDim.x so that every lane reaches the warp-wide calls; lanes past the
-  // end carry the key -1 and add nothing
-  const int rounds = (n + blockDim.x - 1) / blockDim.x;
-  for (int q = 0; q < rounds; ++q) {
-    const int it = q * blockDim.x + t;
-    const int key = it < n ? s_cnt[it] : -1;
-    const unsigned peers = __match_any_sync(full, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
-  }
+  for (int it = t; it < n; it += blockDim.x) atomicAdd(&hist[s_cnt[it]], 1);
   __syncthreads();
   // thread t owns count NT - t (t < NT): inclusive scan in descending count order
   const int c = NT - t;
@@ -169,15 +160,9 @@ __global__ void __launch_bounds__(1024) schedule_kernel(int32_t* sched_f, int32_
   if (t < NT) hist[c] = incl - v;   // first position of count c
   if (t == NT - 1) hist[0] = incl;  // rows without tiles go last
   __syncthreads();
-  for (int q = 0; q < rounds; ++q) {
-    const int it = q * blockDim.x + t;
-    const int key = it < n ? s_cnt[it] : -1;
-    const unsigned peers = __match_any_sync(full, key);
-    const int leader = __ffs(peers) - 1;
-    int base = 0;
-    if (key >= 0 && lane == leader) base = atomicAdd(&hist[key], __popc(peers));
-    base = __shfl_sync(full, base, leader);
-    if (key >= 0) sched[base + __popc(peers & ((1u << lane) - 1u))] = ((it / NT) << 16) | (it % NT);
+  for (int it = t; it < n; it += blockDim.x) {
+    const int pos = atomicAdd(&hist[s_cnt[it]], 1);
+    sched[pos] = ((it / NT) << 16) | (it % NT);
   }
 }
 
