@@ -389,12 +389,14 @@ def run_gpu(args):
                        "preprocess_gbs": prep_bytes / (build_ms / 1e3) / 1e9,
                        "preprocess_sweep": sweep,
                        "peak_source": f"{peak_src} bf16_tflops_sustained"},
-            "roofline": {"bound": "tensor", "kernel": "attention backward (prologue + main + dQ convert)",
+            "roofline": {"bound": "tensor", "kernel": "attention backward (prologue + dK/dV kernel + dQ kernel)",
                          "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": bwd_tf / peak, "traffic": traffic},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 6 * args.steps,
+            # per step: descriptor (2 generated kernels + schedule), forward, backward (prologue,
+            # dK/dV, dQ)
+            "gpu_launches": 7 * args.steps,
             "clocks": clk,
         }
         if world == 1 and not args.no_cpu_baseline:

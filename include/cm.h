@@ -50,7 +50,8 @@ enum {
   CM_ERR_UNSUPPORTED = -3,  /* valid request outside the supported shapes (d, S, tile, limits) */
   CM_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
   CM_ERR_TIMEOUT = -5,      /* device status: a bounded wait inside a kernel expired */
-  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation */
+  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation (or a kernel found its
+                               shared memory misaligned and did nothing) */
 };
 
 /* Opaque compiled MaskSpec (host memory, owned by the caller after cm_compile_spec). */
@@ -160,14 +161,16 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
                        void* o, float* lse, int B, int H, int S, int d, float scale,
                        void* stream);
 
-/* Workspace bytes cm_attn_bwd needs: per-row D = rowsum(dO * O) and LSE * log2(e) (fp32), and the
- * fp32 dQ accumulator. */
+/* Workspace bytes cm_attn_bwd needs: per-row D = rowsum(dO * O) and LSE * log2(e), fp32 (8 bytes
+ * per row of B*H*S, each array rounded up to 256 bytes). */
 CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes);
 
 /* Backward: dq, dk, dv (device bf16 [B][H][S][d]) of sum(o * dO) given the forward's o and lse.
- * Uses the forward descriptor's itab_f/bm_f for nothing but validation and the backward half
- * (itab_b, bm_b, sched_b) to traverse key tiles.  `workspace` (device, >= the size above,
- * 16-byte aligned) is overwritten. */
+ * Three kernels: a prologue (D, LSE * log2(e) into the workspace), dK and dV along key tiles with
+ * the backward half of the descriptor (itab_b, bm_b, sched_b), and dQ along query tiles with the
+ * forward half (itab_f, bm_f, sched_f).  Every output element is written exactly once (no
+ * atomics), so results are deterministic.  `workspace` (device, >= the size above, 16-byte
+ * aligned) is overwritten. */
 CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
                        const void* o, const float* lse, const void* d_o, void* dq, void* dk,
                        void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
@@ -184,13 +187,13 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
  * scratch comes from a fixed file-scope device array inside the library instead, so this call
  * allocates nothing.
  *   - Limit: the workspace cm_attn_bwd_workspace_size reports must fit CM_NOALLOC_SCRATCH_BYTES
- *     (e.g. B*H*S <= 64527 rows at d = 128); larger problems return CM_ERR_UNSUPPORTED and queue
+ *     (B*H*S <= 4,194,304 rows); larger problems return CM_ERR_UNSUPPORTED and queue
  *     nothing.
  *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call on each
  *     device, with that device current; make that first call before any stream capture.
  *   - The array is held by every GPU that loads the library until the process exits.
  *   - All calls share the one array per device, and it keeps the previous call's contents (each
- *     call re-initialises what must start at zero).  Calls whose work overlaps on the GPU, e.g.
+ *     call rewrites all of it before reading it).  Calls whose work overlaps on the GPU, e.g.
  *     on two streams, race on it: order them on one stream. */
 CM_API int cm_attn_bwd_noalloc(const cm_descriptor* desc, const void* q, const void* k,
                                const void* v, const void* o, const float* lse, const void* d_o,

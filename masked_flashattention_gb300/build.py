@@ -16,9 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcm.so")
 
-SOURCES = ["compiler.cpp", "codegen.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "api.cu",
+SOURCES = ["compiler.cpp", "codegen.cpp", "preprocess.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_dq.cu", "api.cu",
            "attn_bwd_noalloc.cu"]
-HEADERS = ["program.h", "kernels.h", "ptx.cuh", "tma_host.h", "descriptor_core.cuh"]
+HEADERS = ["program.h", "kernels.h", "ptx.cuh", "tma_host.h", "descriptor_core.cuh", "mask.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -48,7 +48,7 @@ CM_API const char* cm_error_string(int code) {
     case CM_ERR_UNSUPPORTED: return "unsupported shape or limit";
     case CM_ERR_CUDA: return "CUDA runtime error";
     case CM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
-    case CM_ERR_DEVICE_CHECK: return "segment metadata failed device-side validation";
+    case CM_ERR_DEVICE_CHECK: return "a device-side check failed (segment metadata, or shared-memory alignment)";
     default: return "unknown error";
   }
 }
@@ -143,7 +143,7 @@ CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes)
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
   const size_t rows = static_cast<size_t>(B) * H * S;
   const size_t row_floats = (rows * 4 + 255) / 256 * 256;  // D, then LSE * log2(e)
-  *bytes = 2 * row_floats + rows * d * 4;
+  *bytes = 2 * row_floats;
   return CM_OK;
 }
 
@@ -176,7 +176,6 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.lse = lse;
   p.delta = static_cast<float*>(workspace);
   p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + row_floats);
-  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * row_floats);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.B = B;
@@ -187,9 +186,25 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.NI = desc->ni_b;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return cm::launch_attn_bwd(p, d, q, k, v, o, d_o, dq, static_cast<cudaStream_t>(stream)) == 0
-             ? CM_OK
-             : CM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cm::launch_attn_bwd(p, d, q, k, v, o, d_o, st) != 0) return CM_ERR_CUDA;
+  cm::DqParams g;
+  g.itab = desc->itab_f;
+  g.bm = desc->bm_f;
+  g.sched = desc->sched_f;
+  g.status = desc->status;
+  g.delta = p.delta;
+  g.lse2 = p.lse2;
+  g.dq = static_cast<__nv_bfloat16*>(dq);
+  g.B = B;
+  g.H = H;
+  g.S = S;
+  g.NT = p.NT;
+  g.W = p.W;
+  g.NI = desc->ni_f;
+  g.scale = scale;
+  g.scale_log2 = p.scale_log2;
+  return cm::launch_attn_dq(g, d, q, k, v, d_o, st) == 0 ? CM_OK : CM_ERR_CUDA;
 }
 
 CM_API int cm_get_status(const cm_descriptor* desc, void* stream) {

@@ -1,4 +1,5 @@
-// Descriptor-guided attention, backward (CompileMask sections 3.2.2 / 3.3 / 3.3.2), for sm_103a.
+// Descriptor-guided attention, backward, dK and dV (CompileMask sections 3.2.2 / 3.3 / 3.3.2),
+// for sm_103a.
 //
 // The backward pass traverses key tiles, so it uses the backward descriptor: per key column j,
 // the visible query intervals, and per (key tile, query tile) the 2-bit state.  One CTA owns one
@@ -8,7 +9,9 @@
 //   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
 //   dK  += dS^T Q           (TMEM accumulator)
 //   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
-//   dQ_part = dS K          (TMEM) -> shared memory -> TMA bulk add into the fp32 dQ accumulator
+//
+// dQ is computed by a second kernel that walks query tiles (attn_dq.cu); adding every key tile's
+// dQ partial into an fp32 accumulator here would make L2 read-modify-write traffic the bound.
 //
 // Partial tiles check each query index against the key column's intervals with the unsigned
 // test of section 4.4 and zero P there (the -inf of the forward); full tiles skip the check.
@@ -16,27 +19,24 @@
 //
 // Warp roles (320 threads):
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
-//              half w / 4: queries [64*half, +64) of S^T / dP^T, and head-dim columns
-//              [half*d/2, +d/2) of dQ_part, dV and dK.
-//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) into one of
-//              two slots, and dO (+ D).
+//              half w / 4: queries [64*half, +64) of S^T / dP^T and head-dim columns
+//              [half*d/2, +d/2) of dV and dK.
+//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) and dO
+//              (+ D), each into one of two slots.
 //   warp 9     MMA issuer (one thread).
 // TMEM (512 columns): dV [0, d), dK [128, 128+d), and two 128-column regions RA [256, 384),
 // RB [384, 512) whose roles alternate between query tiles.  For tile m with X = RA (m even) or
 // RB (m odd) and Y the other one:
 //   S^T(m) -> X; the compute warps overwrite it in place with the bf16 P^T pairs (each warp
 //   writes only columns it has already read); dP^T(m) -> Y.
-//   After the compute warps hand over P^T and dS^T, the MMA issues dV(m) (reads P^T from X),
-//   dK(m), S^T(m+1) -> Y (free: dP^T(m) was consumed), dQ_part(m) -> X (after dV read P^T), and,
-//   once dQ_part(m) has been read out, dP^T(m+1) -> X.
-// So the next tile's S^T is computed while the compute warps wait for dQ_part, and its dP^T while
-// they stage dQ_part and compute P(m+1): the tensor pipe does not idle for the whole P/dS phase.
-// Shared memory: K, V, Q (two slots), dO, dS^T (bf16, 128-byte swizzle), one 16 KB fp32 staging
-// tile per column half for the dQ bulk adds, LSE*log2e (per Q slot) and D of the current tile, and
-// the CTA's row of the backward bitmap (the non-empty query tiles are found by scanning it).
-// dQ_part is read out of TMEM at once; each half stages its first 32-column chunk in its staging
-// tile and the second in its dS^T box (idle from the dQ_part MMA until the next tile's dS^T), so
-// the bulk adds of one tile overlap the next tile's P/dS work.
+//   Once the compute warps have handed over P^T and dS^T, the MMA issues S^T(m+1) -> Y (its
+//   dP^T was consumed), dV(m) (reads P^T from X), dK(m), and dP^T(m+1) -> X (after dV read it).
+// So the compute warps start on the next tile's P while the tensor pipe runs dV and dK.
+// Shared memory (d = 128: 231,808 bytes, no room for alignment slack, so the kernel checks that
+// its dynamic shared memory starts on a 1024-byte boundary and exits with a status otherwise):
+// K, V, Q and dO (two slots each), dS^T (bf16, 128-byte swizzle), LSE*log2e and D (per slot),
+// barriers, and the CTA's row of the backward bitmap (the non-empty query tiles are found by
+// scanning it).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -67,15 +67,14 @@ struct Smem {
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTileBytes;
   static constexpr uint32_t kQ = 2 * kTileBytes;      // two slots
-  static constexpr uint32_t kdO = 4 * kTileBytes;
-  static constexpr uint32_t kdSt = 5 * kTileBytes;    // [2 boxes][128 keys][64 queries] bf16
-  static constexpr uint32_t kStage = kdSt + 32768u;   // fp32 [2 halves][128 rows][32 cols]
-  static constexpr uint32_t kLse2 = kStage + 32768u;  // [2 slots][128 floats]: -LSE * log2(e)
-  static constexpr uint32_t kDelta = kLse2 + 1024u;   // 128 floats: -D
-  static constexpr uint32_t kBar = kDelta + 512u;
-  static constexpr uint32_t kRow = kBar + 256u;       // bitmap row: at most 64 words (NT <= 1024)
+  static constexpr uint32_t kdO = 4 * kTileBytes;      // two slots
+  static constexpr uint32_t kdSt = 6 * kTileBytes;     // [2 boxes][128 keys][64 queries] bf16
+  static constexpr uint32_t kLse2 = kdSt + 32768u;     // [2 slots][128 floats]: -LSE * log2(e)
+  static constexpr uint32_t kDelta = kLse2 + 1024u;    // [2 slots][128 floats]: -D
+  static constexpr uint32_t kBar = kDelta + 1024u;
+  static constexpr uint32_t kRow = kBar + 128u;        // bitmap row: at most 64 words (NT <= 1024)
   static constexpr uint32_t kTotal = kRow + 256u;
-  static constexpr uint32_t kAlloc = kTotal + 1024u;  // + slack to align the base to 1024 bytes
+  static constexpr uint32_t kAlloc = kTotal;
 };
 static_assert(Smem<128>::kAlloc <= 232448, "backward shared memory exceeds 227 KB");
 
@@ -83,16 +82,13 @@ enum {
   B_KV = 0,        // K and V loaded
   B_QFULL = 1,     // +slot: Q and LSE*log2e of a query tile loaded
   B_QEMPTY = 3,    // +slot: the dK MMA (last reader of that Q slot) is done
-  B_DOFULL = 5,    // dO and D of the current query tile loaded
-  B_DOEMPTY = 6,   // the dV MMA (last reader of dO) of the current tile is done
-  B_SFULL = 7,     // S^T of the current tile computed
-  B_DPFULL = 8,    // dP^T of the current tile computed
-  B_PDS = 9,       // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
-  B_DQFULL = 10,   // dQ_part computed (and every earlier MMA done)
-  B_DQREAD = 11,   // compute warps read dQ_part from TMEM (8 arrivals)
-  B_STGFREE = 12,  // +2*half+buffer: the buffer may be written (the half's leader, 1 arrival)
-  B_STGFULL = 16,  // +2*half+buffer: the half's 4 warps wrote their rows (4 arrivals)
-  B_COUNT = 20
+  B_DOFULL = 5,    // +slot: dO and D of a query tile loaded
+  B_DOEMPTY = 7,   // +slot: the dV MMA (last reader of that dO slot) is done
+  B_SFULL = 9,     // S^T of the current tile computed
+  B_DPFULL = 10,   // dP^T of the current tile computed
+  B_PDS = 11,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
+  B_DONE = 12,     // every MMA of the CTA completed (dK, dV final)
+  B_COUNT = 13
 };
 
 // first query tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
@@ -190,14 +186,15 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ BwdParams p) {
+                const __grid_constant__ BwdParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;           // head-dim columns per compute warp
-  constexpr int kChunks = kHalf / 32;    // 32-column dQ chunks per warp
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if ((sbase & 1023u) != 0) {  // the 128-byte swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, kDevSmemAlign, 0x2ff);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
@@ -219,18 +216,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_QFULL + x), 1);
       mbar_init(bar(B_QEMPTY + x), 1);
+      mbar_init(bar(B_DOFULL + x), 1);
+      mbar_init(bar(B_DOEMPTY + x), 1);
     }
-    for (int x = 0; x < 4; ++x) {
-      mbar_init(bar(B_STGFREE + x), 1);
-      mbar_init(bar(B_STGFULL + x), 4);
-    }
-    mbar_init(bar(B_DOFULL), 1);
-    mbar_init(bar(B_DOEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PDS), kComputeWarps);
-    mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQREAD), kComputeWarps);
+    mbar_init(bar(B_DONE), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -263,7 +255,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      tma_prefetch_desc(&tmdQ);
       mbar_arrive_expect_tx(bar(B_KV), 2 * L::kTileBytes);
       for (int x = 0; x < D / 64; ++x) {
         tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
@@ -273,8 +264,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int m = 0; m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
         const int slot = m & 1;
         const size_t r = static_cast<size_t>(row0) + qt * 128;
-        // a Q slot is free once the dK MMA of the tile two back is done; dO once the previous
-        // tile's dV MMA is done
+        // a Q slot is free once the dK MMA of the tile two back is done, a dO slot once its dV
+        // MMA is done
         if (m >= 2 && !mbar_wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x201))
           break;
         mbar_arrive_expect_tx(bar(B_QFULL + slot), L::kTileBytes + 512u);
@@ -282,11 +273,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
                       row0 + qt * 128, bar(B_QFULL + slot));
         bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, bar(B_QFULL + slot));
-        if (m >= 1 && !mbar_wait(bar(B_DOEMPTY), (m - 1) & 1, abort_flag, p.status, 0x20b)) break;
-        mbar_arrive_expect_tx(bar(B_DOFULL), L::kTileBytes + 512u);
+        if (m >= 2 && !mbar_wait(bar(B_DOEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x20b))
+          break;
+        mbar_arrive_expect_tx(bar(B_DOFULL + slot), L::kTileBytes + 512u);
         for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kdO + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_DOFULL));
-        bulk_load(sbase + L::kDelta, p.delta + r, 512u, bar(B_DOFULL));
+          tma_load_2d(sbase + L::kdO + slot * L::kTileBytes + x * 16384u, &tmdO, x * 64,
+                      row0 + qt * 128, bar(B_DOFULL + slot));
+        bulk_load(sbase + L::kDelta + slot * 512u, p.delta + r, 512u, bar(B_DOFULL + slot));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -294,9 +287,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
-      constexpr uint32_t idMM = make_idesc_bf16(128, D, 1, 1);    // dQ_part
-      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdO = sbase + L::kdO,
-                     sdSt = sbase + L::kdSt;
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdSt = sbase + L::kdSt;
       // tile 0: S^T -> RA, dP^T -> RB
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202) &&
                 mbar_wait(bar(B_QFULL), 0, abort_flag, p.status, 0x203);
@@ -313,30 +304,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColRB, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
-                  kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColRB, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sbase + L::kdO, kk, 16384u),
+                  idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_DPFULL));
       }
       for (int m = 0; ok && m < nt; ++m) {
         const uint32_t X = (m & 1) ? kColRB : kColRA;
         const uint32_t Y = (m & 1) ? kColRA : kColRB;
         const uint32_t sQ = sbase + L::kQ + (m & 1) * L::kTileBytes;
+        const uint32_t sdO = sbase + L::kdO + (m & 1) * L::kTileBytes;
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
-        // dV += P^T dO; P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DOEMPTY));
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
-                  (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY + (m & 1)));
         if (m + 1 < nt) {
-          // S^T of the next tile into Y, whose dP^T the compute warps have consumed
+          // S^T of the next tile first, into Y (its dP^T was consumed), so that the compute warps
+          // can start on it while the tensor pipe runs dV and dK
           const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
           if (!mbar_wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x203))
             break;
@@ -347,22 +328,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_SFULL));
         }
-        // dQ_part = dS K into X, after the dV MMA above has read P^T from it
+        // dV += P^T dO; P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + X, sdesc_mnmajor(sdSt, kk, 16384u), sdesc_mnmajor(sK, kk, 16384u), idMM,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar(B_DQFULL));
+          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_DOEMPTY + (m & 1)));
+        // dK += dS^T Q
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_QEMPTY + (m & 1)));
         if (m + 1 < nt) {
-          // dP^T of the next tile into X once dQ_part has been read out of it
-          if (!mbar_wait(bar(B_DOFULL), (m + 1) & 1, abort_flag, p.status, 0x20c)) break;
-          if (!mbar_wait(bar(B_DQREAD), m & 1, abort_flag, p.status, 0x204)) break;
+          // dP^T of the next tile into X, after the dV MMA above has read P^T from it
+          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
+          if (!mbar_wait(bar(B_DOFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x20c))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdO, kk, 16384u), idSS,
+            umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdOn, kk, 16384u), idSS,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_DPFULL));
+        } else {
+          umma_commit(bar(B_DONE));
         }
       }
     }
@@ -370,13 +360,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // ---------------------------------------------------------------- compute warps 0-7
     const int quarter = warp & 3;
     const int hf = warp >> 2;
-    const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_part)
+    const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK)
     const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool leader = (quarter == 0 && lane == 0);  // issues this half's bulk adds
-    // staging buffers of this half: chunk 0 in the staging tile, chunk 1 in the half's dS^T box,
-    // which nothing reads between the dQ_part MMA and the next tile's dS^T
-    const uint32_t stage_buf[2] = {sbase + L::kStage + hf * 16384u, sbase + L::kdSt + hf * 16384u};
     int st[4];
     uint32_t len[4];
 #pragma unroll
@@ -397,12 +383,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint32_t X = (m & 1) ? kColRB : kColRA;
       const uint32_t Y = (m & 1) ? kColRA : kColRB;
 
-      // the previous tile's chunk-0 bulk add has read the staging tile: free it for this tile
-      if (leader) {
-        if (kChunks == 2) bulk_wait_read_but1();  // the chunk-1 add may still be reading
-        else bulk_wait_read_all();
-        mbar_arrive(bar(B_STGFREE + 2 * hf));
-      }
       // ---- P^T: S^T from X, written back in place as bf16 pairs; fp32 P kept for dS ----
       bool ready = mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206) &&
                    mbar_wait(bar(B_QFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x207);
@@ -435,14 +415,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
 
       // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T into this half's box ----
-      if (leader) {
-        // the previous tile's chunk-1 bulk add has read the dS^T box
-        bulk_wait_read_all();
-        mbar_arrive(bar(B_STGFREE + 2 * hf + 1));
-      }
       ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e) &&
-              mbar_wait(bar(B_DOFULL), m & 1, abort_flag, p.status, 0x20d) &&
-              mbar_wait(bar(B_STGFREE + 2 * hf + 1), m & 1, abort_flag, p.status, 0x209);
+              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -452,7 +426,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint32_t dpr[32], dd[16];
         tmem_ld32(tmem + lane_off + Y + q0, dpr);
         tmem_wait_ld();
-        ds_chunk(pf[ch], dpr, sbase + L::kDelta + q0 * 4u, dd);
+        ds_chunk(pf[ch], dpr, sbase + L::kDelta + (m & 1) * 512u + q0 * 4u, dd);
         // dS^T row r, queries q0..q0+31 = four 16-byte chunks of box hf
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -467,54 +441,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PDS));
 
-      // ---- dQ_part from X: query row r, head-dim columns [hf * kHalf, +kHalf), read at once ----
-      ready = mbar_wait(bar(B_DQFULL), m & 1, abort_flag, p.status, 0x208);
-      __syncwarp();
-      if (!ready) { ok = false; break; }
-      tc_fence_after();
-      uint32_t v[kChunks][32];
-#pragma unroll
-      for (int cc = 0; cc < kChunks; ++cc) tmem_ld32(tmem + lane_off + X + hf * kHalf + cc * 32, v[cc]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DQREAD));  // X may be overwritten now
-#pragma unroll
-      for (int cc = 0; cc < kChunks; ++cc) {
-        // chunk 0 waits for its staging tile; chunk 1 uses the dS^T box, free since DQFULL
-        if (cc == 0) {
-          const bool free_ok = mbar_wait(bar(B_STGFREE + 2 * hf), m & 1, abort_flag, p.status, 0x209);
-          __syncwarp();
-          if (!free_ok) { ok = false; break; }
-        }
-        const uint32_t buf = stage_buf[cc];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(buf + r * 128u + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4), v[cc][4 * c],
-                       v[cc][4 * c + 1], v[cc][4 * c + 2], v[cc][4 * c + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STGFULL + 2 * hf + cc));
-        bool full_ok = true;
-        if (leader) {
-          full_ok = mbar_wait(bar(B_STGFULL + 2 * hf + cc), m & 1, abort_flag, p.status, 0x20a);
-          if (full_ok) {
-            tma_reduce_add_2d(&tmdQ, hf * kHalf + cc * 32, row0 + qt * 128, buf);
-            bulk_commit_group();
-          }
-        }
-        full_ok = __shfl_sync(0xFFFFFFFFu, full_ok, 0);
-        if (!full_ok) { ok = false; break; }
-      }
     }
-    if (leader) bulk_wait_all();
     __syncwarp();
 
     // ---- epilogue: dV, dK (scaled) -> bf16, this warp's half of the head dim ----
     __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
     __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
-    if (nt > 0 && ok) {
-      // the last DQFULL wait above guarantees every MMA of this CTA has completed
+    const bool done = nt > 0 && ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status, 0x20f);
+    __syncwarp();
+    if (done) {
+      tc_fence_after();
 #pragma unroll
       for (int c = 0; c < kHalf; c += 32) {
         uint32_t a[32], k2[32];
@@ -556,15 +492,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// Per row, negated for the main kernel's paired FMAs: -D = -sum_c dO[c] * O[c] (fp32) and
-// -LSE * log2(e) (-inf for a row that sees nothing, so that its P is exp2(-inf) = 0); and a zeroed
-// dQ accumulator row.  One warp per row.
+// Per row, negated for the paired FMAs of the backward kernels: -D = -sum_c dO[c] * O[c] (fp32)
+// and -LSE * log2(e) (-inf for a row that sees nothing, so that its P is exp2(-inf) = 0).  One
+// warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* o,
                                                            const __nv_bfloat16* d_o,
                                                            const float* lse, float* delta,
-                                                           float* lse2, float* dq_acc,
-                                                           size_t rows) {
+                                                           float* lse2, size_t rows) {
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -581,48 +516,28 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* 
     const float l = lse[row];
     lse2[row] = l == -INFINITY ? -INFINITY : -l * kLog2e;
   }
-  float* z = dq_acc + row * D + lane * kPer;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) z[e] = 0.f;
-}
-
-// dQ = bf16(scale * dQ_acc), 8 elements per thread
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* dq_acc, __nv_bfloat16* dq,
-                                                         size_t n8, float scale) {
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
-  const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
-  uint4 v;
-  v.x = pack_bf16x2(a.x * scale, a.y * scale);
-  v.y = pack_bf16x2(a.z * scale, a.w * scale);
-  v.z = pack_bf16x2(c.x * scale, c.y * scale);
-  v.w = pack_bf16x2(c.z * scale, c.w * scale);
-  reinterpret_cast<uint4*>(dq)[t] = v;
 }
 
 }  // namespace bwd
 
 int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
-                    const void* o, const void* d_o, void* dq, cudaStream_t stream) {
+                    const void* o, const void* d_o, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
-  // prologue: D, LSE * log2(e) and the zeroed accumulator
   {
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
     if (d == 128)
       bwd::bwd_prologue_kernel<128><<<blocks, 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
-          p.delta, p.lse2, p.dq_acc, rows);
+          p.delta, p.lse2, rows);
     else
       bwd::bwd_prologue_kernel<64><<<blocks, 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
-          p.delta, p.lse2, p.dq_acc, rows);
+          p.delta, p.lse2, rows);
     if (cudaGetLastError() != cudaSuccess) return -1;
   }
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo;
   if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
-      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d) ||
-      !make_f32_tile_map(&mdq, p.dq_acc, rows, d))
+      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
     return -1;
   const dim3 grid(p.B * p.NT * p.H);
   if (d == 128) {
@@ -630,18 +545,14 @@ int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, con
     if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return -1;
-    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
+    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
   } else {
     const uint32_t smem = bwd::Smem<64>::kAlloc;
     if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return -1;
-    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, p);
+    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
   }
-  if (cudaGetLastError() != cudaSuccess) return -1;
-  const size_t n8 = rows * d / 8;
-  bwd::dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, p.scale);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

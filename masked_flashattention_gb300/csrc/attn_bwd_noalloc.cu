@@ -3,7 +3,8 @@
 // Some callers of this library run inside a host framework that owns all device memory and
 // forbids its plugins to allocate (a fixed memory budget handed out up front), or on a
 // latency-critical thread where cudaMalloc's implicit device synchronisation is not acceptable.
-// They can still pass their own inputs and outputs, but not the fp32 workspace cm_attn_bwd needs.
+// They can still pass their own inputs and outputs, but not the fp32 workspace cm_attn_bwd needs
+// (per-row D and LSE * log2(e)).
 // cm_attn_bwd_noalloc serves them from a fixed scratch array that lives in this file's device
 // module instead of a caller buffer.
 //
@@ -12,8 +13,9 @@
 // device address, so the address is looked up once per device with cudaGetSymbolAddress (with
 // that device current) and cached; the first call on a device does that lookup, so it should come
 // before any stream capture.  All calls share the array and it keeps the last call's contents:
-// the backward's prologue kernel rewrites D and zeroes the dQ accumulator at the start of every
-// call, and calls whose work overlaps on the GPU (e.g. on different streams) race on the array.
+// the backward's prologue kernel rewrites D and LSE * log2(e) at the start of every call before
+// anything reads them, and calls whose work overlaps on the GPU (e.g. on different streams) race
+// on the array.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <mutex>

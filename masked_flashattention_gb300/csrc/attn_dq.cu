@@ -1,0 +1,387 @@
+// Descriptor-guided attention, backward, dQ part (CompileMask sections 3.3.2 / 4.4), for sm_103a.
+//
+// dQ = scale * sum over key tiles of dS K, with dS = P * (dP - D), P = exp(scale * Q K^T - LSE)
+// and dP = dO V^T.  The main backward kernel walks key tiles (it owns dK and dV); accumulating dQ
+// there would need an fp32 read-modify-write of every (key tile, query tile) partial in L2, and on
+// GB300 that traffic limits the whole backward.  This kernel walks query tiles instead, like the
+// forward: one CTA owns one 128-row query tile of one (sample, head), visits the key tiles of the
+// forward bitmap row (empty tiles skipped, full tiles unmasked, partial tiles checked with the
+// unsigned interval test against the forward Interval Table), recomputes S and dP, and keeps dQ
+// in TMEM.  It writes dQ once, in bf16, with no atomics.
+//
+// Warp roles (320 threads):
+//   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (query rows 32*(w%4) ..) and
+//              column half w / 4 of each 128-key tile: P = exp2(S * scale*log2e - LSE*log2e),
+//              dS = P * (dP - D), written back as bf16 pairs over the S columns it has read.
+//   warp 8     TMA producer: Q and dO once; K through a 3-slot ring, V through a 2-slot ring.
+//   warp 9     MMA issuer (one thread).  Per key tile n: S(n+1) = Q K^T into the other S buffer,
+//              dQ += dS(n) K(n) (A operand dS from TMEM), dP(n+1) = dO V^T.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), dP [256,384), dQ [384, 384+d).
+// A buffer is rewritten only by MMAs issued after the ones that read it: tcgen05 MMAs of one
+// thread run in issue order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "mask.cuh"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace cm {
+namespace dq {
+
+constexpr int kComputeWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColDP = 256;
+constexpr uint32_t kColDQ = 384;
+
+template <int D>
+struct Smem {
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kdO = kTileBytes;
+  static constexpr uint32_t kK = 2 * kTileBytes;                    // kKStages slots
+  static constexpr uint32_t kV = kK + kKStages * kTileBytes;        // kVStages slots
+  static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
+  static constexpr uint32_t kRow = kBar + 256u;                     // bitmap row (<= 64 words)
+  static constexpr uint32_t kTotal = kRow + 256u;
+  static constexpr uint32_t kAlloc = kTotal + 1024u;                // slack for 1024-byte alignment
+};
+static_assert(Smem<128>::kAlloc <= 232448, "dQ kernel shared memory exceeds 227 KB");
+
+enum {
+  B_QDO = 0,      // Q and dO loaded
+  B_KFULL = 1,    // +slot (3)
+  B_KEMPTY = 4,   // +slot (3): the dQ MMA that last read the K slot is done
+  B_VFULL = 7,    // +slot (2)
+  B_VEMPTY = 9,   // +slot (2): the dP MMA that read the V slot is done
+  B_SFULL = 11,   // +buffer (2)
+  B_DPFULL = 13,  // dP of the current tile computed
+  B_DSFULL = 14,  // compute warps wrote dS and read dP (8 arrivals)
+  B_DONE = 15,    // every MMA of the CTA completed
+  B_COUNT = 16
+};
+
+// first key tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
+__device__ __forceinline__ int next_tile(const uint32_t* row, int NT, int c) {
+  while (c < NT) {
+    const int w = c >> 4;
+    uint32_t x = row[w];
+    x = (x | (x >> 1)) & 0x55555555u;
+    x &= 0xFFFFFFFFu << (2 * (c & 15));
+    if (x != 0) return (w << 4) + ((__ffs(x) - 1) >> 1);
+    c = (w + 1) << 4;
+  }
+  return NT;
+}
+__device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
+  return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+               const __grid_constant__ DqParams p) {
+  using L = Smem<D>;
+  constexpr int kHalf = D / 2;  // dQ columns per compute warp
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
+  int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
+  uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = p.sched[blockIdx.x / p.H];
+  const int h = blockIdx.x % p.H;
+  const int b = item >> 16;
+  const int qt = item & 0xFFFF;
+  const int bh = b * p.H + h;
+  const int row0 = bh * p.S;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_QDO), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFULL + 1), 1);
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_DSFULL), kComputeWarps);
+    mbar_init(bar(B_DONE), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    // this CTA's forward bitmap row (W <= 64 words) and its count of non-empty key tiles
+    const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + qt) * p.W;
+    int cnt = 0;
+    for (int w = lane; w < p.W; w += 32) {
+      const uint32_t x = row[w];
+      bmrow[w] = x;
+      cnt += __popc((x | (x >> 1)) & 0x55555555u);
+    }
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    if (lane == 0) *s_ntiles = cnt;
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nt = *s_ntiles;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(B_QDO), 2 * L::kTileBytes);
+      for (int x = 0; x < D / 64; ++x) {
+        tma_load_2d(sbase + L::kQ + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QDO));
+        tma_load_2d(sbase + L::kdO + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_QDO));
+      }
+      int kt = next_tile(bmrow, p.NT, 0);
+      for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
+        const int sk = n % kKStages, sv = n % kVStages;
+        if (n >= kKStages &&
+            !mbar_wait(bar(B_KEMPTY + sk), ((n / kKStages) - 1) & 1, abort_flag, p.status, 0x301))
+          break;
+        mbar_arrive_expect_tx(bar(B_KFULL + sk), L::kTileBytes);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kK + sk * L::kTileBytes + x * 16384u, &tmK, x * 64,
+                      row0 + kt * 128, bar(B_KFULL + sk));
+        if (n >= kVStages &&
+            !mbar_wait(bar(B_VEMPTY + sv), ((n / kVStages) - 1) & 1, abort_flag, p.status, 0x302))
+          break;
+        mbar_arrive_expect_tx(bar(B_VFULL + sv), L::kTileBytes);
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_2d(sbase + L::kV + sv * L::kTileBytes + x * 16384u, &tmV, x * 64,
+                      row0 + kt * 128, bar(B_VFULL + sv));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t idQ = make_idesc_bf16(128, D, 0, 1);    // dQ += dS K
+      const uint32_t sQ = sbase + L::kQ, sdO = sbase + L::kdO;
+      auto issue_s = [&](int n) -> bool {  // S(n) into buffer n % 2
+        const int sk = n % kKStages;
+        if (!mbar_wait(bar(B_KFULL + sk), (n / kKStages) & 1, abort_flag, p.status, 0x303)) return false;
+        tc_fence_after();
+        const uint32_t sK = sbase + L::kK + sk * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColS + (n & 1) * 128, sdesc_kmajor(sQ, kk, 16384u),
+                  sdesc_kmajor(sK, kk, 16384u), idS, kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL + (n & 1)));
+        return true;
+      };
+      auto issue_dp = [&](int n) -> bool {  // dP(n); the compute warps have read dP(n-1)
+        const int sv = n % kVStages;
+        if (!mbar_wait(bar(B_VFULL + sv), (n / kVStages) & 1, abort_flag, p.status, 0x304)) return false;
+        tc_fence_after();
+        const uint32_t sV = sbase + L::kV + sv * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColDP, sdesc_kmajor(sdO, kk, 16384u), sdesc_kmajor(sV, kk, 16384u), idS,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_DPFULL));
+        umma_commit(bar(B_VEMPTY + sv));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_QDO), 0, abort_flag, p.status, 0x305) && issue_s(0) && issue_dp(0);
+      for (int n = 0; ok && n < nt; ++n) {
+        if (n + 1 < nt && !issue_s(n + 1)) break;  // its buffer's dS(n-1) was read by dQ(n-1)
+        if (!mbar_wait(bar(B_DSFULL), n & 1, abort_flag, p.status, 0x306)) break;
+        tc_fence_after();
+        // dQ += dS(n) K(n): dS pairs of keys [0,64) at S columns [0,32), [64,128) at [64,96)
+        const int sk = n % kKStages;
+        const uint32_t sK = sbase + L::kK + sk * L::kTileBytes;
+        const uint32_t sS = tmem + kColS + (n & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColDQ, sS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sK, kk, 16384u), idQ, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_KEMPTY + sk));
+        if (n + 1 < nt) {
+          if (!issue_dp(n + 1)) break;
+        } else {
+          umma_commit(bar(B_DONE));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps 0-7
+    const int quarter = warp & 3;
+    const int hf = warp >> 2;           // column half of the key tile, and of dQ
+    const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
+    const int i = qt * 128 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    int st[4];
+    uint32_t len[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      st[n] = 0;
+      len[n] = 0;
+      if (n < p.NI) {
+        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + i];
+        st[n] = iv.x;
+        len[n] = static_cast<uint32_t>(iv.y - iv.x);
+      }
+    }
+    // per-row constants from the backward prologue: -LSE * log2(e) (-inf for a row that sees
+    // nothing) and -D
+    const float lse2 = p.lse2[static_cast<size_t>(row0) + i];
+    const float negd = p.delta[static_cast<size_t>(row0) + i];
+    const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 lse2x2 = make_float2(lse2, lse2), negd2 = make_float2(negd, negd);
+    bool ok = true;
+    int kt = next_tile(bmrow, p.NT, 0);
+    for (int n = 0; ok && n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
+      const int sb = n & 1;
+      const uint32_t sS = tmem + lane_off + kColS + sb * 128 + 64 * hf;
+      bool ready = mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x307);
+      __syncwarp();
+      if (!ready) { ok = false; break; }
+      tc_fence_after();
+      float pf[64];
+      {
+        uint32_t t0[32], t1[32];
+        tmem_ld32(sS, t0);
+        tmem_ld32(sS + 32, t1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          pf[c] = __uint_as_float(t0[c]);
+          pf[32 + c] = __uint_as_float(t1[c]);
+        }
+      }
+      if (!tile_is_full(bmrow, kt)) {
+        const int j0 = kt * 128 + 64 * hf;
+        switch (p.NI) {
+          case 1: mask_cols<1>(pf, j0, st, len); break;
+          case 2: mask_cols<2>(pf, j0, st, len); break;
+          case 3: mask_cols<3>(pf, j0, st, len); break;
+          default: mask_cols<4>(pf, j0, st, len); break;
+        }
+      }
+      // P = exp2(s * scale*log2e - LSE*log2e); masked scores are -inf and give 0
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 x = fma2(make_float2(pf[c], pf[c + 1]), scale2, lse2x2);
+        pf[c] = ex2_approx(x.x);
+        pf[c + 1] = ex2_approx(x.y);
+      }
+      ready = mbar_wait(bar(B_DPFULL), n & 1, abort_flag, p.status, 0x308);
+      __syncwarp();
+      if (!ready) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dpr[32];
+        tmem_ld32(tmem + lane_off + kColDP + 64 * hf + 32 * ch, dpr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 g = add2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])), negd2);
+          const float2 ds = mul2(make_float2(pf[32 * ch + c], pf[32 * ch + c + 1]), g);
+          pk[16 * ch + c / 2] = pack_bf16x2(ds.x, ds.y);
+        }
+      }
+      // dS over the S columns this warp has read: keys [64*hf, +64) -> columns [64*hf, +32)
+      tmem_st32(sS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+    }
+
+    // ---- epilogue: dQ = scale * accumulator -> bf16, this warp's half of the head dim ----
+    __nv_bfloat16* qrow = p.dq + (static_cast<size_t>(row0) + i) * D + hf * kHalf;
+    const bool done = ok && nt > 0 && mbar_wait(bar(B_DONE), 0, abort_flag, p.status, 0x309);
+    __syncwarp();
+    if (done) {
+      tc_fence_after();
+      const float sc = p.scale;
+#pragma unroll
+      for (int c = 0; c < kHalf; c += 32) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + kColDQ + hf * kHalf + c, a);
+        tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(qrow + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 x;
+          x.x = pack_bf16x2(__uint_as_float(a[8 * q + 0]) * sc, __uint_as_float(a[8 * q + 1]) * sc);
+          x.y = pack_bf16x2(__uint_as_float(a[8 * q + 2]) * sc, __uint_as_float(a[8 * q + 3]) * sc);
+          x.z = pack_bf16x2(__uint_as_float(a[8 * q + 4]) * sc, __uint_as_float(a[8 * q + 5]) * sc);
+          x.w = pack_bf16x2(__uint_as_float(a[8 * q + 6]) * sc, __uint_as_float(a[8 * q + 7]) * sc);
+          dst[q] = x;
+        }
+      }
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(qrow);
+      for (int q = 0; q < kHalf / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace dq
+
+int launch_attn_dq(const DqParams& p, int d, const void* q, const void* k, const void* v,
+                   const void* d_o, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
+      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
+    return -1;
+  const dim3 grid(p.B * p.NT * p.H);
+  if (d == 128) {
+    const uint32_t smem = dq::Smem<128>::kAlloc;
+    if (cudaFuncSetAttribute(dq::attn_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    dq::attn_dq_kernel<128><<<grid, dq::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  } else {
+    const uint32_t smem = dq::Smem<64>::kAlloc;
+    if (cudaFuncSetAttribute(dq::attn_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    dq::attn_dq_kernel<64><<<grid, dq::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace cm

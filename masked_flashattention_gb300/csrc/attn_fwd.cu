@@ -31,6 +31,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "mask.cuh"
 #include "ptx.cuh"
 #include "tma_host.h"
 
@@ -75,23 +76,6 @@ enum {
   B_PAIR = 20,    // +2*quarter+parity: row-max / row-sum exchange of a warp pair (2 arrivals)
   B_COUNT = 28
 };
-
-// Replace invisible scores by -inf: key j0 + c is visible to the row iff for some interval
-// (start, end): (u32)(j0 + c - start) < (u32)(end - start).
-template <int NI, int N>
-__device__ __forceinline__ void mask_cols(float (&s)[N], int j0, const int (&st)[4],
-                                          const uint32_t (&len)[4]) {
-  uint32_t base[NI];
-#pragma unroll
-  for (int n = 0; n < NI; ++n) base[n] = static_cast<uint32_t>(j0 - st[n]);
-#pragma unroll
-  for (int c = 0; c < N; ++c) {
-    bool vis = false;
-#pragma unroll
-    for (int n = 0; n < NI; ++n) vis |= (base[n] + static_cast<uint32_t>(c)) < len[n];
-    s[c] = vis ? s[c] : -INFINITY;
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -34,12 +34,25 @@ struct BwdParams {
   const float* lse;      // [B][H][S] natural log (forward output)
   float* delta;          // [B][H][S] -rowsum(dO * O), written by the prologue
   float* lse2;           // [B][H][S] -LSE * log2(e) (-inf for rows that see nothing), prologue
-  float* dq_acc;         // [B][H][S][d] fp32
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H, S, NT, W, NI;
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
+};
+
+// dQ pass of the backward: traverses query tiles with the forward descriptor.
+struct DqParams {
+  const int32_t* itab;   // forward Interval Table [B][NI][S][2]
+  const uint32_t* bm;    // forward bitmaps [B][NT][W]
+  const int32_t* sched;  // (b << 16 | q_tile), longest first
+  int32_t* status;
+  const float* delta;    // [B][H][S] -rowsum(dO * O)
+  const float* lse2;     // [B][H][S] -LSE * log2(e)
+  __nv_bfloat16* dq;
+  int B, H, S, NT, W, NI;
+  float scale;
+  float scale_log2;
 };
 
 // Runs the generated kernels when both gen_fwd and gen_bwd are given, else the generic kernel.
@@ -50,7 +63,10 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_fw
                       cudaStream_t stream);
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream);
+// Prologue (D, LSE * log2(e)) and the dK/dV kernel; then launch_attn_dq for dQ.
 int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
-                    const void* o, const void* d_o, void* dq, cudaStream_t stream);
+                    const void* o, const void* d_o, cudaStream_t stream);
+int launch_attn_dq(const DqParams& p, int d, const void* q, const void* k, const void* v,
+                   const void* d_o, cudaStream_t stream);
 
 }  // namespace cm

@@ -22,6 +22,7 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,      // an mbarrier wait exceeded its limit
   kDevBadMeta = 2,      // segment metadata not monotone / not ending at S
+  kDevSmemAlign = 3,    // dynamic shared memory not 1024-byte aligned (a kernel needing it exits)
 };
 
 __device__ __forceinline__ void set_status(int* status, int code, int where) {
@@ -127,10 +128,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 // wait until no committed bulk group of this thread still reads shared memory
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// wait until at most the most recent committed bulk group of this thread still reads shared memory
-__device__ __forceinline__ void bulk_wait_read_but1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // wait until every committed bulk group of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() {

@@ -40,20 +40,3 @@ inline bool make_bf16_tile_map(CUtensorMap* map, const void* base, uint64_t rows
 }
 
 }  // namespace cm
-
-namespace cm {
-
-// 2-D fp32 matrix [rows][cols], box of 32 columns (128 bytes) x 128 rows, 128-byte swizzle.
-inline bool make_f32_tile_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 4};
-  cuuint32_t box[2] = {32, 128};
-  cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace cm

@@ -54,7 +54,7 @@ def test_noalloc_rejects_problems_beyond_the_scratch_array():
     from masked_flashattention_gb300 import specs
 
     B.lib()
-    S, H, d = 32768, 4, 128  # needs > 32 MiB of scratch
+    S, H, d = 32768, 160, 64  # 5.2M rows: needs > 32 MiB of scratch
     need = B.cm_attn_bwd_workspace_size(1, H, S, d)
     assert need > B.NOALLOC_SCRATCH_BYTES
     f, b = B.cm_compile_spec(specs.FWD[2]), B.cm_compile_spec(specs.BWD[2])
