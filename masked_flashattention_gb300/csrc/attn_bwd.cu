@@ -29,9 +29,10 @@
 // RB (m odd) and Y the other one:
 //   S^T(m) -> X; the compute warps overwrite it in place with the bf16 P^T pairs (each warp
 //   writes only columns it has already read); dP^T(m) -> Y.
-//   Once the compute warps have handed over P^T and dS^T, the MMA issues S^T(m+1) -> Y (its
-//   dP^T was consumed), dV(m) (reads P^T from X), dK(m), and dP^T(m+1) -> X (after dV read it).
-// So the compute warps start on the next tile's P while the tensor pipe runs dV and dK.
+//   As soon as P^T is written the MMA issues dV(m) (reads P^T from X) while the compute warps
+//   form dS^T; once dS^T is in shared memory it issues S^T(m+1) -> Y (its dP^T was consumed),
+//   dP^T(m+1) -> X (dV read P^T before), and dK(m).  The compute warps wait for dK(m) only
+//   before overwriting the dS^T buffer, so the next tile's P and dS overlap dK and dV.
 // Shared memory (d = 128: 231,808 bytes, no room for alignment slack, so the kernel checks that
 // its dynamic shared memory starts on a 1024-byte boundary and exits with a status otherwise):
 // K, V, Q and dO (two slots each), dS^T (bf16, 128-byte swizzle), LSE*log2e and D (per slot),
@@ -72,7 +73,7 @@ struct Smem {
   static constexpr uint32_t kLse2 = kdSt + 32768u;     // [2 slots][128 floats]: -LSE * log2(e)
   static constexpr uint32_t kDelta = kLse2 + 1024u;    // [2 slots][128 floats]: -D
   static constexpr uint32_t kBar = kDelta + 1024u;
-  static constexpr uint32_t kRow = kBar + 128u;        // bitmap row: at most 64 words (NT <= 1024)
+  static constexpr uint32_t kRow = kBar + 256u;        // bitmap row: at most 64 words (NT <= 1024)
   static constexpr uint32_t kTotal = kRow + 256u;
   static constexpr uint32_t kAlloc = kTotal;
 };
@@ -86,9 +87,11 @@ enum {
   B_DOEMPTY = 7,   // +slot: the dV MMA (last reader of that dO slot) is done
   B_SFULL = 9,     // S^T of the current tile computed
   B_DPFULL = 10,   // dP^T of the current tile computed
-  B_PDS = 11,      // compute warps wrote P^T (TMEM) and dS^T (smem) (8 arrivals)
+  B_PDS = 11,      // compute warps wrote dS^T (smem) and read dP^T (8 arrivals)
   B_DONE = 12,     // every MMA of the CTA completed (dK, dV final)
-  B_COUNT = 13
+  B_PREADY = 13,   // compute warps wrote P^T (TMEM) (8 arrivals)
+  B_DKDONE = 14,   // the dK MMA (last reader of dS^T in shared memory) is done
+  B_COUNT = 15
 };
 
 // first query tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
@@ -223,6 +226,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_PREADY), kComputeWarps);
+    mbar_init(bar(B_DKDONE), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -313,12 +318,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t Y = (m & 1) ? kColRA : kColRB;
         const uint32_t sQ = sbase + L::kQ + (m & 1) * L::kTileBytes;
         const uint32_t sdO = sbase + L::kdO + (m & 1) * L::kTileBytes;
+        // dV += P^T dO as soon as P^T is in X, while the compute warps work on dS^T.
+        // P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
+        if (!mbar_wait(bar(B_PREADY), m & 1, abort_flag, p.status, 0x210)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_DOEMPTY + (m & 1)));
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
         if (m + 1 < nt) {
-          // S^T of the next tile first, into Y (its dP^T was consumed), so that the compute warps
-          // can start on it while the tensor pipe runs dV and dK
+          // the next tile's S^T into Y (its dP^T was consumed) and dP^T into X (dV above read
+          // P^T from it), so that its P and dS can start while the tensor pipe runs dK
           const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
+          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
           if (!mbar_wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x203))
             break;
           tc_fence_after();
@@ -327,22 +342,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_ss(tmem + Y, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQn, kk, 16384u), idSS,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_SFULL));
-        }
-        // dV += P^T dO; P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DOEMPTY + (m & 1)));
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
-                  (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY + (m & 1)));
-        if (m + 1 < nt) {
-          // dP^T of the next tile into X, after the dV MMA above has read P^T from it
-          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
           if (!mbar_wait(bar(B_DOFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x20c))
             break;
           tc_fence_after();
@@ -351,9 +350,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdOn, kk, 16384u), idSS,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_DPFULL));
-        } else {
-          umma_commit(bar(B_DONE));
         }
+        // dK += dS^T Q; its completion frees the Q slot and the dS^T buffer
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
+                  (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_QEMPTY + (m & 1)));
+        umma_commit(bar(m + 1 < nt ? B_DKDONE : B_DONE));
       }
     }
   } else {
@@ -414,9 +418,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_st16(tmem + lane_off + X + hf * 64 + ch * 16, pp);
       }
 
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PREADY));
+
       // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T into this half's box ----
+      // the previous tile's dK MMA has stopped reading the dS^T buffer
       ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e) &&
-              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d);
+              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d) &&
+              (m == 0 || mbar_wait(bar(B_DKDONE), (m - 1) & 1, abort_flag, p.status, 0x211));
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -435,7 +446,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           st_shared_v4(sbase + L::kdSt + off, dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
         }
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
