@@ -367,10 +367,11 @@ def run_gpu(args):
         import hashlib
         with open(tp) as f:
             rec = json.load(f).get(f"attn_bwd@{w.name}")
-        src = os.path.join(ROOT, "masked_flashattention_gb300", "csrc", "attn_bwd.cu")
-        with open(src, "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()
-        if rec and rec.get("source_sha1") == sha:  # counters only count for the kernel they measured
+        def sha1(name):
+            with open(os.path.join(ROOT, "masked_flashattention_gb300", "csrc", name), "rb") as f:
+                return hashlib.sha1(f.read()).hexdigest()
+        # counters only count for the kernel sources they were measured on
+        if rec and all(sha1(n) == h for n, h in rec.get("source_sha1", {}).items()):
             traffic = rec["bytes"]
 
     if rank == 0:
