@@ -50,8 +50,7 @@ enum {
   CM_ERR_UNSUPPORTED = -3,  /* valid request outside the supported shapes (d, S, tile, limits) */
   CM_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
   CM_ERR_TIMEOUT = -5,      /* device status: a bounded wait inside a kernel expired */
-  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation (or a kernel found its
-                               shared memory misaligned and did nothing) */
+  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation */
 };
 
 /* Opaque compiled MaskSpec (host memory, owned by the caller after cm_compile_spec). */

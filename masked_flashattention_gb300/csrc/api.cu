@@ -48,7 +48,7 @@ CM_API const char* cm_error_string(int code) {
     case CM_ERR_UNSUPPORTED: return "unsupported shape or limit";
     case CM_ERR_CUDA: return "CUDA runtime error";
     case CM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
-    case CM_ERR_DEVICE_CHECK: return "a device-side check failed (segment metadata, or shared-memory alignment)";
+    case CM_ERR_DEVICE_CHECK: return "segment metadata failed device-side validation";
     default: return "unknown error";
   }
 }

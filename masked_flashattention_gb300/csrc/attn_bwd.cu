@@ -7,7 +7,7 @@
 //
 //   S^T  = K Q^T            (tcgen05, TMEM)        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
 //   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
-//   dK  += dS^T Q           (TMEM accumulator)
+//   dK  += dS^T Q           (TMEM accumulator; dS^T is the A operand, read from TMEM)
 //   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
 //
 // dQ is computed by a second kernel that walks query tiles (attn_dq.cu); adding every key tile's
@@ -29,13 +29,13 @@
 // RB (m odd) and Y the other one:
 //   S^T(m) -> X; the compute warps overwrite it in place with the bf16 P^T pairs (each warp
 //   writes only columns it has already read); dP^T(m) -> Y.
-//   As soon as P^T is written the MMA issues dV(m) (reads P^T from X) while the compute warps
-//   form dS^T; once dS^T is in shared memory it issues S^T(m+1) -> Y (its dP^T was consumed),
-//   dP^T(m+1) -> X (dV read P^T before), and dK(m).  The compute warps wait for dK(m) only
-//   before overwriting the dS^T buffer, so the next tile's P and dS overlap dK and dV.
-// Shared memory (d = 128: 231,808 bytes, no room for alignment slack, so the kernel checks that
-// its dynamic shared memory starts on a 1024-byte boundary and exits with a status otherwise):
-// K, V, Q and dO (two slots each), dS^T (bf16, 128-byte swizzle), LSE*log2e and D (per slot),
+//   The compute warps then write the bf16 dS^T pairs into the other half of the columns they read
+//   from X (warp half h: P^T at 64h + [0,32), dS^T at 64h + [32,64)).
+//   As soon as P^T is written the MMA issues dV(m) (A = P^T from X) while the compute warps form
+//   dS^T; once dS^T is written it issues S^T(m+1) -> Y (its dP^T was consumed), dK(m) (A = dS^T
+//   from X) and dP^T(m+1) -> X (after dV and dK read it).  Both gradient MMAs take their A operand
+//   from TMEM, so shared memory carries only K, V, Q and dO, and the next tile's P overlaps dK.
+// Shared memory: K, V, Q and dO (two slots each, 128-byte swizzle), LSE*log2e and D (per slot),
 // barriers, and the CTA's row of the backward bitmap (the non-empty query tiles are found by
 // scanning it).
 #include <cuda_bf16.h>
@@ -69,13 +69,12 @@ struct Smem {
   static constexpr uint32_t kV = kTileBytes;
   static constexpr uint32_t kQ = 2 * kTileBytes;      // two slots
   static constexpr uint32_t kdO = 4 * kTileBytes;      // two slots
-  static constexpr uint32_t kdSt = 6 * kTileBytes;     // [2 boxes][128 keys][64 queries] bf16
-  static constexpr uint32_t kLse2 = kdSt + 32768u;     // [2 slots][128 floats]: -LSE * log2(e)
+  static constexpr uint32_t kLse2 = 6 * kTileBytes;    // [2 slots][128 floats]: -LSE * log2(e)
   static constexpr uint32_t kDelta = kLse2 + 1024u;    // [2 slots][128 floats]: -D
   static constexpr uint32_t kBar = kDelta + 1024u;
   static constexpr uint32_t kRow = kBar + 256u;        // bitmap row: at most 64 words (NT <= 1024)
   static constexpr uint32_t kTotal = kRow + 256u;
-  static constexpr uint32_t kAlloc = kTotal;
+  static constexpr uint32_t kAlloc = kTotal + 1024u;  // + slack to align the base to 1024 bytes
 };
 static_assert(Smem<128>::kAlloc <= 232448, "backward shared memory exceeds 227 KB");
 
@@ -87,11 +86,10 @@ enum {
   B_DOEMPTY = 7,   // +slot: the dV MMA (last reader of that dO slot) is done
   B_SFULL = 9,     // S^T of the current tile computed
   B_DPFULL = 10,   // dP^T of the current tile computed
-  B_PDS = 11,      // compute warps wrote dS^T (smem) and read dP^T (8 arrivals)
+  B_PDS = 11,      // compute warps wrote dS^T (TMEM) and read dP^T (8 arrivals)
   B_DONE = 12,     // every MMA of the CTA completed (dK, dV final)
   B_PREADY = 13,   // compute warps wrote P^T (TMEM) (8 arrivals)
-  B_DKDONE = 14,   // the dK MMA (last reader of dS^T in shared memory) is done
-  B_COUNT = 15
+  B_COUNT = 14
 };
 
 // first query tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
@@ -192,12 +190,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ BwdParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;           // head-dim columns per compute warp
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  if ((sbase & 1023u) != 0) {  // the 128-byte swizzled tiles need 1024-byte alignment
-    if (threadIdx.x == 0) set_status(p.status, kDevSmemAlign, 0x2ff);
-    return;
-  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
@@ -227,7 +223,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DONE), 1);
     mbar_init(bar(B_PREADY), kComputeWarps);
-    mbar_init(bar(B_DKDONE), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -292,7 +287,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
-      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdSt = sbase + L::kdSt;
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
       // tile 0: S^T -> RA, dP^T -> RB
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202) &&
                 mbar_wait(bar(B_QFULL), 0, abort_flag, p.status, 0x203);
@@ -330,10 +325,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
         if (m + 1 < nt) {
-          // the next tile's S^T into Y (its dP^T was consumed) and dP^T into X (dV above read
-          // P^T from it), so that its P and dS can start while the tensor pipe runs dK
+          // the next tile's S^T into Y (its dP^T was consumed), so that its P can start while
+          // the tensor pipe runs dK
           const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
-          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
           if (!mbar_wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x203))
             break;
           tc_fence_after();
@@ -342,6 +336,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_ss(tmem + Y, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQn, kk, 16384u), idSS,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_SFULL));
+        }
+        // dK += dS^T Q with dS^T read from X: queries [64h + 32c, +32) at columns 64h + 32 + 16c
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColDK, tmem + X + 64 * (kk >> 2) + 32 + 8 * (kk & 3),
+                  sdesc_mnmajor(sQ, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_QEMPTY + (m & 1)));
+        if (m + 1 < nt) {
+          // dP^T of the next tile into X, after dV and dK above have read P^T and dS^T from it
+          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
           if (!mbar_wait(bar(B_DOFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x20c))
             break;
           tc_fence_after();
@@ -350,14 +354,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdOn, kk, 16384u), idSS,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(B_DPFULL));
+        } else {
+          umma_commit(bar(B_DONE));
         }
-        // dK += dS^T Q; its completion frees the Q slot and the dS^T buffer
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kColDK, sdesc_kmajor(sdSt, kk, 16384u), sdesc_mnmajor(sQ, kk, 16384u), idKM,
-                  (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY + (m & 1)));
-        umma_commit(bar(m + 1 < nt ? B_DKDONE : B_DONE));
       }
     }
   } else {
@@ -423,11 +422,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PREADY));
 
-      // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T into this half's box ----
-      // the previous tile's dK MMA has stopped reading the dS^T buffer
+      // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T as bf16 pairs into X ----
       ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e) &&
-              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d) &&
-              (m == 0 || mbar_wait(bar(B_DKDONE), (m - 1) & 1, abort_flag, p.status, 0x211));
+              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -438,15 +435,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_ld32(tmem + lane_off + Y + q0, dpr);
         tmem_wait_ld();
         ds_chunk(pf[ch], dpr, sbase + L::kDelta + (m & 1) * 512u + q0 * 4u, dd);
-        // dS^T row r, queries q0..q0+31 = four 16-byte chunks of box hf
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = ch * 4 + q4;
-          const uint32_t off = hf * 16384u + r * 128u + ((chunk ^ (r & 7)) << 4);
-          st_shared_v4(sbase + L::kdSt + off, dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
-        }
+        // dS^T pairs into X columns this warp has read and P^T does not use: 64 hf + 32 + 16 ch
+        tmem_st16(tmem + lane_off + X + hf * 64 + 32 + ch * 16, dd);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PDS));

@@ -22,7 +22,6 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,      // an mbarrier wait exceeded its limit
   kDevBadMeta = 2,      // segment metadata not monotone / not ending at S
-  kDevSmemAlign = 3,    // dynamic shared memory not 1024-byte aligned (a kernel needing it exits)
 };
 
 __device__ __forceinline__ void set_status(int* status, int code, int where) {
