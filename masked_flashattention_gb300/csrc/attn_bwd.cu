@@ -43,6 +43,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "mask.cuh"
 #include "ptx.cuh"
 #include "tma_host.h"
 
@@ -92,21 +93,6 @@ enum {
   B_COUNT = 14
 };
 
-// first query tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
-__device__ __forceinline__ int next_tile(const uint32_t* row, int NT, int c) {
-  while (c < NT) {
-    const int w = c >> 4;
-    uint32_t x = row[w];
-    x = (x | (x >> 1)) & 0x55555555u;
-    x &= 0xFFFFFFFFu << (2 * (c & 15));
-    if (x != 0) return (w << 4) + ((__ffs(x) - 1) >> 1);
-    c = (w + 1) << 4;
-  }
-  return NT;
-}
-__device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
-  return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
-}
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {

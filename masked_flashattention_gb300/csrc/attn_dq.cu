@@ -69,21 +69,6 @@ enum {
   B_COUNT = 16
 };
 
-// first key tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
-__device__ __forceinline__ int next_tile(const uint32_t* row, int NT, int c) {
-  while (c < NT) {
-    const int w = c >> 4;
-    uint32_t x = row[w];
-    x = (x | (x >> 1)) & 0x55555555u;
-    x &= 0xFFFFFFFFu << (2 * (c & 15));
-    if (x != 0) return (w << 4) + ((__ffs(x) - 1) >> 1);
-    c = (w + 1) << 4;
-  }
-  return NT;
-}
-__device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
-  return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)

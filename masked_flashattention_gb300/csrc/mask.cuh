@@ -1,10 +1,27 @@
-// Partial-tile visibility check shared by the kernels that traverse query rows (the forward and
-// the dQ kernel): the unsigned interval test of CompileMask section 4.4.
+// Helpers shared by the attention kernels: walking the non-empty tiles of a Tile-State Bitmap row
+// (CompileMask section 3.3.1) and the partial-tile visibility check of the kernels that traverse
+// query rows (the unsigned interval test of section 4.4).
 #pragma once
 #include <cmath>
 #include <cstdint>
 
 namespace cm {
+
+// first tile c' >= c whose 2-bit state in the bitmap row is not empty, or NT
+__device__ __forceinline__ int next_tile(const uint32_t* row, int NT, int c) {
+  while (c < NT) {
+    const int w = c >> 4;
+    uint32_t x = row[w];
+    x = (x | (x >> 1)) & 0x55555555u;
+    x &= 0xFFFFFFFFu << (2 * (c & 15));
+    if (x != 0) return (w << 4) + ((__ffs(x) - 1) >> 1);
+    c = (w + 1) << 4;
+  }
+  return NT;
+}
+__device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
+  return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
+}
 
 // Replace invisible scores by -inf: key j0 + c is visible to the row iff for some interval
 // (start, end): (u32)(j0 + c - start) < (u32)(end - start).
