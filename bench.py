@@ -321,6 +321,32 @@ def run_gpu(args):
     t_max, units = aggregate(elapsed, flops * args.steps, world)
     value = units / t_max / 1e12
 
+    # ---- optional: the partial-tile check forms of the paper's section 4.4 ablation ----
+    ablation = None
+    if args.ablation:
+        ablation = {}
+        names = {Bd.CM_CHECK_UNSIGNED: "unsigned_visible", Bd.CM_CHECK_TWO_COMPARE: "two_compare_visible",
+                 Bd.CM_CHECK_MASKED: "masked_intervals"}
+        for mode in (Bd.CM_CHECK_UNSIGNED, Bd.CM_CHECK_TWO_COMPARE, Bd.CM_CHECK_MASKED):
+            Bd.cm_set_interval_check(mode)
+            for _ in range(max(3, args.warmup)):
+                step()
+            aevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+            torch.cuda.synchronize(dev)
+            for s_ in range(args.steps):
+                step(aevs[s_])
+            torch.cuda.synchronize(dev)
+            f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in aevs)
+            b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in aevs)
+            ablation[names[mode]] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_bwd_ms": f_ms + b_ms}
+        Bd.cm_set_interval_check(Bd.CM_CHECK_UNSIGNED)
+        st = Bd.cm_get_status(desc)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {Bd.cm_error_string(st)}")
+        base = ablation["unsigned_visible"]["fwd_bwd_ms"]
+        for v_ in ablation.values():
+            v_["vs_unsigned"] = v_["fwd_bwd_ms"] / base
+
     # ---- end to end through the public API with pinned host buffers ----
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
     hseg, hnseg = seg.cpu().pin_memory(), nseg.cpu().pin_memory()
@@ -400,6 +426,8 @@ def run_gpu(args):
             "gpu_launches": 7 * args.steps,
             "clocks": clk,
         }
+        if ablation is not None:
+            line["ablation"] = ablation
         if world == 1 and not args.no_cpu_baseline:
             dt, pr, cores, sdesc = oracle_sample(args.config, args.ref_rows or 8192)
             line["cpu_baseline"] = {"value": FLOPS_PER_PAIR_PER_D * d * pr / dt / 1e12,
@@ -423,6 +451,8 @@ def main():
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", action="store_true",
+                    help="also time the three partial-tile check forms (section 4.4); use with --config 4")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -153,6 +153,20 @@ CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_
 
 /* ---- descriptor-guided attention (section 3.3.2) -------------------------------------------- */
 
+/* Form of the attention kernels' partial-tile check, for the whole process (the ablation of
+ * section 4.4; full and empty tiles are unaffected):
+ * CM_CHECK_UNSIGNED (default): key x is visible iff (uint32)(x - s) < (uint32)(e - s) for one of
+ *   the row's visible intervals [s, e): one subtraction and one comparison per interval;
+ * CM_CHECK_TWO_COMPARE: visible iff s <= x && x < e for one of them;
+ * CM_CHECK_MASKED: the kernels turn the row's visible intervals into the masked intervals of
+ *   their complement in [0, S) (the FlashMask form) and test x against those.
+ * All three give the same results.  Returns CM_ERR_INVALID_ARG for any other mode.  Not
+ * synchronised with launches in flight on other host threads. */
+#define CM_CHECK_UNSIGNED 0
+#define CM_CHECK_TWO_COMPARE 1
+#define CM_CHECK_MASKED 2
+CM_API int cm_set_interval_check(int mode);
+
 /* Forward: o = softmax(scale * q k^T masked by desc) v; lse = natural-log row sums.
  * q, k, v, o: device bf16 [B][H][S][d]; lse: device fp32 [B][H][S].  The mask is shared by
  * all heads of a sample.  A row with no visible key gets o = 0 and lse = -inf. */

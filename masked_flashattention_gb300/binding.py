@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         L.cm_spec_kernel_source.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
         L.cm_spec_kernel_status.argtypes = [vp, i32, ctypes.c_char_p, sz]
         L.cm_set_preprocess_mode.argtypes = [i32]
+        L.cm_set_interval_check.argtypes = [i32]
         L.cm_descriptor_sizes.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(sz)]
         L.cm_build_descriptor.argtypes = [vp, vp, ctypes.POINTER(cm_meta), i32, i32,
                                           ctypes.POINTER(cm_descriptor), vp]
@@ -164,6 +165,17 @@ CM_PREPROCESS_GENERIC = 1
 def cm_set_preprocess_mode(mode: int) -> None:
     """Process-wide choice of descriptor kernels: generated per spec (default) or generic."""
     _check(lib().cm_set_preprocess_mode(mode), "cm_set_preprocess_mode")
+
+
+CM_CHECK_UNSIGNED = 0
+CM_CHECK_TWO_COMPARE = 1
+CM_CHECK_MASKED = 2
+
+
+def cm_set_interval_check(mode: int) -> None:
+    """Process-wide form of the attention kernels' partial-tile check (the paper's section 4.4
+    ablation): unsigned visible-interval test (default), two comparisons, or masked intervals."""
+    _check(lib().cm_set_interval_check(mode), "cm_set_interval_check")
 
 
 def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE) -> list[int]:

@@ -15,6 +15,8 @@ constexpr int kMaxS = 131072;
 
 // which descriptor kernels cm_build_descriptor runs (cm_set_preprocess_mode)
 std::atomic<int> g_preprocess_mode{CM_PREPROCESS_GENERATED};
+// form of the attention kernels' partial-tile check (cm_set_interval_check)
+std::atomic<int> g_interval_check{CM_CHECK_UNSIGNED};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -70,6 +72,13 @@ CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, in
   sizes[4] = static_cast<size_t>(B) * NT * 4;
   sizes[5] = static_cast<size_t>(B) * NT * 4;
   sizes[6] = 4;
+  return CM_OK;
+}
+
+CM_API int cm_set_interval_check(int mode) {
+  if (mode != CM_CHECK_UNSIGNED && mode != CM_CHECK_TWO_COMPARE && mode != CM_CHECK_MASKED)
+    return CM_ERR_INVALID_ARG;
+  g_interval_check.store(mode);
   return CM_OK;
 }
 
@@ -132,6 +141,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.NT = S / kTile;
   p.W = (p.NT + 15) / 16;
   p.NI = desc->ni_f;
+  p.check = g_interval_check.load();
   p.scale_log2 = scale * 1.4426950408889634f;
   return cm::launch_attn_fwd(p, d, q, k, v, static_cast<cudaStream_t>(stream)) == 0
              ? CM_OK
@@ -184,6 +194,7 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.NT = S / kTile;
   p.W = (p.NT + 15) / 16;
   p.NI = desc->ni_b;
+  p.check = g_interval_check.load();
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -202,6 +213,7 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   g.NT = p.NT;
   g.W = p.W;
   g.NI = desc->ni_f;
+  g.check = p.check;
   g.scale = scale;
   g.scale_log2 = p.scale_log2;
   return cm::launch_attn_dq(g, d, q, k, v, d_o, st) == 0 ? CM_OK : CM_ERR_CUDA;

@@ -110,21 +110,6 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   return v;
 }
 
-template <int NI>
-__device__ __forceinline__ uint32_t visible_bits(int i0, const int (&st)[4], const uint32_t (&len)[4]) {
-  // bit c set iff query i0 + c (c < 32) lies in one of the column's intervals
-  uint32_t bits = 0;
-#pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    bool vis = false;
-#pragma unroll
-    for (int n = 0; n < NI; ++n)
-      vis |= (static_cast<uint32_t>(i0 - st[n]) + static_cast<uint32_t>(c)) < len[n];
-    bits |= vis ? (1u << c) : 0u;
-  }
-  return bits;
-}
-
 // P^T of 32 queries of this key row: p = exp2(s * scale*log2e + (-LSE*log2e)) in fp32 (kept for
 // dS) and as bf16 pairs (the A operand of dV).  Shared memory holds -LSE*log2e per query, so the
 // exponent is one paired FMA.  For a partial tile, queries whose bit in `vis` is clear get p = 0.
@@ -352,18 +337,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK)
     const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    int st[4];
-    uint32_t len[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      st[n] = 0;
-      len[n] = 0;
-      if (n < p.NI) {
-        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + j];
-        st[n] = iv.x;
-        len[n] = static_cast<uint32_t>(iv.y - iv.x);
-      }
-    }
+    RowIntervals ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, j, p.check, ri);
     const float sl2 = p.scale_log2;
     bool ok = true;
     int qt = next_tile(bmrow, p.NT, 0);
@@ -390,13 +365,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           p_chunk<true>(sr, lse2_base + q0 * 4u, sl2, 0u, pf[ch], pp);
         } else {
           const int i0 = qt * 128 + q0;
-          uint32_t vis;
-          switch (p.NI) {
-            case 1: vis = visible_bits<1>(i0, st, len); break;
-            case 2: vis = visible_bits<2>(i0, st, len); break;
-            case 3: vis = visible_bits<3>(i0, st, len); break;
-            default: vis = visible_bits<4>(i0, st, len); break;
-          }
+          const uint32_t vis = visible_bits_any(i0, ri, p.NI, p.check);
           p_chunk<false>(sr, lse2_base + q0 * 4u, sl2, vis, pf[ch], pp);
         }
         // P^T pairs into X columns this warp has already read: hf * 64 + ch * 16

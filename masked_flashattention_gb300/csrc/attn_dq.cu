@@ -227,18 +227,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    int st[4];
-    uint32_t len[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      st[n] = 0;
-      len[n] = 0;
-      if (n < p.NI) {
-        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + i];
-        st[n] = iv.x;
-        len[n] = static_cast<uint32_t>(iv.y - iv.x);
-      }
-    }
+    RowIntervals ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, i, p.check, ri);
     // per-row constants from the backward prologue: -LSE * log2(e) (-inf for a row that sees
     // nothing) and -D
     const float lse2 = p.lse2[static_cast<size_t>(row0) + i];
@@ -268,12 +258,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
       if (!tile_is_full(bmrow, kt)) {
         const int j0 = kt * 128 + 64 * hf;
-        switch (p.NI) {
-          case 1: mask_cols<1>(pf, j0, st, len); break;
-          case 2: mask_cols<2>(pf, j0, st, len); break;
-          case 3: mask_cols<3>(pf, j0, st, len); break;
-          default: mask_cols<4>(pf, j0, st, len); break;
-        }
+        mask_cols_any(pf, j0, ri, p.NI, p.check);
       }
       // P = exp2(s * scale*log2e - LSE*log2e); masked scores are -inf and give 0
 #pragma unroll

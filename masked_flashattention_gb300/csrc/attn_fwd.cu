@@ -237,18 +237,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t my_o = tmem + lane_off + kColO + 128 * hf;
-    int st[4];
-    uint32_t len[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      st[n] = 0;
-      len[n] = 0;
-      if (n < p.NI) {
-        const int2 iv = reinterpret_cast<const int2*>(p.itab)[(static_cast<size_t>(b) * p.NI + n) * p.S + i];
-        st[n] = iv.x;
-        len[n] = static_cast<uint32_t>(iv.y - iv.x);
-      }
-    }
+    RowIntervals ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, i, p.check, ri);
     bool ok = nt > 0;
     float m_run = -INFINITY;  // this half's running max (log2 domain)
     float l_run = 0.f;        // this half's running row sum
@@ -275,12 +265,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (!tile_is_full(bmrow, kt)) {
         const int j0 = kt * 128 + 64 * hf;
-        switch (p.NI) {
-          case 1: mask_cols<1>(s, j0, st, len); break;
-          case 2: mask_cols<2>(s, j0, st, len); break;
-          case 3: mask_cols<3>(s, j0, st, len); break;
-          default: mask_cols<4>(s, j0, st, len); break;
-        }
+        mask_cols_any(s, j0, ri, p.NI, p.check);
       }
       float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[32], s[33]);
 #pragma unroll

@@ -23,6 +23,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int B, H, S, NT, W, NI;
+  int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale_log2;      // softmax scale * log2(e)
 };
 
@@ -37,6 +38,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H, S, NT, W, NI;
+  int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
 };
@@ -51,6 +53,7 @@ struct DqParams {
   const float* lse2;     // [B][H][S] -LSE * log2(e)
   __nv_bfloat16* dq;
   int B, H, S, NT, W, NI;
+  int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale;
   float scale_log2;
 };

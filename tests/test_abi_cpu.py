@@ -181,3 +181,11 @@ def test_preprocess_mode_validation(B):
     B.cm_set_preprocess_mode(B.CM_PREPROCESS_GENERIC)
     B.cm_set_preprocess_mode(B.CM_PREPROCESS_GENERATED)
     assert L.cm_spec_kernel_status(None, 0, None, 0) == B.CM_ERR_INVALID_ARG
+
+
+def test_interval_check_mode_validation(B):
+    L = B.lib()
+    assert L.cm_set_interval_check(3) == B.CM_ERR_INVALID_ARG
+    assert L.cm_set_interval_check(-1) == B.CM_ERR_INVALID_ARG
+    for mode in (B.CM_CHECK_TWO_COMPARE, B.CM_CHECK_MASKED, B.CM_CHECK_UNSIGNED):
+        B.cm_set_interval_check(mode)

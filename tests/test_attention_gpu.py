@@ -135,3 +135,41 @@ def test_full_size_sampled_heads(wid):
     out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO)
     heads = range(w.H) if wid == 1 else sorted({0, w.H - 1})
     check_heads(wid, seg, nseg, Q, K, V, dO, out, heads)
+
+
+CHECKS = {"two_compare": 1, "masked": 2}
+
+
+@pytest.mark.parametrize("check", sorted(CHECKS))
+@pytest.mark.parametrize("wid", [1, 3, 4, 5])
+def test_interval_check_forms_small(wid, check):
+    """The two-compare and masked-interval forms of the partial-tile check (the paper's section
+    4.4 ablation) give the same attention as the oracle, on masks with 1 to 3 intervals per row."""
+    from masked_flashattention_gb300 import specs
+    B = _lib()
+    S = 1024
+    w = W.scaled(W.WORKLOADS[wid], S, B=2, H=2, d=128)
+    seg, nseg = W.segments(wid, w.B, S, seed=31 + wid)
+    Q, K, V, dO = W.full_tensors(w, seed=13 + wid)
+    B.cm_set_interval_check(CHECKS[check])
+    try:
+        out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO)
+    finally:
+        B.cm_set_interval_check(B.CM_CHECK_UNSIGNED)
+    check_heads(wid, seg, nseg, Q, K, V, dO, out, range(w.H))
+
+
+@pytest.mark.parametrize("check", sorted(CHECKS))
+def test_interval_check_forms_full_size_hstu(check):
+    """The ablation forms at the HSTU workload's full size (heads 0 and H-1 against the oracle)."""
+    from masked_flashattention_gb300 import specs
+    B = _lib()
+    w = W.WORKLOADS[4]
+    seg, nseg = W.segments(4, w.B, w.S)
+    Q, K, V, dO = W.full_tensors(w)
+    B.cm_set_interval_check(CHECKS[check])
+    try:
+        out = run_gpu(B, specs.FWD[4], specs.BWD[4], seg, nseg, Q, K, V, dO)
+    finally:
+        B.cm_set_interval_check(B.CM_CHECK_UNSIGNED)
+    check_heads(4, seg, nseg, Q, K, V, dO, out, sorted({0, w.H - 1}))
