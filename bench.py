@@ -444,7 +444,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=3, help="workload 1..5 (default: 3, RM 32K)")
+    ap.add_argument("--config", type=int, default=3, help="workload 1..6 (default: 3, RM 32K)")
     ap.add_argument("--impl", default="cm", choices=["cm", "reference"])
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="query rows of the oracle sample (default: sized to the run length)")

@@ -94,7 +94,8 @@ typedef struct cm_descriptor {
  *     region <guard> : <rule>
  * <guard> is `all` or a boolean expression of the row index i; <rule> is a boolean expression
  * over i and the other index j (&&, ||, !, comparisons < <= > >= == !=).  Integer terms: i, j,
- * S, nseg, integer constants, + - and multiplication by a constant, min(a, b), max(a, b),
+ * S, nseg, integer constants, + - and multiplication by a constant, % by a positive constant
+ * (non-negative remainder), min(a, b), max(a, b),
  * seg_idx(e), seg_start(e), seg_end(e), seg_start_at(k), seg_end_at(k).  Lines starting with '#'
  * are comments.  Regions are tried in order; the first whose guard holds applies to the row.
  * On success *out receives a new cm_spec.  On CM_ERR_PARSE a message is written to err (if

@@ -46,8 +46,8 @@ struct CompileError : std::runtime_error {
 // ---------------------------------------------------------------------------------------------
 // lexer
 // ---------------------------------------------------------------------------------------------
-enum class T { Ident, Int, LParen, RParen, Comma, Plus, Minus, Star, Lt, Le, Gt, Ge, Eq, Ne, And,
-               Or, Not, Colon, End };
+enum class T { Ident, Int, LParen, RParen, Comma, Plus, Minus, Star, Percent, Lt, Le, Gt, Ge, Eq,
+               Ne, And, Or, Not, Colon, End };
 
 struct Tok {
   T t;
@@ -98,6 +98,7 @@ std::vector<Tok> lex(const std::string& line, int lineno) {
           case '+': k.t = T::Plus; break;
           case '-': k.t = T::Minus; break;
           case '*': k.t = T::Star; break;
+          case '%': k.t = T::Percent; break;
           case '<': k.t = T::Lt; break;
           case '>': k.t = T::Gt; break;
           case '!': k.t = T::Not; break;
@@ -119,7 +120,8 @@ std::vector<Tok> lex(const std::string& line, int lineno) {
 // ---------------------------------------------------------------------------------------------
 // AST
 // ---------------------------------------------------------------------------------------------
-enum class EK { Const, I, J, S, Nseg, Add, Sub, Neg, MulC, Min, Max, SegIdx, SegStartAt, SegEndAt };
+enum class EK { Const, I, J, S, Nseg, Add, Sub, Neg, MulC, ModC, Min, Max, SegIdx, SegStartAt,
+                SegEndAt };
 struct Expr;
 using EP = std::shared_ptr<Expr>;
 struct Expr {
@@ -235,12 +237,20 @@ struct Parser {
   }
   EP term() {
     EP e = primary();
-    while (peek().t == T::Star) {
+    while (peek().t == T::Star || peek().t == T::Percent) {
+      const bool mod = peek().t == T::Percent;
       ++p;
       EP r = primary();
-      if (r->k == EK::Const) e = mk(EK::MulC, e, nullptr, r->v);
-      else if (e->k == EK::Const) e = mk(EK::MulC, r, nullptr, e->v);
-      else fail("multiplication needs a constant factor");
+      if (mod) {
+        if (r->k != EK::Const || r->v < 1) fail("'%' needs a positive constant divisor");
+        e = mk(EK::ModC, e, nullptr, r->v);
+      } else if (r->k == EK::Const) {
+        e = mk(EK::MulC, e, nullptr, r->v);
+      } else if (e->k == EK::Const) {
+        e = mk(EK::MulC, r, nullptr, e->v);
+      } else {
+        fail("multiplication needs a constant factor");
+      }
     }
     return e;
   }
@@ -310,8 +320,9 @@ struct Parser {
 // ---------------------------------------------------------------------------------------------
 struct Lin;
 struct Atom {
-  EK kind;                 // I, J, S, Nseg, Min, Max, SegIdx, SegStartAt, SegEndAt
+  EK kind;                 // I, J, S, Nseg, Min, Max, ModC, SegIdx, SegStartAt, SegEndAt
   std::vector<Lin> args;
+  long long c = 0;         // the divisor of ModC
   std::string key;
 };
 using AP = std::shared_ptr<Atom>;
@@ -378,11 +389,13 @@ Lin lscale(const Lin& x, long long k) {
 }
 bool lequal(const Lin& a, const Lin& b) { return a.str() == b.str(); }
 
-AP make_atom(EK kind, std::vector<Lin> args) {
+AP make_atom(EK kind, std::vector<Lin> args, long long c = 0) {
   auto a = std::make_shared<Atom>();
   a->kind = kind;
   a->args = std::move(args);
+  a->c = c;
   switch (kind) {
+    case EK::ModC: a->key = "mod(" + a->args[0].str() + ", " + std::to_string(c) + ")"; break;
     case EK::I: a->key = "i"; break;
     case EK::J: a->key = "j"; break;
     case EK::S: a->key = "S"; break;
@@ -431,6 +444,11 @@ Lin lin_of(const EP& e, bool allow_j) {
     }
     case EK::SegIdx: case EK::SegStartAt: case EK::SegEndAt:
       return latom(make_atom(e->k, {lin_of(e->a, false)}));
+    case EK::ModC: {  // non-negative remainder by a positive constant
+      Lin x = lin_of(e->a, false);
+      if (x.is_const()) return lconst(((x.c % e->v) + e->v) % e->v);
+      return latom(make_atom(EK::ModC, {x}, e->v));
+    }
   }
   throw CompileError("internal: bad expression");
 }
@@ -644,6 +662,7 @@ struct Emitter {
       }
       case EK::SegStartAt: lin(a.args[0]); op(OP_SEG_START_AT); break;
       case EK::SegEndAt: lin(a.args[0]); op(OP_SEG_END_AT); break;
+      case EK::ModC: lin(a.args[0]); op(OP_MODC, a.c); break;
       default: throw CompileError("internal: j in an endpoint");
     }
   }
@@ -683,7 +702,7 @@ int max_depth(const std::vector<int32_t>& code, int start) {
       case OP_I: case OP_S: case OP_NSEG: case OP_SEG_IDX_I: ++d; break;
       case OP_ADD: case OP_SUB: case OP_MIN: case OP_MAX: case OP_AND: case OP_OR: --d; break;
       case OP_CMP: --d; ++p; break;
-      case OP_MULC: ++p; break;
+      case OP_MULC: case OP_MODC: ++p; break;
       default: break;  // unary ops keep the depth
     }
     m = std::max(m, d);
@@ -695,6 +714,7 @@ int max_depth(const std::vector<int32_t>& code, int start) {
 // Names in scope of the generated code: i (row), ki (= seg_idx(i)), seg (segment starts in shared
 // memory), nseg, S.  Sums and products wrap like the stack programs' arithmetic.
 std::string c_lin(const Lin& l);
+std::string c_const(long long v);
 std::string c_atom(const Atom& a) {
   switch (a.kind) {
     case EK::I: return "i";
@@ -710,6 +730,7 @@ std::string c_atom(const Atom& a) {
     }
     case EK::SegStartAt: return "cmcore::seg_start_at(seg, nseg, " + c_lin(a.args[0]) + ")";
     case EK::SegEndAt: return "cmcore::seg_end_at(seg, nseg, " + c_lin(a.args[0]) + ")";
+    case EK::ModC: return "cmcore::imod(" + c_lin(a.args[0]) + ", " + c_const(a.c) + ")";
     default: throw CompileError("internal: j in an endpoint");
   }
 }

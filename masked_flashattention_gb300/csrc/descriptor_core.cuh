@@ -55,6 +55,11 @@ __device__ __forceinline__ int wadd(int a, int b) {
 __device__ __forceinline__ int wmul(int a, int c) {
   return static_cast<int>(static_cast<unsigned>(a) * static_cast<unsigned>(c));
 }
+// non-negative remainder by a positive constant
+__device__ __forceinline__ int imod(int a, int c) {
+  const int r = a % c;
+  return r < 0 ? r + c : r;
+}
 // segment holding position e: the largest k in [0, nseg - 1] with seg[k] <= e
 __device__ __forceinline__ int seg_index(const int* seg_s, int nseg, int e) {
   int lo = 0, hi = nseg - 1;

@@ -44,6 +44,7 @@ __device__ int eval_prog(const int32_t* code, int pc, int row, int row_seg, cons
       case OP_S: PUSH(S); break;
       case OP_NSEG: PUSH(nseg); break;
       case OP_SEG_IDX_I: PUSH(row_seg); break;
+      case OP_MODC: TOP = cmcore::imod(TOP, code[pc]); ++pc; break;
       case OP_MULC: TOP = static_cast<int>(static_cast<unsigned>(TOP) * static_cast<unsigned>(code[pc])); ++pc; break;
       case OP_NEG: TOP = static_cast<int>(0u - static_cast<unsigned>(TOP)); break;
       case OP_NOT: TOP = (TOP == 0); break;

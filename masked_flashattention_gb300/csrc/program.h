@@ -36,6 +36,7 @@ enum Op : int32_t {
   OP_NOT = 16,
   OP_NEG = 17,
   OP_SEG_IDX_I = 18,  // seg_idx(i) of the row, computed once per row by the evaluator
+  OP_MODC = 19,       // imm > 0: non-negative remainder
 };
 
 enum CmpOp : int32_t { CMP_LT = 0, CMP_LE = 1, CMP_GT = 2, CMP_GE = 3, CMP_EQ = 4, CMP_NE = 5 };

@@ -7,7 +7,8 @@ from its own MaskSpec so that its intervals follow the backward traversal (secti
 
 Segment conventions (metadata, see ``workloads``):
   1  documents; 2  one segment; 3  segment 0 = prompt, then responses;
-  4  segment 0 = history, segment 1 = candidates; 5  segment 0 = system prefix, then documents.
+  4  segment 0 = history, segment 1 = candidates; 5  segment 0 = system prefix, then documents;
+  6  users packed back to back, user u = history segment 2u and candidate segment 2u + 1.
 """
 
 FWD = {
@@ -36,6 +37,12 @@ region seg_idx(i) >= 1 : j < seg_end_at(0) || j == i
 region seg_idx(i) == 0 : j <= i
 region seg_idx(i) >= 1 : j < seg_end_at(0) || (seg_idx(i) >= 2 && j >= seg_start_at(seg_idx(i) - 1) && j < min(seg_start_at(seg_idx(i) - 1) + 64, seg_end_at(seg_idx(i) - 1))) || (j >= seg_start(i) && j <= i)
 """,
+    6: """
+# variable-length packed HSTU: per user, history rows are causal within the history; a candidate
+# row sees its user's history (the previous segment) and itself
+region seg_idx(i) % 2 == 0 : j >= seg_start(i) && j <= i
+region seg_idx(i) % 2 == 1 : (j >= seg_start_at(seg_idx(i) - 1) && j < seg_start(i)) || j == i
+""",
 }
 
 BWD = {
@@ -62,5 +69,11 @@ region seg_idx(i) >= 1 : j == i
 # of its document and, within the document's first 64 tokens, by every row of the next document
 region seg_idx(i) == 0 : j >= i
 region seg_idx(i) >= 1 : (j >= i && j < seg_end(i)) || (i < seg_start(i) + 64 && j >= seg_start_at(seg_idx(i) + 1) && j < seg_end_at(seg_idx(i) + 1))
+""",
+    6: """
+# a history key is seen by the later history rows and all candidates of its user (the next
+# segment); a candidate key only by itself
+region seg_idx(i) % 2 == 0 : j >= i && j < seg_end_at(seg_idx(i) + 1)
+region seg_idx(i) % 2 == 1 : j == i
 """,
 }

@@ -13,6 +13,8 @@ used there is not available, so every length is drawn here instead):
   3 shared-prompt RM         B=1  H=32 S=32768  d=128  prompt P ~ U[S/8, 3S/8], then 4 responses
   4 HSTU                     B=4  H=16 S=16384  d=128  history h ~ U[S/2, S - S/16] per sample
   5 three-interval packed    B=2  H=32 S=32768  d=128  prefix S/64, documents ~ U[S/32, 3S/16]
+  6 varlen packed HSTU       B=2  H=16 S=32768  d=128  users of length ~ U[S/32, S/4] packed to S,
+                                                     each a history (50-90 %) then candidates
 
 Metadata layout: ``seg`` is int32 [B, nseg_max + 1] with seg[b, 0] = 0 and seg[b, nseg[b]] = S,
 entries past nseg[b] repeat S; ``nseg`` is int32 [B].
@@ -41,6 +43,7 @@ WORKLOADS = {
     3: Workload(3, "shared_prompt_rm_32k", 1, 32, 32768, 128),
     4: Workload(4, "hstu_16k", 4, 16, 16384, 128),
     5: Workload(5, "three_interval_packed_32k", 2, 32, 32768, 128),
+    6: Workload(6, "varlen_hstu_packed_32k", 2, 16, 32768, 128),
 }
 
 
@@ -94,6 +97,26 @@ def segments(wid: int, B: int, S: int, seed: int | None = None) -> tuple[np.ndar
                 n = min(n, S - total)
                 lens.append(n)
                 total += n
+        elif wid == 6:
+            # users packed back to back (variable lengths, as in a batch of recommendation
+            # sequences); the last one takes the remainder, or joins the previous user when the
+            # remainder is too short; each user splits into history and candidates
+            lo, hi = max(4, S // 32), max(8, S // 4)
+            users: list[int] = []
+            total = 0
+            while total < S:
+                n = int(rng.integers(lo, hi, endpoint=True))
+                n = min(n, S - total)
+                if n < max(4, S // 128) and users:
+                    users[-1] += n
+                else:
+                    users.append(n)
+                total += n
+            lens = []
+            for n in users:
+                h = int(np.floor(n * rng.uniform(0.5, 0.9)))
+                h = min(max(h, 1), n - 1)
+                lens += [h, n - h]
         else:
             raise ValueError(f"unknown workload {wid}")
         out.append([int(x) for x in lens])

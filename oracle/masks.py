@@ -23,7 +23,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
 Segment conventions: seg_row[k] is the first position of segment k, seg_row[nseg] = S.
   workload 3: segment 0 is the prompt (P = seg_row[1]), segments 1..4 the responses;
   workload 4: segment 0 is the history (h = seg_row[1]), segment 1 the candidates;
-  workload 5: segment 0 is the system prefix (b = seg_row[1]), segments 1.. the documents.
+  workload 5: segment 0 is the system prefix (b = seg_row[1]), segments 1.. the documents;
+  workload 6: variable-length packing of users, each as two consecutive segments: segment 2u
+  is user u's history, segment 2u + 1 its candidates (the HSTU rule applied per user).
 """
 from __future__ import annotations
 
@@ -34,7 +36,7 @@ PREV_DOC_HEAD = 64  # workload 5: tokens of the previous document that stay visi
 
 def num_intervals(wid: int) -> tuple[int, int]:
     """Forward / backward interval counts of each workload's rule (max over its regions)."""
-    return {1: (1, 1), 2: (1, 1), 3: (2, 1), 4: (2, 1), 5: (3, 2)}[wid]
+    return {1: (1, 1), 2: (1, 1), 3: (2, 1), 4: (2, 1), 5: (3, 2), 6: (2, 1)}[wid]
 
 
 def segment_index(seg_row: np.ndarray, nseg: int, pos: np.ndarray) -> np.ndarray:
@@ -80,6 +82,13 @@ def dense_mask(wid: int, seg_row: np.ndarray, nseg: int, S: int,
                           | (has_prev_doc & (j >= prev_start) & (j < head_end))
                           | ((j >= start_i) & (j <= i)))
         return prefix | doc
+    if wid == 6:   # per user: history rows causal within the history; a candidate row sees the
+        #           user's history and itself
+        in_hist = (ki % 2) == 0
+        hist_start = np.where(in_hist, start_i, seg[np.maximum(ki - 1, 0)])
+        history = in_hist & (j >= start_i) & (j <= i)
+        candidate = (~in_hist) & (((j >= hist_start) & (j < start_i)) | (j == i))
+        return history | candidate
     raise ValueError(wid)
 
 
@@ -115,6 +124,8 @@ def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.n
             else:
                 ps, pe = seg[k - 1], seg[k]
                 slots = [(0, seg[1]), (ps, min(ps + PREV_DOC_HEAD, pe)), (seg[k], i + 1)]
+        elif wid == 6:
+            slots = [(seg[k], i + 1)] if k % 2 == 0 else [(seg[k - 1], seg[k]), (i, i + 1)]
         else:
             raise ValueError(wid)
         for n, (lo, hi) in enumerate(slots):
@@ -146,6 +157,10 @@ def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.n
                 if j < seg[k] + PREV_DOC_HEAD and k + 1 < nseg:
                     nxt = (seg[k + 1], seg[k + 2])
                 slots = [(j, end_k), nxt]
+        elif wid == 6:
+            # a history key is seen by the later history rows and every candidate of its user
+            # (the candidate segment follows the history); a candidate key only by itself
+            slots = [(j, seg[k + 2])] if k % 2 == 0 else [(j, j + 1)]
         else:
             raise ValueError(wid)
         for n, (lo, hi) in enumerate(slots):

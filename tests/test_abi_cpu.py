@@ -43,7 +43,7 @@ def test_region_c_lowering(B):
     assert "slot 1: [seg_start(i), i + 1)" in region1
 
 
-@pytest.mark.parametrize("wid,nif,nib", [(1, 1, 1), (2, 1, 1), (3, 2, 1), (4, 2, 1), (5, 3, 2)])
+@pytest.mark.parametrize("wid,nif,nib", [(1, 1, 1), (2, 1, 1), (3, 2, 1), (4, 2, 1), (5, 3, 2), (6, 2, 1)])
 def test_interval_counts(B, wid, nif, nib):
     from masked_flashattention_gb300 import specs
     from oracle import masks as M
@@ -75,6 +75,19 @@ def test_conditions_without_j_become_slot_conditions(B):
     s = B.cm_compile_spec("region all : j <= i || (i < 100 && j == 200)")
     text = B.cm_spec_describe(s)
     assert "slot 1: [200, 201) if i - 100 < 0" in text
+
+
+def test_modulo_by_a_constant():
+    """'%' by a positive constant: a guard on the parity of the segment index lowers to a
+    remainder term; constant remainders fold; other divisors are rejected."""
+    from masked_flashattention_gb300 import binding as B
+    d = B.cm_spec_describe(B.cm_compile_spec("region seg_idx(i) % 2 == 1 : j <= i"))
+    assert "mod(seg_idx(i), 2) == 1" in d
+    d = B.cm_spec_describe(B.cm_compile_spec("region all : j < 7 % 4 + i"))
+    assert "[0, i + 3)" in d
+    for bad in ("region all : j < i % 0", "region all : j < i % i", "region all : j % 2 < i"):
+        with pytest.raises(B.CMError):
+            B.cm_compile_spec(bad)
 
 
 @pytest.mark.parametrize("bad", [
@@ -147,7 +160,7 @@ def test_error_strings(B):
         assert B.cm_error_string(code)
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_generated_preprocess_kernels_compile(B, wid):
     """Each workload spec's mask-specific preprocess kernel (section 3.1) compiles with NVRTC for
     sm_103a (host only; loading needs a GPU and is checked by the GPU tests)."""

@@ -78,7 +78,7 @@ def check_heads(wid, seg, nseg, Q, K, V, dO, out, heads, mask_fn=None):
             _assert_close(f"dV b{b}h{h}", dv[b, h], rv)
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 @pytest.mark.parametrize("d", [64, 128])
 def test_small_all_heads(wid, d):
     from masked_flashattention_gb300 import specs
@@ -125,7 +125,7 @@ def test_rows_and_columns_that_see_nothing():
     check_heads(0, seg, nseg, Q, K, V, dO, out, range(2), mask_fn=lambda r0, r1: dense[r0:r1])
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_full_size_sampled_heads(wid):
     from masked_flashattention_gb300 import specs
     B = _lib()
@@ -141,7 +141,7 @@ CHECKS = {"two_compare": 1, "masked": 2}
 
 
 @pytest.mark.parametrize("check", sorted(CHECKS))
-@pytest.mark.parametrize("wid", [1, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 3, 4, 5, 6])
 def test_interval_check_forms_small(wid, check):
     """The two-compare and masked-interval forms of the partial-tile check (the paper's section
     4.4 ablation) give the same attention as the oracle, on masks with 1 to 3 intervals per row."""

@@ -68,7 +68,7 @@ def _check(desc, wid, seg, nseg, S):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_descriptor_full_size(wid, mode):
     B = _lib()
     w = W.WORKLOADS[wid]
@@ -78,7 +78,7 @@ def test_descriptor_full_size(wid, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 @pytest.mark.parametrize("S", [128, 384, 1024, 2048])
 def test_descriptor_small_seeded(wid, S, mode):
     B = _lib()
@@ -107,7 +107,7 @@ def test_bad_metadata_is_reported_not_faulted():
     assert B.cm_get_status(desc) == B.CM_OK
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_generated_kernels_load_and_agree_with_the_generic_kernel(wid):
     """The mask-specific kernels compile and load on this GPU (so the default mode really runs
     them), and build the same bytes as the generic kernel on a batch of several samples."""

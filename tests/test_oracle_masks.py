@@ -18,7 +18,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _small_cases():
-    for wid in (1, 2, 3, 4, 5):
+    for wid in (1, 2, 3, 4, 5, 6):
         for S in (256, 512, 1024):
             for seed in range(3):
                 seg, nseg = W.segments(wid, 2, S, seed=seed * 7 + wid)
@@ -86,6 +86,12 @@ def closed_form_visible(wid, seg, nseg, S):
             if d >= 2:
                 tot += L[d] * min(64, L[d - 1])
         return tot
+    if wid == 6:  # per user: a causal history of h rows, then c candidates that see h + 1 keys
+        tot = 0
+        for u in range(0, nseg, 2):
+            h, c = L[u], L[u + 1]
+            tot += h * (h + 1) // 2 + c * (h + 1)
+        return tot
     raise ValueError(wid)
 
 
@@ -95,7 +101,7 @@ def test_visible_count_closed_form_small(case):
     assert int(M.dense_mask(wid, seg, nseg, S).sum()) == closed_form_visible(wid, seg, nseg, S)
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_visible_count_closed_form_full_size(wid):
     w = W.WORKLOADS[wid]
     seg, nseg = W.segments(wid, w.B, w.S)
@@ -182,7 +188,7 @@ def test_unsigned_interval_check_exhaustive():
     assert not one[(s == 0) & (e == 0)].any()
 
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_interval_count_matches_visible_runs(wid):
     """The forward interval count is tight: some row has exactly that many separate visible
     runs (workload 5 rows see three, which a two-interval encoding could not hold); no row or
@@ -197,3 +203,19 @@ def test_interval_count_matches_visible_runs(wid):
     nif, nib = M.num_intervals(wid)
     assert int(runs(dense).max()) == nif
     assert int(runs(dense.T).max()) <= nib
+
+
+def test_varlen_users_are_independent():
+    """Workload 6 packs users back to back: no query row sees a key of another user, and a
+    user's block of the mask equals the single-sample HSTU mask (workload 4) of that user's
+    history and candidates, shifted to the user's offset."""
+    S = 2048
+    seg, nseg = W.segments(6, 1, S, seed=3)
+    seg, n = seg[0], int(nseg[0])
+    dense = M.dense_mask(6, seg, n, S)
+    for u in range(0, n, 2):
+        a, h_end, e = int(seg[u]), int(seg[u + 1]), int(seg[u + 2])
+        block = dense[a:e, a:e]
+        one = np.array([0, h_end - a, e - a, e - a], dtype=np.int64)
+        np.testing.assert_array_equal(block, M.dense_mask(4, one, 2, e - a))
+        assert not dense[a:e, :a].any() and not dense[a:e, e:].any()
