@@ -42,6 +42,19 @@ def _not_self_causal(i, j, sg, n, S):
     return (j <= i) & (j != i) | ((i == 0) & (j == 0))
 
 
+def _four_intervals(i, j, sg, n, S):
+    k, start, _ = _seg_arrays(sg, n, S)
+    ki = k[i]
+
+    def head(m):  # the first 8 positions of segment m (fewer if it is shorter)
+        h0 = sg[np.clip(m, 0, n)]
+        h1 = np.minimum(h0 + 8, sg[np.clip(m + 1, 0, n)])
+        return (j >= h0) & (j < h1)
+
+    far = (ki >= 2) & (head(ki - 2) | head(ki - 1))
+    return (j < 16) | ((j >= start[i]) & (j <= i)) | far
+
+
 RULES = [
     ("sliding_window_200",
      "region all : j > i - 200 && j <= i",
@@ -58,6 +71,19 @@ RULES = [
      "region i < 32 : j >= 0\n"
      "region all : (j >= seg_start(i) && j < seg_end(i)) || j < 32",
      _doc_bidir_global),
+    # four visible intervals per row (the compiler's slot limit; the CLEAR-style multi-interval
+    # case): 16 sink tokens, the heads of the two previous segments, the own segment causally
+    ("sink_two_previous_heads_and_own_segment",
+     "region seg_idx(i) >= 2 : j < 16 "
+     "|| (j >= seg_start_at(seg_idx(i) - 2) && j < min(seg_start_at(seg_idx(i) - 2) + 8, seg_end_at(seg_idx(i) - 2))) "
+     "|| (j >= seg_start_at(seg_idx(i) - 1) && j < min(seg_start_at(seg_idx(i) - 1) + 8, seg_end_at(seg_idx(i) - 1))) "
+     "|| (j >= seg_start(i) && j <= i)\n"
+     "region all : j < 16 || (j >= seg_start(i) && j <= i)",
+     "region i < 16 : j >= 0\n"
+     "region seg_idx(i) == 0 && i < seg_start(i) + 8 : (j >= i && j < seg_end(i)) || (j >= seg_start_at(2) && j < seg_end_at(2))\n"
+     "region i < seg_start(i) + 8 : (j >= i && j < seg_end(i)) || (j >= seg_start_at(seg_idx(i) + 1) && j < seg_end_at(seg_idx(i) + 2))\n"
+     "region all : j >= i && j < seg_end(i)",
+     _four_intervals),
     ("causal_without_the_diagonal",
      "region i == 0 : j == 0\n"
      "region all : j < i",
@@ -124,3 +150,11 @@ def test_attention_on_custom_rule(rule):
                 rel = ((g - want).norm() / want.norm()).item()
                 mx = (g - want).abs().max().item()
                 assert rel <= 1e-2 and mx <= 3e-2, f"{name} {nm} b{b}h{h}: {rel:.3e} {mx:.3e}"
+
+
+def test_four_interval_rule_uses_four_slots():
+    from masked_flashattention_gb300 import binding as B
+    B.lib()
+    rule = [r for r in RULES if r[0] == "sink_two_previous_heads_and_own_segment"][0]
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(rule[1])) == 4
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(rule[2])) == 2
