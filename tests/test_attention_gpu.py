@@ -173,3 +173,45 @@ def test_interval_check_forms_full_size_hstu(check):
     finally:
         B.cm_set_interval_check(B.CM_CHECK_UNSIGNED)
     check_heads(4, seg, nseg, Q, K, V, dO, out, sorted({0, w.H - 1}))
+
+
+def test_maximum_sequence_length_causal():
+    """The largest supported sequence (S = 131072, 1024 tiles per row) on a causal mask.  The
+    oracle runs on the first and the last 128 query rows against all keys: that gives O, LSE
+    and dQ of those rows, and the complete dK and dV of the last 128 keys, which no other row
+    sees.  The descriptor is checked against the closed-form causal tables and tile census."""
+    from masked_flashattention_gb300 import specs
+    B = _lib()
+    S, H, d = 131072, 1, 128
+    seg = np.array([[0, S]], dtype=np.int32)
+    nseg = np.array([1], dtype=np.int32)
+    w = W.Workload(2, "causal@S131072", 1, H, S, d)
+    Q, K, V, dO = W.full_tensors(w, seed=17)
+    f = B.cm_compile_spec(specs.FWD[2])
+    b = B.cm_compile_spec(specs.BWD[2])
+    desc = B.Descriptor(f, b, 1, S)
+    B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
+    q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
+    o, lse = B.attention_forward(desc, q, k, v)
+    dq, dk, dv = B.attention_backward(desc, q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    assert B.cm_get_status(desc) == 0
+    # descriptor: row i sees [0, i + 1); tile census n(n-1)/2 full, n partial, the rest empty
+    itf = desc.interval_table_fwd()[0, 0]
+    np.testing.assert_array_equal(itf[:, 0], np.zeros(S, dtype=np.int32))
+    np.testing.assert_array_equal(itf[:, 1], np.arange(1, S + 1, dtype=np.int32))
+    words = desc.bitmap_fwd()[0]
+    codes = np.stack([(words >> (2 * t)) & 3 for t in range(16)], axis=-1).reshape(words.shape[0], -1)
+    n = S // 128
+    assert int((codes == 2).sum()) == n * (n - 1) // 2 and int((codes == 1).sum()) == n
+    for r0 in (0, S - 128):
+        R = slice(r0, r0 + 128)
+        mask = lambda a, c, r0=r0: (np.arange(S)[None, :] <= (r0 + np.arange(a, c))[:, None])
+        ro, rl = A.attention_forward(Q[0, 0, R], K[0, 0], V[0, 0], mask)
+        rq, rk, rv = A.attention_backward(Q[0, 0, R], K[0, 0], V[0, 0], dO[0, 0, R], mask)
+        _assert_close(f"O rows {r0}+", o[0, 0, R].cpu(), ro)
+        _assert_close(f"LSE rows {r0}+", lse[0, 0, R].cpu(), rl)
+        _assert_close(f"dQ rows {r0}+", dq[0, 0, R].cpu(), rq)
+        if r0 == S - 128:
+            _assert_close("dK last keys", dk[0, 0, R].cpu(), rk[R])
+            _assert_close("dV last keys", dv[0, 0, R].cpu(), rv[R])
