@@ -19,17 +19,17 @@
 //              masks partial tiles, runs its half's online softmax in the log2 domain, writes P
 //              (bf16 pairs) back over the S columns it has read, rescales its half's O when the
 //              running max moved, and at the end merges the halves and writes O and the LSE.
-//   warp 8     TMA producer: Q once, then K and V of each visited key tile through two 3-slot
-//              rings (a K slot frees when its S MMA completes, a V slot when both PV MMAs
-//              completed).
+//   warp 8     TMA producer: Q once, then K and V of each visited key tile into one of 3 stages
+//              (one barrier for both tiles; the stage frees when the tile's PV MMAs completed).
 //   warp 9     MMA issuer (one thread): S = Q K^T (Q and K from shared memory) and, per half,
 //              O_h += P_h V_h with P_h read from TMEM.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O_0 [256, 256+d), O_1 [384, 384+d).  P of tile n
 // lives in S buffer n % 2: keys [0,64) in columns [0,32), keys [64,128) in [64,96).
 // Ordering without extra barriers: the MMA issues S(n+2) into a buffer only after it saw P(n) and
 // issued PV(n), which reads P(n) from that buffer; tcgen05 MMAs of one thread run in issue order.
-// The softmax warps wait for their half's PV(n-1) only when they must rescale O: the completion
-// of S(n), which they wait for anyway, already covers every PV issued before it (up to PV(n-2)).
+// The softmax warps wait for PV(n-1) (its stage's release) only when they must rescale O: the
+// completion of S(n), which they wait for anyway, already covers every PV issued before it (up to
+// PV(n-2)).
 // The running max is refreshed lazily: O and l are rescaled only when the row max grows by more
 // than 2^8, which keeps P <= 256 and the result exact because O, l and the LSE use the same max.
 #include <cuda_bf16.h>
@@ -57,27 +57,26 @@ template <int D>
 struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kQ = 0;  // also the merge exchange area once every MMA is done
-  static constexpr uint32_t kK = kTileBytes;
-  static constexpr uint32_t kV = kK + kStages * kTileBytes;
-  static constexpr uint32_t kBar = kV + kStages * kTileBytes;
+  static constexpr uint32_t kKV = kTileBytes;  // stage s: K at kKV + 2*s*tile, V right after it
+  static constexpr uint32_t kBar = kKV + kStages * 2u * kTileBytes;
   static constexpr uint32_t kRow = kBar + 256u;  // bitmap row: at most 64 words (NT <= 1024)
   static constexpr uint32_t kTotal = kRow + 256u;
   static constexpr uint32_t kAlloc = kTotal + 1024u;  // slack for 1024-byte alignment
 };
 static_assert(Smem<128>::kAlloc <= 232448, "forward shared memory exceeds 227 KB");
 
+// The MMA thread waits twice per key tile (P ready, next K/V landed) and commits twice (S ready,
+// PV done): every wait of the issuing thread leaves a gap in the tensor pipe, so the barriers are
+// shared where the ordering allows it.
 enum {
   B_Q = 0,        // Q tile in shared memory (TMA)
-  B_KFULL = 1,    // +stage
-  B_VFULL = 4,    // +stage
-  B_KEMPTY = 7,   // +stage: the S MMA that read the K slot has completed
-  B_VEMPTY = 10,  // +stage: both PV MMAs that read the V slot have completed
-  B_SFULL = 13,   // +buffer
-  B_PFULL = 15,   // +2*half+buffer: the half's P of a tile in that S buffer (4 arrivals)
-  B_ODONE = 19,   // +half: the half's PV of the tile has completed
-  B_PAIR = 21,    // +quarter: merge exchange of a warp pair (2 arrivals, once)
-  B_ALLDONE = 25, // every MMA of the CTA has completed (once)
-  B_COUNT = 26
+  B_KVFULL = 1,   // +stage: K and V of a key tile landed (TMA, 2 tiles of bytes)
+  B_KVEMPTY = 4,  // +stage: S and PV of the stage's tile have completed (also "O is up to date")
+  B_SFULL = 7,    // +buffer
+  B_PFULL = 9,    // +buffer: P of a tile in that S buffer, both halves (8 arrivals)
+  B_PAIR = 11,    // +quarter: merge exchange of a warp pair (2 arrivals, once)
+  B_ALLDONE = 15, // every MMA of the CTA has completed (once)
+  B_COUNT = 16
 };
 
 template <int D>
@@ -110,16 +109,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     *abort_flag = 0;
     mbar_init(bar(B_Q), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
-      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_KVFULL + s), 1);
+      mbar_init(bar(B_KVEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_ODONE + s), 1);
+      mbar_init(bar(B_PFULL + s), kSoftmaxWarps);
     }
-    for (int s = 0; s < 4; ++s) mbar_init(bar(B_PFULL + s), kSoftmaxWarps / 2);
     for (int s = 0; s < 4; ++s) mbar_init(bar(B_PAIR + s), 2);
     mbar_init(bar(B_ALLDONE), 1);
     fence_barrier_init();
@@ -160,19 +156,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
         const int st = n % kStages;
         if (n >= kStages &&
-            !mbar_wait(bar(B_KEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
+            !mbar_wait(bar(B_KVEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
           break;
-        mbar_arrive_expect_tx(bar(B_KFULL + st), L::kTileBytes);
+        const uint32_t sK = sbase + L::kKV + st * 2u * L::kTileBytes;
+        mbar_arrive_expect_tx(bar(B_KVFULL + st), 2u * L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kK + st * L::kTileBytes + x * 16384u, &tmK, x * 64,
-                      row0 + kt * 128, bar(B_KFULL + st));
-        if (n >= kStages &&
-            !mbar_wait(bar(B_VEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x10d))
-          break;
-        mbar_arrive_expect_tx(bar(B_VFULL + st), L::kTileBytes);
+          tma_load_2d(sK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KVFULL + st));
         for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kV + st * L::kTileBytes + x * 16384u, &tmV, x * 64,
-                      row0 + kt * 128, bar(B_VFULL + st));
+          tma_load_2d(sK + L::kTileBytes + x * 16384u, &tmV, x * 64, row0 + kt * 128,
+                      bar(B_KVFULL + st));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -180,44 +172,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // A = Q, B = K, both K-major
       constexpr uint32_t idO = make_idesc_bf16(128, D, 0, 1);    // A = P (TMEM), B = V MN-major
-      const uint32_t sQ = sbase + L::kQ;
+      const uint32_t dQ = sdesc_lo(sbase + L::kQ, 16u);
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, 0x102);
-      // O_h += P_h V_h for tile m: keys [64h, +64) are the K-steps kk = 4h .. 4h+3
+      // O_h += P_h V_h for tile m: keys [64h, +64) are the K-steps kk = 4h .. 4h+3.  V(m) landed
+      // before S(m) was issued (same barrier as K(m)).
       auto issue_pv = [&](int m) -> bool {
         const int st = m % kStages;
-        if (!mbar_wait(bar(B_VFULL + st), (m / kStages) & 1, abort_flag, p.status, 0x104))
+        // one barrier per S buffer: the softmax warps can be at most one tile ahead of this
+        // wait, so a barrier never runs two phases ahead of its waiter
+        if (!mbar_wait(bar(B_PFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x103))
           return false;
-        const uint32_t sV = sbase + L::kV + st * L::kTileBytes;
+        tc_fence_after();
+        const uint32_t dV = sdesc_lo(sbase + L::kKV + st * 2u * L::kTileBytes + L::kTileBytes, 16384u);
         const uint32_t sP = tmem + kColS + (m & 1) * 128;
+        const uint32_t acc0 = m > 0 ? 1u : 0u;
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          // one barrier per (half, S buffer): a half's warps can be at most one tile ahead of
-          // this wait, so a barrier never runs two phases ahead of its waiter
-          if (!mbar_wait(bar(B_PFULL + 2 * hh + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x103))
-            return false;
-          tc_fence_after();
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = 4 * hh + k4;
-            umma_ts(tmem + kColO + 128 * hh, sP + 64 * hh + 8 * k4, sdesc_mnmajor(sV, kk, 16384u),
-                    idO, (m > 0 || k4 > 0) ? 1u : 0u);
+            umma_ts_lo(tmem + kColO + 128 * hh, sP + 64 * hh + 8 * k4, dV + kstep_mnmajor(kk), idO,
+                       k4 > 0 ? 1u : acc0);
           }
-          umma_commit(bar(B_ODONE + hh));
         }
-        umma_commit(bar(B_VEMPTY + st));
+        umma_commit(bar(B_KVEMPTY + st));
         return true;
       };
       // S(n) into buffer n % 2 = Q K(n)^T
       auto issue_s = [&](int n) -> bool {
         const int st = n % kStages;
-        if (!mbar_wait(bar(B_KFULL + st), (n / kStages) & 1, abort_flag, p.status, 0x105)) return false;
+        if (!mbar_wait(bar(B_KVFULL + st), (n / kStages) & 1, abort_flag, p.status, 0x105))
+          return false;
         tc_fence_after();
-        const uint32_t sK = sbase + L::kK + st * L::kTileBytes;
+        const uint32_t dK = sdesc_lo(sbase + L::kKV + st * 2u * L::kTileBytes, 16u);
+        const uint32_t dS = tmem + kColS + (n & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS + (n & 1) * 128, sdesc_kmajor(sQ, kk, 16384u),
-                  sdesc_kmajor(sK, kk, 16384u), idS, kk > 0 ? 1u : 0u);
+          umma_ss_lo(dS, dQ + kstep_kmajor(kk), dK + kstep_kmajor(kk), idS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL + (n & 1)));
-        umma_commit(bar(B_KEMPTY + st));
         return true;
       };
       // Both S buffers first; then per tile: PV(n) as soon as its P is written, and S(n+2) into
@@ -298,9 +290,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       l_run = l_run * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
       if (n >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-        // rescale this half's O: its PV(n-1) must be complete (PV(n-2) and earlier are, since
-        // S(n) is)
-        const bool o_ready = mbar_wait(bar(B_ODONE + hf), (n - 1) & 1, abort_flag, p.status, 0x108);
+        // rescale this half's O: PV(n-1) must be complete (PV(n-2) and earlier are, since S(n)
+        // is).  Its stage barrier is at most one phase ahead of this wait: PV(n+2) needs this
+        // warp's P(n+2).
+        const bool o_ready = mbar_wait(bar(B_KVEMPTY + (n - 1) % kStages), ((n - 1) / kStages) & 1,
+                                       abort_flag, p.status, 0x108);
         __syncwarp();
         if (!o_ready) { ok = false; break; }
         tc_fence_after();
@@ -319,7 +313,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + 2 * hf + sb));
+      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
     }
 
     // ---- epilogue: merge the two halves, O -> bf16, LSE (natural log) ----

@@ -197,15 +197,13 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn_ma
 }
 
 // shared-memory matrix descriptor with the 128-byte swizzle
-__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                     uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
-  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
-  return d;
+__host__ __device__ constexpr uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                        uint32_t sbo_bytes) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) |
+         (static_cast<uint64_t>(1) << 46)  // descriptor version for tcgen05
+         | (static_cast<uint64_t>(2) << 61);  // 128-byte swizzle
 }
 // K-major operand, 16-element K step `kk` of a tile made of 64-column boxes `box_bytes` apart
 __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t tile, int kk, uint32_t box_bytes) {
@@ -217,6 +215,52 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t tile, int kk, uint32_t
 __device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t tile, int kk, uint32_t box_bytes) {
   const uint32_t addr = tile + static_cast<uint32_t>(kk) * 2048u;
   return make_sdesc_sw128(addr, box_bytes, 1024u);
+}
+
+// The same SW128 descriptors split into halves for a lean issue loop.  The high word (stride
+// 1024 B, version, swizzle) is one constant for every operand here; the low word holds the
+// address field (bits 0-13, address >> 4) and the leading byte offset.  A shared address below
+// 256 KB gives an address field below 2^14, so the K step of an operand is one 32-bit add of
+// (step offset >> 4) to its base low word: no carry leaves the field.
+constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+// low-word offset of K step kk: K-major (64-column boxes 16 KB apart, 32 B per step inside a
+// box) and MN-major (16 rows of 128 B per step)
+__host__ __device__ constexpr uint32_t kstep_kmajor(int kk) {
+  return static_cast<uint32_t>(kk >> 2) * (16384u >> 4) + static_cast<uint32_t>(kk & 3) * 2u;
+}
+__host__ __device__ constexpr uint32_t kstep_mnmajor(int kk) {
+  return static_cast<uint32_t>(kk) * (2048u >> 4);
+}
+// the split form gives the full descriptors bit for bit (last K step of a tile at 208 KB)
+static_assert(make_sdesc_sw128(0x34000u + 16384u + 3 * 32u, 16u, 1024u) ==
+                  ((static_cast<uint64_t>(kSdescHi) << 32) | (sdesc_lo(0x34000u, 16u) + kstep_kmajor(7))),
+              "K-major split descriptor");
+static_assert(make_sdesc_sw128(0x34000u + 7 * 2048u, 16384u, 1024u) ==
+                  ((static_cast<uint64_t>(kSdescHi) << 32) | (sdesc_lo(0x34000u, 16384u) + kstep_mnmajor(7))),
+              "MN-major split descriptor");
+__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi)
+      : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (quarter*32 + t), cols c..c+31
