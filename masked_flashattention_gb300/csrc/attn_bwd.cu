@@ -21,8 +21,8 @@
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
 //              half w / 4: queries [64*half, +64) of S^T / dP^T and head-dim columns
 //              [half*d/2, +d/2) of dV and dK.
-//   warp 8     TMA producer: K, V once; per query tile Q (+ LSE*log2e by bulk copy) and dO
-//              (+ D), each into one of two slots.
+//   warp 8     TMA producer: K, V once; per query tile Q and dO (+ LSE*log2e and D by bulk
+//              copy) into one of two slots, one barrier per slot.
 //   warp 9     MMA issuer (one thread).
 // TMEM (512 columns): dV [0, d), dK [128, 128+d), and two 128-column regions RA [256, 384),
 // RB [384, 512) whose roles alternate between query tiles.  For tile m with X = RA (m even) or
@@ -81,16 +81,15 @@ static_assert(Smem<128>::kAlloc <= 232448, "backward shared memory exceeds 227 K
 
 enum {
   B_KV = 0,        // K and V loaded
-  B_QFULL = 1,     // +slot: Q and LSE*log2e of a query tile loaded
-  B_QEMPTY = 3,    // +slot: the dK MMA (last reader of that Q slot) is done
-  B_DOFULL = 5,    // +slot: dO and D of a query tile loaded
-  B_DOEMPTY = 7,   // +slot: the dV MMA (last reader of that dO slot) is done
-  B_SFULL = 9,     // S^T of the current tile computed
-  B_DPFULL = 10,   // dP^T of the current tile computed
-  B_PDS = 11,      // compute warps wrote dS^T (TMEM) and read dP^T (8 arrivals)
-  B_DONE = 12,     // every MMA of the CTA completed (dK, dV final)
-  B_PREADY = 13,   // compute warps wrote P^T (TMEM) (8 arrivals)
-  B_COUNT = 14
+  B_QFULL = 1,     // +slot: Q, dO, LSE*log2e and D of a query tile loaded (one barrier: each
+                   // wait of the MMA thread leaves a gap in the tensor pipe)
+  B_QEMPTY = 3,    // +slot: the dK MMA (last reader of the slot, after dV) is done
+  B_SFULL = 5,     // S^T of the current tile computed
+  B_DPFULL = 6,    // dP^T of the current tile computed
+  B_PDS = 7,       // compute warps wrote dS^T (TMEM) and read dP^T (8 arrivals)
+  B_DONE = 8,      // every MMA of the CTA completed (dK, dV final)
+  B_PREADY = 9,    // compute warps wrote P^T (TMEM) (8 arrivals)
+  B_COUNT = 10
 };
 
 
@@ -186,8 +185,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_QFULL + x), 1);
       mbar_init(bar(B_QEMPTY + x), 1);
-      mbar_init(bar(B_DOFULL + x), 1);
-      mbar_init(bar(B_DOEMPTY + x), 1);
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
@@ -235,22 +232,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int m = 0; m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
         const int slot = m & 1;
         const size_t r = static_cast<size_t>(row0) + qt * 128;
-        // a Q slot is free once the dK MMA of the tile two back is done, a dO slot once its dV
-        // MMA is done
+        // a slot is free once the dK MMA of the tile two back (its last reader) is done
         if (m >= 2 && !mbar_wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x201))
           break;
-        mbar_arrive_expect_tx(bar(B_QFULL + slot), L::kTileBytes + 512u);
-        for (int x = 0; x < D / 64; ++x)
+        const uint32_t full = bar(B_QFULL + slot);
+        mbar_arrive_expect_tx(full, 2u * (L::kTileBytes + 512u));
+        for (int x = 0; x < D / 64; ++x) {
           tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
-                      row0 + qt * 128, bar(B_QFULL + slot));
-        bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, bar(B_QFULL + slot));
-        if (m >= 2 && !mbar_wait(bar(B_DOEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x20b))
-          break;
-        mbar_arrive_expect_tx(bar(B_DOFULL + slot), L::kTileBytes + 512u);
-        for (int x = 0; x < D / 64; ++x)
+                      row0 + qt * 128, full);
           tma_load_2d(sbase + L::kdO + slot * L::kTileBytes + x * 16384u, &tmdO, x * 64,
-                      row0 + qt * 128, bar(B_DOFULL + slot));
-        bulk_load(sbase + L::kDelta + slot * 512u, p.delta + r, 512u, bar(B_DOFULL + slot));
+                      row0 + qt * 128, full);
+        }
+        bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, full);
+        bulk_load(sbase + L::kDelta + slot * 512u, p.delta + r, 512u, full);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -269,7 +263,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           umma_ss(tmem + kColRA, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sbase + L::kQ, kk, 16384u),
                   idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL));
-        ok = mbar_wait(bar(B_DOFULL), 0, abort_flag, p.status, 0x20c);
       }
       if (ok) {
         tc_fence_after();
@@ -292,7 +285,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                   sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_DOEMPTY + (m & 1)));
         if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
         tc_fence_after();
         if (m + 1 < nt) {
@@ -316,10 +308,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         umma_commit(bar(B_QEMPTY + (m & 1)));
         if (m + 1 < nt) {
           // dP^T of the next tile into X, after dV and dK above have read P^T and dS^T from it
+          // (its dO landed with its Q, waited for before S^T)
           const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
-          if (!mbar_wait(bar(B_DOFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x20c))
-            break;
-          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdOn, kk, 16384u), idSS,
@@ -378,8 +368,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (lane == 0) mbar_arrive(bar(B_PREADY));
 
       // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T as bf16 pairs into X ----
-      ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e) &&
-              mbar_wait(bar(B_DOFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x20d);
+      ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();

@@ -14,8 +14,9 @@
 //              column half w / 4 of each 128-key tile: P = exp2(S * scale*log2e - LSE*log2e),
 //              dS = P * (dP - D), written back as bf16 pairs over the S columns it has read.
 //   warp 8     TMA producer: Q and dO once; K through a 3-slot ring, V through a 2-slot ring.
-//   warp 9     MMA issuer (one thread).  Per key tile n: S(n+1) = Q K^T into the other S buffer,
-//              dQ += dS(n) K(n) (A operand dS from TMEM), dP(n+1) = dO V^T.
+//   warp 9     MMA issuer (one thread).  Per key tile n: S(n+1) = Q K^T into the other S buffer;
+//              once dS(n) is written, dP(n+1) = dO V^T and dQ += dS(n) K(n) (A operand dS from
+//              TMEM).
 // TMEM (512 columns): S0 [0,128), S1 [128,256), dP [256,384), dQ [384, 384+d).
 // A buffer is rewritten only by MMAs issued after the ones that read it: tcgen05 MMAs of one
 // thread run in issue order.
@@ -204,6 +205,9 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (n + 1 < nt && !issue_s(n + 1)) break;  // its buffer's dS(n-1) was read by dQ(n-1)
         if (!mbar_wait(bar(B_DSFULL), n & 1, abort_flag, p.status, 0x306)) break;
         tc_fence_after();
+        // dP(n+1) first: the compute warps have read dP(n), and the next tile's dS waits for it,
+        // while dQ(n) only feeds the accumulator
+        if (n + 1 < nt && !issue_dp(n + 1)) break;
         // dQ += dS(n) K(n): dS pairs of keys [0,64) at S columns [0,32), [64,128) at [64,96)
         const int sk = n % kKStages;
         const uint32_t sK = sbase + L::kK + sk * L::kTileBytes;
@@ -213,11 +217,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           umma_ts(tmem + kColDQ, sS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                   sdesc_mnmajor(sK, kk, 16384u), idQ, (n > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_KEMPTY + sk));
-        if (n + 1 < nt) {
-          if (!issue_dp(n + 1)) break;
-        } else {
-          umma_commit(bar(B_DONE));
-        }
+        if (n + 1 == nt) umma_commit(bar(B_DONE));
       }
     }
   } else {
