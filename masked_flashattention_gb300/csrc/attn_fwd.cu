@@ -259,13 +259,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int j0 = kt * 128 + 64 * hf;
         mask_cols_any(s, j0, ri, p.NI, p.check);
       }
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[32], s[33]);
+      // row max of the 64 scores as a tree of 3-input maxima (depth 4: 64 -> 22 -> 8 -> 3 -> 1),
+      // so the two softmax warps of an SMSP do not wait on one long dependent chain
+      float a[22], c8[8];
 #pragma unroll
-      for (int c = 2; c < 32; c += 2) {
-        mx0 = max3f(mx0, s[c], s[c + 1]);
-        mx1 = max3f(mx1, s[32 + c], s[33 + c]);
-      }
-      const float m_tile = fmaxf(mx0, mx1) * sl2;
+      for (int k = 0; k < 21; ++k) a[k] = max3f(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
+      a[21] = s[63];
+#pragma unroll
+      for (int k = 0; k < 7; ++k) c8[k] = max3f(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
+      c8[7] = a[21];
+      const float m_tile =
+          max3f(max3f(c8[0], c8[1], c8[2]), max3f(c8[3], c8[4], c8[5]), fmaxf(c8[6], c8[7])) * sl2;
       float alpha = 1.f;
       if (m_tile > m_run + 8.f) {  // also true when m_run = -inf and the tile has a visible key
         alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
