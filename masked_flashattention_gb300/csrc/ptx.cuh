@@ -370,26 +370,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 // pack two floats into a bf16x2 word (round to nearest even); `lo` goes to the low half
-// 2^x for two values on the FMA pipe instead of the special-function unit, so that part of a
-// tile's exponentials can run beside the ex2.approx ones.  Cody-Waite style range reduction:
-// n = rint(x) by the round-to-nearest add of 1.5 * 2^23 (n ends up in the low mantissa bits),
-// f = x - n in [-0.5, 0.5]; 2^f by a degree-3 polynomial fitted here for minimum relative error
-// on that interval (below 8e-5, well under the bf16 rounding of P); 2^n by adding n to the
-// exponent field.  x is clamped to >= -126, so arguments below give ~1.2e-38 rather than 0:
-// callers that need exact zeros (masked scores) select them separately.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -126.f);
-  x.y = fmaxf(x.y, -126.f);
-  const float2 j = add2(x, make_float2(12582912.f, 12582912.f));
-  const float2 n = add2(j, make_float2(-12582912.f, -12582912.f));
-  const float2 f = fma2(n, make_float2(-1.f, -1.f), x);
-  float2 q = fma2(make_float2(0.0551716648f, 0.0551716648f), f,
-                  make_float2(0.2426111251f, 0.2426111251f));
-  q = fma2(q, f, make_float2(0.6932609677f, 0.6932609677f));
-  q = fma2(q, f, make_float2(0.9999280572f, 0.9999280572f));
-  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(j.x) << 23)),
-                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(j.y) << 23)));
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
