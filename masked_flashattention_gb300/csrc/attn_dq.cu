@@ -91,8 +91,11 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int item = p.sched[blockIdx.x / p.H];
-  const int h = blockIdx.x % p.H;
+  // heads are the slowest index of the grid: the CTAs resident at one time work on tiles of
+  // the same (sample, head), so the K/V (or Q/dO) tiles they share stay in L2
+  const int n_items = p.B * p.NT;
+  const int item = p.sched[blockIdx.x % n_items];
+  const int h = blockIdx.x / n_items;
   const int b = item >> 16;
   const int qt = item & 0xFFFF;
   const int bh = b * p.H + h;
