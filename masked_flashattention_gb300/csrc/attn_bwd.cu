@@ -173,11 +173,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // heads are the slowest index of the grid: the CTAs resident at one time work on tiles of
-  // the same (sample, head), so the K/V (or Q/dO) tiles they share stay in L2
-  const int n_items = p.B * p.NT;
-  const int item = p.sched[blockIdx.x % n_items];
-  const int h = blockIdx.x / n_items;
+  int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
+  cta_work(blockIdx.x, p.B * p.NT, p.H, item_idx, h);
+  const int item = p.sched[item_idx];
   const int b = item >> 16;
   const int kt = item & 0xFFFF;
   const int bh = b * p.H + h;

@@ -23,6 +23,25 @@ __device__ __forceinline__ bool tile_is_full(const uint32_t* row, int c) {
   return ((row[c >> 4] >> (2 * (c & 15))) & 3u) == 2u;
 }
 
+// Work item (index into the longest-first schedule) and head of CTA q of a grid of n_items * H
+// CTAs.  Items are taken in chunks of kChunkItems in schedule order, and within a chunk the heads
+// follow one another: the CTAs resident at one time then work on one or two (sample, head)s,
+// whose K/V (or Q/dO) tiles stay in L2, while the longest rows of every head still start first.
+constexpr int kChunkItems = 128;
+__device__ __forceinline__ void cta_work(int q, int n_items, int H, int& item_idx, int& h) {
+  const int full = n_items / kChunkItems;
+  const int span = kChunkItems * H;
+  if (q < full * span) {
+    const int k = q / span, r = q - k * span;
+    h = r / kChunkItems;
+    item_idx = k * kChunkItems + (r - h * kChunkItems);
+  } else {  // the last, partial chunk of rem items (rem > 0 here)
+    const int r = q - full * span, rem = n_items - full * kChunkItems;
+    h = r / rem;
+    item_idx = full * kChunkItems + (r - h * rem);
+  }
+}
+
 // Forms of the partial-tile visibility check (the ablation of CompileMask section 4.4):
 //   kCheckUnsigned    visible iff (u32)(x - s) < (u32)(e - s) for some visible interval [s, e):
 //                     one subtraction and one unsigned comparison per interval (the default);
