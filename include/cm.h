@@ -29,7 +29,8 @@
  *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous, layout [B][H][S][d].  The LSE is
  *     fp32 [B][H][S] in natural log.  Row i of a descriptor is a query row (forward) or a key
  *     column (backward).
- *   - Supported shapes: d in {64, 128}; S a positive multiple of 128; tile = 128.
+ *   - Supported shapes: d in {64, 128}; S a positive multiple of 128; tile = 128; at most 2^24
+ *     heads (CM_ERR_UNSUPPORTED above that).
  */
 #ifndef CM_H_
 #define CM_H_

@@ -11,6 +11,10 @@
 namespace {
 
 constexpr int kTile = 128;
+// The kernels map CTAs to (work item, head) in chunks of 128 work items with every head inside a
+// chunk, in 32-bit arithmetic: 128 * H must stay below 2^31.  (No call that fits in device memory
+// comes near: 2^24 heads of one 128-row tile are 0.5 TB per tensor at d = 128.)
+constexpr int kMaxHeads = 1 << 24;
 constexpr int kMaxS = 131072;
 
 // which descriptor kernels cm_build_descriptor runs (cm_set_preprocess_mode)
@@ -123,6 +127,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   rc = check_desc(desc, B, S);
   if (rc != CM_OK) return rc;
   if (H < 1 || static_cast<long long>(B) * H * (S / kTile) > 0x7FFFFFFFLL) return CM_ERR_INVALID_ARG;
+  if (H > kMaxHeads) return CM_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return CM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -166,6 +171,7 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   rc = check_desc(desc, B, S);
   if (rc != CM_OK) return rc;
   if (H < 1 || static_cast<long long>(B) * H * (S / kTile) > 0x7FFFFFFFLL) return CM_ERR_INVALID_ARG;
+  if (H > kMaxHeads) return CM_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
     return CM_ERR_INVALID_ARG;
