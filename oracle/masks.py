@@ -18,7 +18,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
     bits 2*(t % 16) of word t // 16;
   * slot order within a row is the order in which the rule names the intervals;
   * workload 5: prefix rows are causal over the prefix; the "previous document" of the first
-    document is empty, and the prefix is not a document.
+    document is empty, and the prefix is not a document.  The other reading of the prefix rows
+    (each sees the whole prefix [0, b)) is available with prefix_bidirectional=True in
+    dense_mask, the Interval Tables and tile_states; the library's specs follow the causal one.
 
 Segment conventions: seg_row[k] is the first position of segment k, seg_row[nseg] = S.
   workload 3: segment 0 is the prompt (P = seg_row[1]), segments 1..4 the responses;
@@ -49,8 +51,12 @@ def segment_index(seg_row: np.ndarray, nseg: int, pos: np.ndarray) -> np.ndarray
 # dense masks: the visibility rule of each workload, written directly as a predicate on (i, j)
 # ------------------------------------------------------------------------------------------------
 def dense_mask(wid: int, seg_row: np.ndarray, nseg: int, S: int,
-               rows: np.ndarray | None = None, cols: np.ndarray | None = None) -> np.ndarray:
-    """bool [len(rows), len(cols)]: True where query row i may attend to key column j."""
+               rows: np.ndarray | None = None, cols: np.ndarray | None = None,
+               prefix_bidirectional: bool = False) -> np.ndarray:
+    """bool [len(rows), len(cols)]: True where query row i may attend to key column j.
+
+    prefix_bidirectional (workload 5 only): prefix rows see the whole prefix instead of being
+    causal over it (the other reading of the pages' three-interval workload)."""
     i = (np.arange(S) if rows is None else np.asarray(rows)).astype(np.int64)[:, None]
     j = (np.arange(S) if cols is None else np.asarray(cols)).astype(np.int64)[None, :]
     seg = np.asarray(seg_row, dtype=np.int64)
@@ -72,7 +78,7 @@ def dense_mask(wid: int, seg_row: np.ndarray, nseg: int, S: int,
         return history | candidate
     if wid == 5:   # prefix causal; document row sees [0, b), head of previous doc, own doc causal
         b = seg[1]
-        prefix = (i < b) & (j <= i)
+        prefix = (i < b) & ((j < b) if prefix_bidirectional else (j <= i))
         prev = np.maximum(ki - 1, 0)
         prev_start = seg[prev]
         prev_len = seg[np.minimum(prev + 1, nseg)] - prev_start
@@ -101,8 +107,10 @@ def _slot(lo: int, hi: int, S: int) -> tuple[int, int]:
     return (lo, hi) if hi > lo else (0, 0)
 
 
-def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.ndarray:
-    """int32 [NI_f, S, 2]: the visible key intervals of every query row."""
+def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int,
+                       prefix_bidirectional: bool = False) -> np.ndarray:
+    """int32 [NI_f, S, 2]: the visible key intervals of every query row (prefix_bidirectional:
+    see dense_mask)."""
     ni, _ = num_intervals(wid)
     out = np.zeros((ni, S, 2), dtype=np.int32)
     seg = [int(x) for x in seg_row[: nseg + 1]]
@@ -118,7 +126,7 @@ def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.n
             slots = [(0, i + 1)] if k == 0 else [(0, seg[1]), (i, i + 1)]
         elif wid == 5:
             if k == 0:
-                slots = [(0, i + 1)]
+                slots = [(0, seg[1])] if prefix_bidirectional else [(0, i + 1)]
             elif k == 1:
                 slots = [(0, seg[1]), (0, 0), (seg[k], i + 1)]
             else:
@@ -133,8 +141,10 @@ def interval_table_fwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.n
     return out
 
 
-def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.ndarray:
-    """int32 [NI_b, S, 2]: for every key column j, the query rows that see it."""
+def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int,
+                       prefix_bidirectional: bool = False) -> np.ndarray:
+    """int32 [NI_b, S, 2]: for every key column j, the query rows that see it (prefix_bidirectional:
+    see dense_mask)."""
     _, ni = num_intervals(wid)
     out = np.zeros((ni, S, 2), dtype=np.int32)
     seg = [int(x) for x in seg_row[: nseg + 1]]
@@ -150,8 +160,8 @@ def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int) -> np.n
         elif wid == 4:
             slots = [(j, S)] if k == 0 else [(j, j + 1)]
         elif wid == 5:
-            if k == 0:
-                slots = [(j, S)]
+            if k == 0:  # a prefix key: the prefix rows from j on (or all of them), every document row
+                slots = [(0, S)] if prefix_bidirectional else [(j, S)]
             else:
                 nxt = (0, 0)
                 if j < seg[k] + PREV_DOC_HEAD and k + 1 < nseg:
@@ -194,19 +204,22 @@ def tile_states_of(mask: np.ndarray, tile_r: int, tile_c: int) -> np.ndarray:
 
 
 def tile_states(wid: int, seg_row: np.ndarray, nseg: int, S: int, tile: int = 128,
-                backward: bool = False) -> np.ndarray:
+                backward: bool = False, prefix_bidirectional: bool = False) -> np.ndarray:
     """Tile states of the forward mask, or of its transpose for the backward descriptor.
 
     Built one tile-row at a time from the dense predicate so that 32K masks fit in memory.
+    prefix_bidirectional: see dense_mask.
     """
     nt = S // tile
     out = np.zeros((nt, nt), dtype=np.uint8)
     for t in range(nt):
         span = np.arange(t * tile, (t + 1) * tile)
         if backward:  # rows of the transposed mask = key columns of the forward mask
-            block = dense_mask(wid, seg_row, nseg, S, rows=None, cols=span).T
+            block = dense_mask(wid, seg_row, nseg, S, rows=None, cols=span,
+                               prefix_bidirectional=prefix_bidirectional).T
         else:
-            block = dense_mask(wid, seg_row, nseg, S, rows=span, cols=None)
+            block = dense_mask(wid, seg_row, nseg, S, rows=span, cols=None,
+                               prefix_bidirectional=prefix_bidirectional)
         out[t] = tile_states_of(block, tile, tile)[0]
     return out
 

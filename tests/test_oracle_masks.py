@@ -219,3 +219,34 @@ def test_varlen_users_are_independent():
         one = np.array([0, h_end - a, e - a, e - a], dtype=np.int64)
         np.testing.assert_array_equal(block, M.dense_mask(4, one, 2, e - a))
         assert not dense[a:e, :a].any() and not dense[a:e, e:].any()
+
+
+# ------------------------------------------------------------------------------------------------
+# the other reading of workload 5's prefix rows (behind an oracle flag)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(3))
+def test_w5_bidirectional_prefix_reading(seed):
+    """With prefix_bidirectional the prefix rows see all of [0, b): exactly the b(b-1)/2 pairs of
+    the prefix block above its diagonal are added, nothing else changes, and the flagged Interval
+    Tables and bitmaps describe the flagged mask."""
+    S = 1024
+    seg, nseg = W.segments(5, 2, S, seed=100 + seed)
+    for b in range(2):
+        sb, nb = seg[b], int(nseg[b])
+        P = int(sb[1])
+        base = M.dense_mask(5, sb, nb, S)
+        alt = M.dense_mask(5, sb, nb, S, prefix_bidirectional=True)
+        added = alt & ~base
+        ii, jj = np.nonzero(added)
+        assert (ii < P).all() and (jj < P).all() and (jj > ii).all()
+        assert int(added.sum()) == P * (P - 1) // 2
+        assert not (base & ~alt).any()
+        assert int(alt.sum()) == closed_form_visible(5, sb, nb, S) + P * (P - 1) // 2
+        fwd = M.interval_table_fwd(5, sb, nb, S, prefix_bidirectional=True)
+        bwd = M.interval_table_bwd(5, sb, nb, S, prefix_bidirectional=True)
+        assert np.array_equal(M.intervals_to_mask(fwd, S), alt)
+        assert np.array_equal(M.intervals_to_mask(bwd, S), alt.T)
+        states = M.tile_states(5, sb, nb, S, prefix_bidirectional=True)
+        assert np.array_equal(states, M.tile_states_of(alt, 128, 128))
+        bstates = M.tile_states(5, sb, nb, S, backward=True, prefix_bidirectional=True)
+        assert np.array_equal(bstates, states.T)
