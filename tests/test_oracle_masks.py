@@ -250,3 +250,16 @@ def test_w5_bidirectional_prefix_reading(seed):
         assert np.array_equal(states, M.tile_states_of(alt, 128, 128))
         bstates = M.tile_states(5, sb, nb, S, backward=True, prefix_bidirectional=True)
         assert np.array_equal(bstates, states.T)
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
+def test_interval_union_equals_dense_many_seeds(wid):
+    """The slot form against the dense predicate (and its transpose) on 200 seeded segmentations
+    per workload at S = 256 and 384, so short and uneven segments are covered."""
+    for seed in range(100):
+        for S in (256, 384):
+            seg, nseg = W.segments(wid, 1, S, seed=10_000 + 131 * seed + wid)
+            sb, nb = seg[0], int(nseg[0])
+            dense = M.dense_mask(wid, sb, nb, S)
+            assert np.array_equal(M.intervals_to_mask(M.interval_table_fwd(wid, sb, nb, S), S), dense)
+            assert np.array_equal(M.intervals_to_mask(M.interval_table_bwd(wid, sb, nb, S), S), dense.T)
