@@ -142,6 +142,12 @@ def test_attention_argument_validation_happens_on_the_host(B):
     assert L.cm_attn_fwd(ctypes.byref(d), odd, p, p, p, p, 1, 2, 256, 64, 0.1, None) == B.CM_ERR_INVALID_ARG
     # non-finite scale
     assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 1, 2, 256, 64, float("nan"), None) == B.CM_ERR_INVALID_ARG
+    # head count: at least 1, at most 2^24 (the kernels' grid mapping)
+    assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 1, 0, 256, 64, 0.1, None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_fwd(ctypes.byref(d), p, p, p, p, p, 1, (1 << 24) + 1, 256, 64, 0.1,
+                         None) == B.CM_ERR_UNSUPPORTED
+    assert L.cm_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, 1 << 40, 1, (1 << 24) + 1,
+                         256, 64, 0.1, None) == B.CM_ERR_UNSUPPORTED
     # backward: workspace too small
     need = B.cm_attn_bwd_workspace_size(1, 2, 256, 64)
     assert need == 2 * (1 * 2 * 256 * 4)  # D and LSE * log2(e), fp32 per row
