@@ -2,7 +2,9 @@
 
 One step = the whole hot path on one batch of synthetic input already resident in HBM:
 Execution Descriptor build (preprocess kernels, forward and backward halves), attention forward,
-attention backward (D prologue, main kernel, dQ conversion).
+attention backward (D prologue, dK/dV kernel, dQ kernel), each stage bracketed by CUDA events.
+The headline workload is the shared-prompt RM mask at 32K; the three-interval packed 32K
+workload is timed in the same run and reported beside it.
 
 Metric: effective TFLOP/s over visible pairs only: sum_b 14 * d * V_b * H / step time, where
 V_b is the number of visible (query, key) pairs of sample b (4 d V for the forward's two
@@ -206,6 +208,17 @@ def visible_pairs(desc, B: int, S: int):
     return [int(x) for x in total.sum(dim=1).tolist()]
 
 
+def nonempty_tiles(desc):
+    """Non-empty 128 x 128 tiles of the forward bitmap, summed over samples (the tiles the
+    kernels execute)."""
+    import numpy as np
+    words = desc.bitmap_fwd()
+    nt = desc.NT
+    codes = np.stack([(words >> (2 * t)) & 3 for t in range(16)], axis=-1)
+    codes = codes.reshape(words.shape[0], words.shape[1], -1)[:, :, :nt]
+    return int((codes != 0).sum())
+
+
 def preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev, target_mb=64.0, reps=20):
     """Descriptor build replicated over a batch large enough that the descriptor (>= 64 MB)
     exceeds what launch latency hides: achieved HBM GB/s of the preprocess kernels."""
@@ -232,6 +245,195 @@ def preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev, target_mb=64.0, reps
     return {"B": Bs, "MB": nbytes / 2**20, "us": us, "gbs": nbytes / (us * 1e-6) / 1e9}
 
 
+STAGES = ("build", "fwd", "prologue", "dkdv", "dq")
+
+
+class Problem:
+    """One workload resident on the device: specs, metadata, descriptor, inputs, outputs."""
+
+    def __init__(self, Bd, w, dev, rank):
+        import torch
+        self.Bd, self.w, self.dev = Bd, w, dev
+        from masked_flashattention_gb300 import specs
+        from masked_flashattention_gb300 import workloads as W
+        Bn, H, S, d = w.B, w.H, w.S, w.d
+        self.scale = 1.0 / math.sqrt(d)
+        self.seg_np, self.nseg_np = W.segments(w.id, Bn, S)
+        self.fwd = Bd.cm_compile_spec(specs.FWD[w.id])
+        self.bwd = Bd.cm_compile_spec(specs.BWD[w.id])
+        self.desc = Bd.Descriptor(self.fwd, self.bwd, Bn, S, device=dev)
+        self.seg = torch.from_numpy(self.seg_np).to(dev)
+        self.nseg = torch.from_numpy(self.nseg_np).to(dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(2000 + w.id + 97 * rank)
+        self.shape = (Bn, H, S, d)
+        self.q, self.k, self.v, self.do = (
+            torch.randn(self.shape, generator=g, device=dev, dtype=torch.float32)
+            .to(torch.bfloat16) for _ in range(4))
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(Bn, H, S, dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws = torch.empty(Bd.cm_attn_bwd_workspace_size(Bn, H, S, d), dtype=torch.uint8,
+                              device=dev)
+
+    def step(self, stream, ev=None, io=None):
+        """The whole hot path once: descriptor build, forward, backward (three stages).  `ev`
+        (6 CUDA events) brackets each stage; `io` swaps in another set of inputs and outputs."""
+        Bd, x = self.Bd, io or self
+        if ev is not None:
+            ev[0].record(stream)
+        Bd.cm_build_descriptor(self.fwd, self.bwd, x.seg, x.nseg, self.desc, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        Bd.cm_attn_fwd(self.desc, x.q, x.k, x.v, x.o, x.lse, self.scale, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        Bd.cm_attn_bwd_prologue(x.o, x.lse, x.do, self.ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        Bd.cm_attn_bwd_dkdv(self.desc, x.q, x.k, x.v, x.do, x.dk, x.dv, self.ws, self.scale,
+                            stream)
+        if ev is not None:
+            ev[4].record(stream)
+        Bd.cm_attn_bwd_dq(self.desc, x.q, x.k, x.v, x.do, x.dq, self.ws, self.scale, stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    def check_status(self):
+        st = self.Bd.cm_get_status(self.desc)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {self.Bd.cm_error_string(st)}")
+
+
+def time_steps(prob, stream, steps):
+    """Per-stage mean milliseconds over `steps` steps (CUDA events on the launching stream)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for s in range(steps):
+        prob.step(stream, evs[s])
+    torch.cuda.synchronize(prob.dev)
+    return {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+            for i, name in enumerate(STAGES)}
+
+
+def workload_report(prob, ms, pairs, tiles, peak_burst):
+    """Per-kernel figures of one workload.  Method FLOPs per visible pair: forward 4 d (QK^T, PV),
+    backward 10 d (S recompute, dP, dV, dK, dQ); the dK/dV kernel's share is 8 d, the dQ kernel's
+    2 d.  Executed FLOPs count every element of the non-empty 128 x 128 tiles: the dK/dV kernel
+    runs 4 MMAs per tile (8 d per element), the dQ kernel 3 (S, dP and dQ: 6 d)."""
+    w = prob.w
+    d, H = w.d, w.H
+    V = sum(pairs) * H
+    E = tiles * 128 * 128 * H
+    kern = {}
+    for name, method, executed in (("fwd", 4, 4), ("dkdv", 8, 8), ("dq", 2, 6)):
+        t = ms[name] / 1e3
+        eff = method * d * V / t / 1e12
+        exe = executed * d * E / t / 1e12
+        kern[name] = {"ms": ms[name], "method_tflops": eff, "executed_tflops": exe,
+                      "executed_frac_of_burst": exe / peak_burst}
+    kern["prologue"] = {"ms": ms["prologue"]}
+    kern["build"] = {"ms": ms["build"]}
+    bwd_ms = ms["prologue"] + ms["dkdv"] + ms["dq"]
+    step_ms = ms["build"] + ms["fwd"] + bwd_ms
+    eff_step = 14 * d * V / (step_ms / 1e3) / 1e12
+    return {
+        "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "d": d,
+        "visible_pairs_per_head": pairs, "nonempty_tiles": tiles,
+        "tile_efficiency": sum(pairs) / (tiles * 128 * 128),
+        "step_ms": step_ms, "fwd_ms": ms["fwd"], "bwd_ms": bwd_ms,
+        "tflops": eff_step,
+        "fwd_tflops": 4 * d * V / (ms["fwd"] / 1e3) / 1e12,
+        "bwd_tflops": 10 * d * V / (bwd_ms / 1e3) / 1e12,
+        "frac_of_bf16_burst": eff_step / peak_burst,
+        "kernels": kern,
+    }
+
+
+def e2e_pipelined(prob, steps, world):
+    """End to end through the public API with pinned host buffers: every step copies its inputs
+    (Q, K, V, dO and the segment metadata) host -> device, runs the whole hot path and copies its
+    results (O, LSE, dQ, dK, dV) device -> host.  Copies run on their own streams, double
+    buffered: the inputs of step n + 1 go up and the outputs of step n - 1 come down while step n
+    computes.  The timed region spans all copies of all steps."""
+    import torch
+    dev, Bd = prob.dev, prob.Bd
+    Bn, H, S, d = prob.shape
+
+    class IO:
+        pass
+
+    host_in = [t.cpu().pin_memory() for t in (prob.q, prob.k, prob.v, prob.do, prob.seg, prob.nseg)]
+    host_out = [torch.empty(prob.shape, dtype=torch.bfloat16).pin_memory(),
+                torch.empty(Bn, H, S, dtype=torch.float32).pin_memory()] + \
+               [torch.empty(prob.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    sets = []
+    for k in range(2):
+        x = IO()
+        if k == 0:
+            x.q, x.k, x.v, x.do, x.seg, x.nseg = prob.q, prob.k, prob.v, prob.do, prob.seg, prob.nseg
+            x.o, x.lse, x.dq, x.dk, x.dv = prob.o, prob.lse, prob.dq, prob.dk, prob.dv
+        else:
+            x.q, x.k, x.v, x.do, x.seg, x.nseg = (torch.empty_like(t) for t in
+                                                   (prob.q, prob.k, prob.v, prob.do, prob.seg,
+                                                    prob.nseg))
+            x.o, x.lse, x.dq, x.dk, x.dv = (torch.empty_like(t) for t in
+                                             (prob.o, prob.lse, prob.dq, prob.dk, prob.dv))
+        sets.append(x)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    compute = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n_steps):
+        in_done = [torch.cuda.Event() for _ in range(n_steps)]
+        comp_done = [torch.cuda.Event() for _ in range(n_steps)]
+        out_done = [torch.cuda.Event() for _ in range(n_steps)]
+
+        def upload(s):
+            x = sets[s % 2]
+            if s >= 2:  # the compute of step s - 2 has finished reading this set's inputs
+                s_in.wait_event(comp_done[s - 2])
+            with torch.cuda.stream(s_in):
+                for dst, src in zip((x.q, x.k, x.v, x.do, x.seg, x.nseg), host_in):
+                    dst.copy_(src, non_blocking=True)
+            in_done[s].record(s_in)
+
+        upload(0)
+        for s in range(n_steps):
+            if s + 1 < n_steps:
+                upload(s + 1)
+            x = sets[s % 2]
+            compute.wait_event(in_done[s])
+            if s >= 2:  # the outputs of step s - 2 (same set) have reached the host
+                compute.wait_event(out_done[s - 2])
+            prob.step(compute, io=x)
+            comp_done[s].record(compute)
+            s_out.wait_event(comp_done[s])
+            with torch.cuda.stream(s_out):
+                for dst, src in zip(host_out, (x.o, x.lse, x.dq, x.dk, x.dv)):
+                    dst.copy_(src, non_blocking=True)
+            out_done[s].record(s_out)
+        return out_done[-1]
+
+    run(2)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(compute)
+    last = run(steps)
+    compute.wait_event(last)
+    b.record(compute)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    prob.check_status()
+    return a.elapsed_time(b) / 1e3, wall, h2d, d2h
+
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -243,58 +445,36 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
 
     from masked_flashattention_gb300 import binding as Bd
-    from masked_flashattention_gb300 import specs
     from masked_flashattention_gb300 import workloads as W
 
     Bd.lib()
-    w = W.WORKLOADS[args.config]
-    if args.heads:
-        w = W.Workload(w.id, f"{w.name}@H{args.heads}", w.B, args.heads, w.S, w.d)
-    Bn, H, S, d = w.B, w.H, w.S, w.d
-    scale = 1.0 / math.sqrt(d)
-    seg_np, nseg_np = W.segments(w.id, Bn, S)
-    fwd, bwd = Bd.cm_compile_spec(specs.FWD[w.id]), Bd.cm_compile_spec(specs.BWD[w.id])
-    desc = Bd.Descriptor(fwd, bwd, Bn, S, device=dev)
-    seg = torch.from_numpy(seg_np).to(dev)
-    nseg = torch.from_numpy(nseg_np).to(dev)
+    peaks, peak_src = load_peaks()
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
 
-    g = torch.Generator(device=dev)
-    g.manual_seed(2000 + w.id + 97 * rank)
-    shape = (Bn, H, S, d)
-    q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
-                   .to(torch.bfloat16) for _ in range(4))
-    o = torch.empty_like(q)
-    lse = torch.empty(Bn, H, S, dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(Bd.cm_attn_bwd_workspace_size(Bn, H, S, d), dtype=torch.uint8, device=dev)
+    def workload(wid):
+        w = W.WORKLOADS[wid]
+        if args.heads:
+            w = W.Workload(w.id, f"{w.name}@H{args.heads}", w.B, args.heads, w.S, w.d)
+        return w
+
+    also = [int(x) for x in args.also.split(",") if x.strip()] if args.also is not None else \
+        ([5] if args.config == 3 else [3] if args.config == 5 else [])
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        Bd.cm_build_descriptor(fwd, bwd, seg, nseg, desc, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        Bd.cm_attn_fwd(desc, q, k, v, o, lse, scale, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        Bd.cm_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws, scale, stream)
-        if ev is not None:
-            ev[3].record(stream)
-
-    step()
+    prob = Problem(Bd, workload(args.config), dev, rank)
+    w = prob.w
+    prob.step(stream)
     torch.cuda.synchronize(dev)
-    st = Bd.cm_get_status(desc)
-    if st != 0:
-        raise RuntimeError(f"device status {st}: {Bd.cm_error_string(st)}")
-    pairs = visible_pairs(desc, Bn, S)
-    flops = FLOPS_PER_PAIR_PER_D * d * H * sum(pairs)
-    fwd_flops = 4 * d * H * sum(pairs)
-    bwd_flops = 10 * d * H * sum(pairs)
+    prob.check_status()
+    pairs = visible_pairs(prob.desc, w.B, w.S)
+    tiles = nonempty_tiles(prob.desc)
+    flops = FLOPS_PER_PAIR_PER_D * w.d * w.H * sum(pairs)
 
     for _ in range(args.warmup):
-        step()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        prob.step(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
@@ -304,95 +484,75 @@ def run_gpu(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        prob.step(stream, evs[s])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     elapsed = t_start.elapsed_time(t_end) / 1e3
-    build_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    st = Bd.cm_get_status(desc)
-    if st != 0:
-        raise RuntimeError(f"device status {st}: {Bd.cm_error_string(st)}")
-
+    ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+          for i, name in enumerate(STAGES)}
+    prob.check_status()
     t_max, units = aggregate(elapsed, flops * args.steps, world)
     value = units / t_max / 1e12
+    reports = {w.name: workload_report(prob, ms, pairs, tiles, peak_burst)}
 
-    # ---- optional: the partial-tile check forms of the paper's section 4.4 ablation ----
+    # ---- the other 32K workload(s), same timing rules, reported beside the headline ----
+    for wid in also:
+        other = Problem(Bd, workload(wid), dev, rank)
+        other.step(stream)
+        torch.cuda.synchronize(dev)
+        other.check_status()
+        opairs = visible_pairs(other.desc, other.w.B, other.w.S)
+        otiles = nonempty_tiles(other.desc)
+        for _ in range(args.warmup):
+            other.step(stream)
+        oms = time_steps(other, stream, args.steps)
+        other.check_status()
+        reports[other.w.name] = workload_report(other, oms, opairs, otiles, peak_burst)
+        del other
+        torch.cuda.empty_cache()
+
+    # ---- optional: the forms of the partial-tile check (the paper's section 4.4 ablation) ----
     ablation = None
     if args.ablation:
         ablation = {}
-        names = {Bd.CM_CHECK_UNSIGNED: "unsigned_visible", Bd.CM_CHECK_TWO_COMPARE: "two_compare_visible",
+        names = {Bd.CM_CHECK_UNSIGNED: "unsigned_visible",
+                 Bd.CM_CHECK_TWO_COMPARE: "two_compare_visible",
                  Bd.CM_CHECK_MASKED: "masked_intervals"}
-        for mode in (Bd.CM_CHECK_UNSIGNED, Bd.CM_CHECK_TWO_COMPARE, Bd.CM_CHECK_MASKED):
+        for mode, name in names.items():
             Bd.cm_set_interval_check(mode)
             for _ in range(max(3, args.warmup)):
-                step()
-            aevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-            torch.cuda.synchronize(dev)
-            for s_ in range(args.steps):
-                step(aevs[s_])
-            torch.cuda.synchronize(dev)
-            f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in aevs)
-            b_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in aevs)
-            ablation[names[mode]] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_bwd_ms": f_ms + b_ms}
+                prob.step(stream)
+            ams = time_steps(prob, stream, args.steps)
+            f_ms, b_ms = ams["fwd"], ams["prologue"] + ams["dkdv"] + ams["dq"]
+            ablation[name] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_bwd_ms": f_ms + b_ms}
         Bd.cm_set_interval_check(Bd.CM_CHECK_UNSIGNED)
-        st = Bd.cm_get_status(desc)
-        if st != 0:
-            raise RuntimeError(f"device status {st}: {Bd.cm_error_string(st)}")
+        prob.check_status()
         base = ablation["unsigned_visible"]["fwd_bwd_ms"]
         for v_ in ablation.values():
             v_["vs_unsigned"] = v_["fwd_bwd_ms"] / base
 
     # ---- end to end through the public API with pinned host buffers ----
-    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
-    hseg, hnseg = seg.cpu().pin_memory(), nseg.cpu().pin_memory()
-    ho, hdq, hdk, hdv = (torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
-    hlse = torch.empty(Bn, H, S, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hseg, hnseg))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
-
-    def e2e_step():
-        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo), (seg, hseg), (nseg, hnseg)):
-            dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-            dst.copy_(src, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_steps = max(1, min(args.steps, 5))
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b_.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_t, e2e_units = aggregate(a.elapsed_time(b_) / 1e3, flops * e2e_steps, world)
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_t, e2e_wall, h2d, d2h = e2e_pipelined(prob, e2e_steps, world)
+    e2e_t, e2e_units = aggregate(e2e_t, flops * e2e_steps, world)
     e2e_value = e2e_units / e2e_t / 1e12
 
-    # ---- roofline of the dominant kernel (the backward pass) ----
-    peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
-    fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
-    meta_bytes = seg.numel() * 4 + nseg.numel() * 4
-    prep_bytes = meta_bytes + desc.nbytes()
-    sweep = preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev)
-    if sweep is not None:
-        sweep["pct_hbm"] = 100.0 * sweep["gbs"] / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # ---- roofline of the dominant kernel: the dK/dV kernel of the headline workload ----
+    rep = reports[w.name]
+    dk = rep["kernels"]["dkdv"]
+    prep_bytes = prob.seg.numel() * 4 + prob.nseg.numel() * 4 + prob.desc.nbytes()
+    sweep = preprocess_sweep(Bd, prob.fwd, prob.bwd, prob.seg_np, prob.nseg_np, w.S, dev)
+    sweep["pct_hbm"] = 100.0 * sweep["gbs"] / hbm
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
+    if os.path.exists(tp) and not args.heads:
         import hashlib
         with open(tp) as f:
-            rec = json.load(f).get(f"attn_bwd@{w.name}")
+            rec = json.load(f).get(f"attn_dkdv@{w.name}")
+
         def sha1(name):
             with open(os.path.join(ROOT, "masked_flashattention_gb300", "csrc", name), "rb") as f:
                 return hashlib.sha1(f.read()).hexdigest()
@@ -406,23 +566,30 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "B": Bn, "H": H, "S": S, "d": d,
-                       "visible_pairs_per_head": pairs, "parallelism": f"replicas{world}",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "d": w.d,
+                       "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
-                             f"{q.numel() * 2 / 2**20:.0f} MiB); no flush",
-                       "pct_bf16_peak": 100.0 * value / peak,
-                       "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "build_ms": build_ms,
-                       "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
-                       "preprocess_gbs": prep_bytes / (build_ms / 1e3) / 1e9,
+                             f"{prob.q.numel() * 2 / 2**20:.0f} MiB); no flush",
+                       "pct_bf16_peak": 100.0 * value / peak_burst,
+                       "pct_bf16_peak_sustained": 100.0 * value / peak_sust,
+                       "peak_source": f"{peak_src} bf16_tflops (burst) {peak_burst}; "
+                                      f"sustained {peak_sust}",
+                       "preprocess_gbs": prep_bytes / (ms["build"] / 1e3) / 1e9,
                        "preprocess_sweep": sweep,
-                       "peak_source": f"{peak_src} bf16_tflops_sustained"},
-            "roofline": {"bound": "tensor", "kernel": "attention backward (prologue + dK/dV kernel + dQ kernel)",
-                         "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": bwd_tf / peak, "traffic": traffic},
+                       "workloads": reports},
+            "roofline": {"bound": "tensor",
+                         "kernel": "attn_bwd_kernel (dK, dV along key tiles)",
+                         "achieved": dk["method_tflops"], "peak": peak_burst, "unit": "TFLOP/s",
+                         "frac": dk["method_tflops"] / peak_burst, "traffic": traffic,
+                         "per_launch": "8 d FLOP per visible pair x H x visible pairs",
+                         "executed_tflops": dk["executed_tflops"],
+                         "peak_note": f"{peak_src} burst bf16 (kernel timed in ms-long launches "
+                                      "at full clock)"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            # per step: descriptor (2 generated kernels + schedule), forward, backward (prologue,
-            # dK/dV, dQ)
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "wall_s": e2e_wall,
+                    "how": "copies on two copy streams, double-buffered, overlapping compute"},
+            # per step: descriptor (2 generated kernels + schedule), forward, prologue, dK/dV, dQ
             "gpu_launches": 7 * args.steps,
             "clocks": clk,
         }
@@ -430,7 +597,7 @@ def run_gpu(args):
             line["ablation"] = ablation
         if world == 1 and not args.no_cpu_baseline:
             dt, pr, cores, sdesc = oracle_sample(args.config, args.ref_rows or 8192)
-            line["cpu_baseline"] = {"value": FLOPS_PER_PAIR_PER_D * d * pr / dt / 1e12,
+            line["cpu_baseline"] = {"value": FLOPS_PER_PAIR_PER_D * w.d * pr / dt / 1e12,
                                     "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": sdesc}
         print(json.dumps(line))
@@ -451,6 +618,9 @@ def main():
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--also", default=None,
+                    help="other workloads timed in the same run and reported under "
+                         "config.workloads (default: the other 32K workload, 5 with 3 and 3 with 5)")
     ap.add_argument("--ablation", action="store_true",
                     help="also time the three partial-tile check forms (section 4.4); use with --config 4")
     args = ap.parse_args()

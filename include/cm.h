@@ -51,7 +51,10 @@ enum {
   CM_ERR_UNSUPPORTED = -3,  /* valid request outside the supported shapes (d, S, tile, limits) */
   CM_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
   CM_ERR_TIMEOUT = -5,      /* device status: a bounded wait inside a kernel expired */
-  CM_ERR_DEVICE_CHECK = -6  /* device status: segment metadata failed validation */
+  CM_ERR_DEVICE_CHECK = -6, /* device status: segment metadata failed validation */
+  CM_ERR_DESC_MISMATCH = -7 /* device status: the backward descriptor's Tile-State Bitmap is not
+                               the transpose of the forward one (the two MaskSpecs do not
+                               describe the same mask) */
 };
 
 /* Opaque compiled MaskSpec (host memory, owned by the caller after cm_compile_spec). */
@@ -181,15 +184,50 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
 CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes);
 
 /* Backward: dq, dk, dv (device bf16 [B][H][S][d]) of sum(o * dO) given the forward's o and lse.
- * Three kernels: a prologue (D, LSE * log2(e) into the workspace), dK and dV along key tiles with
- * the backward half of the descriptor (itab_b, bm_b, sched_b), and dQ along query tiles with the
- * forward half (itab_f, bm_f, sched_f).  Every output element is written exactly once (no
- * atomics), so results are deterministic.  `workspace` (device, >= the size above, 16-byte
- * aligned) is overwritten. */
+ * Section 3.3: each traversal direction has its own descriptor.  Three kernels, the three stages
+ * below in this order: a prologue (D, LSE * log2(e) into the workspace), dK and dV along key
+ * tiles with the backward half of the descriptor (itab_b, bm_b, sched_b), and dQ along query
+ * tiles with the forward half (itab_f, bm_f, sched_f).  Every output element is written exactly
+ * once (no atomics), so results are deterministic.  `workspace` (device, >= the size above,
+ * 16-byte aligned) is overwritten.  Every argument is checked before the first stage is queued.
+ * The dK/dV stage also checks on the device that bm_b is the transpose of bm_f and records
+ * CM_ERR_DESC_MISMATCH in the status word when it is not (the computation still runs). */
 CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
                        const void* o, const float* lse, const void* d_o, void* dq, void* dk,
                        void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
                        int d, float scale, void* stream);
+
+/* The three stages of cm_attn_bwd, for callers that queue or time them one by one.  Queued in
+ * this order on one stream with the same workspace they compute exactly what cm_attn_bwd does.
+ *   cm_attn_bwd_prologue  writes the workspace: per row of B*H*S, -D = -sum_c dO[c] * O[c] and
+ *                         -LSE * log2(e) (-inf for a row that sees nothing), fp32; reads o, lse,
+ *                         d_o (device, layouts as above);
+ *   cm_attn_bwd_dkdv      dk, dv along key tiles with the backward descriptor (section 3.3);
+ *                         reads q, k, v, d_o and the prologue's workspace;
+ *   cm_attn_bwd_dq        dq along query tiles with the forward descriptor; reads q, k, v, d_o
+ *                         and the prologue's workspace.
+ * Same argument rules and error codes as cm_attn_bwd. */
+CM_API int cm_attn_bwd_prologue(const void* o, const float* lse, const void* d_o, void* workspace,
+                                size_t workspace_bytes, int B, int H, int S, int d,
+                                void* stream);
+CM_API int cm_attn_bwd_dkdv(const cm_descriptor* desc, const void* q, const void* k,
+                            const void* v, const void* d_o, void* dk, void* dv,
+                            const void* workspace, size_t workspace_bytes, int B, int H, int S,
+                            int d, float scale, void* stream);
+CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* k, const void* v,
+                          const void* d_o, void* dq, const void* workspace,
+                          size_t workspace_bytes, int B, int H, int S, int d, float scale,
+                          void* stream);
+
+/* Limit of every bounded wait inside the attention kernels, for the whole process, in ns
+ * (0 restores the default of 2 s; at most 60 s, else CM_ERR_INVALID_ARG).  A wait that reaches it
+ * makes its CTA stop: the CTA waits for the copies and MMAs it already issued, writes zeros where
+ * it had no result, records CM_ERR_TIMEOUT in the status word (cm_get_status) and exits; the
+ * context stays usable.  This is a diagnostic hook: a very small limit makes ordinary waits
+ * expire, which tests the time-out path without a fault.  Not synchronised with launches in
+ * flight on other host threads.  (The pages describe no failure handling; this is the library's
+ * own.) */
+CM_API int cm_set_wait_limit_ns(unsigned long long ns);
 
 /* ---- backward without a workspace (no counterpart in the paper) ---------------------------- */
 
@@ -207,9 +245,10 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
  *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call on each
  *     device, with that device current; make that first call before any stream capture.
  *   - The array is held by every GPU that loads the library until the process exits.
- *   - All calls share the one array per device, and it keeps the previous call's contents (each
- *     call rewrites all of it before reading it).  Calls whose work overlaps on the GPU, e.g.
- *     on two streams, race on it: order them on one stream. */
+ *   - All calls share the one array per device, and it keeps the previous call's contents.
+ *     Each call first rewrites the part it reads (8 bytes per row of B*H*S: D and
+ *     LSE * log2(e)), so nothing needs clearing.  Calls whose work overlaps on the GPU, e.g. on
+ *     two streams, race on it: order them on one stream. */
 CM_API int cm_attn_bwd_noalloc(const cm_descriptor* desc, const void* q, const void* k,
                                const void* v, const void* o, const float* lse, const void* d_o,
                                void* dq, void* dk, void* dv, int B, int H, int S, int d,
@@ -217,7 +256,8 @@ CM_API int cm_attn_bwd_noalloc(const cm_descriptor* desc, const void* q, const v
 
 /* ---- status --------------------------------------------------------------------------------- */
 
-/* Wait for `stream`, then read desc->status: CM_OK, CM_ERR_TIMEOUT or CM_ERR_DEVICE_CHECK
+/* Wait for `stream`, then read desc->status: CM_OK, CM_ERR_TIMEOUT, CM_ERR_DEVICE_CHECK or
+ * CM_ERR_DESC_MISMATCH, the first error recorded since cm_build_descriptor cleared the word
  * (CM_ERR_CUDA if the wait or copy itself failed). */
 CM_API int cm_get_status(const cm_descriptor* desc, void* stream);
 

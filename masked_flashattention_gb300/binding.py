@@ -22,6 +22,7 @@ CM_ERR_UNSUPPORTED = -3
 CM_ERR_CUDA = -4
 CM_ERR_TIMEOUT = -5
 CM_ERR_DEVICE_CHECK = -6
+CM_ERR_DESC_MISMATCH = -7
 
 TILE = 128
 
@@ -75,6 +76,12 @@ def lib() -> ctypes.CDLL:
         L.cm_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
         L.cm_attn_bwd.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, sz, i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_attn_bwd_prologue.argtypes = [vp, vp, vp, vp, sz, i32, i32, i32, i32, vp]
+        L.cm_attn_bwd_dkdv.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp,
+                                       sz, i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_attn_bwd_dq.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, sz,
+                                     i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         L.cm_attn_bwd_noalloc.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp,
                                           vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
         L.cm_get_status.argtypes = [ctypes.POINTER(cm_descriptor), vp]
@@ -287,6 +294,53 @@ def cm_attn_bwd(desc: Descriptor, q, k, v, o, lse, d_o, dq, dk, dv, workspace: t
                              dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes,
                              B, H, S, d, scale, _stream(stream)),
            "cm_attn_bwd")
+
+
+def _bwd_shapes(q, others):
+    B, H, S, d = _bhsd(q, "q")
+    for t, n in others:
+        if _bhsd(t, n) != (B, H, S, d):
+            raise ValueError(f"{n} shape mismatch")
+    return B, H, S, d
+
+
+def cm_attn_bwd_prologue(o, lse, d_o, workspace: torch.Tensor, stream=None) -> None:
+    """Stage 1 of cm_attn_bwd: per-row -D and -LSE * log2(e) into the workspace."""
+    B, H, S, d = _bwd_shapes(o, ((d_o, "dO"),))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().cm_attn_bwd_prologue(o.data_ptr(), lse.data_ptr(), d_o.data_ptr(),
+                                      workspace.data_ptr(), nbytes, B, H, S, d, _stream(stream)),
+           "cm_attn_bwd_prologue")
+
+
+def cm_attn_bwd_dkdv(desc: Descriptor, q, k, v, d_o, dk, dv, workspace: torch.Tensor,
+                     scale: float | None = None, stream=None) -> None:
+    """Stage 2 of cm_attn_bwd: dK and dV along key tiles (backward descriptor)."""
+    B, H, S, d = _bwd_shapes(q, ((k, "k"), (v, "v"), (d_o, "dO"), (dk, "dk"), (dv, "dv")))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().cm_attn_bwd_dkdv(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                  d_o.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                  workspace.data_ptr(), nbytes, B, H, S, d, scale, _stream(stream)),
+           "cm_attn_bwd_dkdv")
+
+
+def cm_attn_bwd_dq(desc: Descriptor, q, k, v, d_o, dq, workspace: torch.Tensor,
+                   scale: float | None = None, stream=None) -> None:
+    """Stage 3 of cm_attn_bwd: dQ along query tiles (forward descriptor)."""
+    B, H, S, d = _bwd_shapes(q, ((k, "k"), (v, "v"), (d_o, "dO"), (dq, "dq")))
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().cm_attn_bwd_dq(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                d_o.data_ptr(), dq.data_ptr(), workspace.data_ptr(), nbytes,
+                                B, H, S, d, scale, _stream(stream)),
+           "cm_attn_bwd_dq")
+
+
+def cm_set_wait_limit_ns(ns: int) -> None:
+    """Process-wide limit of the attention kernels' bounded waits (0 = the 2 s default).  A
+    diagnostic hook: a tiny limit makes ordinary waits expire and exercises the time-out path."""
+    _check(lib().cm_set_wait_limit_ns(int(ns)), "cm_set_wait_limit_ns")
 
 
 def cm_attn_bwd_noalloc(desc: Descriptor, q, k, v, o, lse, d_o, dq, dk, dv,

@@ -3,10 +3,12 @@
 #include <cstdint>
 #include <atomic>
 #include <cmath>
+#include <initializer_list>
 
 #include "../../include/cm.h"
 #include "kernels.h"
 #include "program.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -21,6 +23,9 @@ constexpr int kMaxS = 131072;
 std::atomic<int> g_preprocess_mode{CM_PREPROCESS_GENERATED};
 // form of the attention kernels' partial-tile check (cm_set_interval_check)
 std::atomic<int> g_interval_check{CM_CHECK_UNSIGNED};
+// limit of each bounded wait inside the attention kernels (cm_set_wait_limit_ns)
+std::atomic<uint64_t> g_wait_limit_ns{cm::kDefaultWaitLimitNs};
+constexpr unsigned long long kMaxWaitLimitNs = 60ull * 1000000000ull;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -42,6 +47,39 @@ int check_desc(const cm_descriptor* d, int B, int S) {
   return CM_OK;
 }
 
+// Host checks shared by the attention entry points.
+int check_attn(const cm_descriptor* desc, int B, int H, int S, int d, float scale) {
+  int rc = check_shape(B, S);
+  if (rc != CM_OK) return rc;
+  rc = check_desc(desc, B, S);
+  if (rc != CM_OK) return rc;
+  if (H < 1 || static_cast<long long>(B) * H * (S / kTile) > 0x7FFFFFFFLL) return CM_ERR_INVALID_ARG;
+  if (H > kMaxHeads) return CM_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return CM_ERR_INVALID_ARG;
+  return CM_OK;
+}
+
+// Checks of the pointers of a call (all non-null and 16-byte aligned).
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return CM_ERR_INVALID_ARG;
+  return CM_OK;
+}
+
+size_t row_floats_bytes(int B, int H, int S) {
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  return (rows * 4 + 255) / 256 * 256;
+}
+
+int check_workspace(const void* workspace, size_t workspace_bytes, int B, int H, int S, int d) {
+  size_t need = 0;
+  const int rc = cm_attn_bwd_workspace_size(B, H, S, d, &need);
+  if (rc != CM_OK) return rc;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return CM_ERR_INVALID_ARG;
+  return CM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -55,6 +93,8 @@ CM_API const char* cm_error_string(int code) {
     case CM_ERR_CUDA: return "CUDA runtime error";
     case CM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
     case CM_ERR_DEVICE_CHECK: return "segment metadata failed device-side validation";
+    case CM_ERR_DESC_MISMATCH:
+      return "the backward Tile-State Bitmap is not the transpose of the forward one";
     default: return "unknown error";
   }
 }
@@ -119,20 +159,19 @@ CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_
   return CM_OK;
 }
 
+CM_API int cm_set_wait_limit_ns(unsigned long long ns) {
+  if (ns > kMaxWaitLimitNs) return CM_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns == 0 ? cm::kDefaultWaitLimitNs : static_cast<uint64_t>(ns));
+  return CM_OK;
+}
+
 CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
                        void* o, float* lse, int B, int H, int S, int d, float scale,
                        void* stream) {
-  int rc = check_shape(B, S);
+  int rc = check_attn(desc, B, H, S, d, scale);
   if (rc != CM_OK) return rc;
-  rc = check_desc(desc, B, S);
+  rc = check_ptrs({q, k, v, o, lse});
   if (rc != CM_OK) return rc;
-  if (H < 1 || static_cast<long long>(B) * H * (S / kTile) > 0x7FFFFFFFLL) return CM_ERR_INVALID_ARG;
-  if (H > kMaxHeads) return CM_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !o || !lse) return CM_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return CM_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return CM_ERR_INVALID_ARG;
   cm::FwdParams p;
   p.itab = desc->itab_f;
   p.bm = desc->bm_f;
@@ -148,6 +187,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.NI = desc->ni_f;
   p.check = g_interval_check.load();
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_ns = g_wait_limit_ns.load();
   return cm::launch_attn_fwd(p, d, q, k, v, static_cast<cudaStream_t>(stream)) == 0
              ? CM_OK
              : CM_ERR_CUDA;
@@ -156,42 +196,47 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
 CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes) {
   if (!bytes || B < 1 || H < 1 || S < 1) return CM_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
-  const size_t rows = static_cast<size_t>(B) * H * S;
-  const size_t row_floats = (rows * 4 + 255) / 256 * 256;  // D, then LSE * log2(e)
-  *bytes = 2 * row_floats;
+  *bytes = 2 * row_floats_bytes(B, H, S);  // D, then LSE * log2(e)
   return CM_OK;
 }
 
-CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
-                       const void* o, const float* lse, const void* d_o, void* dq, void* dk,
-                       void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
-                       int d, float scale, void* stream) {
-  int rc = check_shape(B, S);
-  if (rc != CM_OK) return rc;
-  rc = check_desc(desc, B, S);
-  if (rc != CM_OK) return rc;
-  if (H < 1 || static_cast<long long>(B) * H * (S / kTile) > 0x7FFFFFFFLL) return CM_ERR_INVALID_ARG;
-  if (H > kMaxHeads) return CM_ERR_UNSUPPORTED;
+CM_API int cm_attn_bwd_prologue(const void* o, const float* lse, const void* d_o, void* workspace,
+                                size_t workspace_bytes, int B, int H, int S, int d,
+                                void* stream) {
+  if (B < 1 || H < 1 || S < 1 || S % kTile != 0) return CM_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return CM_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
-    return CM_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
-  for (const void* x : ptrs)
-    if (!aligned16(x)) return CM_ERR_INVALID_ARG;
-  size_t need = 0;
-  cm_attn_bwd_workspace_size(B, H, S, d, &need);
-  if (workspace_bytes < need) return CM_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return CM_ERR_INVALID_ARG;
-  const size_t rows = static_cast<size_t>(B) * H * S;
-  const size_t row_floats = (rows * 4 + 255) / 256 * 256;
+  int rc = check_ptrs({o, lse, d_o});
+  if (rc != CM_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
+  if (rc != CM_OK) return rc;
+  float* delta = static_cast<float*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + row_floats_bytes(B, H, S));
+  return cm::launch_bwd_prologue(d, o, d_o, lse, delta, lse2, static_cast<size_t>(B) * H * S,
+                                 static_cast<cudaStream_t>(stream)) == 0
+             ? CM_OK
+             : CM_ERR_CUDA;
+}
+
+CM_API int cm_attn_bwd_dkdv(const cm_descriptor* desc, const void* q, const void* k,
+                            const void* v, const void* d_o, void* dk, void* dv,
+                            const void* workspace, size_t workspace_bytes, int B, int H, int S,
+                            int d, float scale, void* stream) {
+  int rc = check_attn(desc, B, H, S, d, scale);
+  if (rc != CM_OK) return rc;
+  rc = check_ptrs({q, k, v, d_o, dk, dv});
+  if (rc != CM_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
+  if (rc != CM_OK) return rc;
   cm::BwdParams p;
   p.itab = desc->itab_b;
   p.bm = desc->bm_b;
+  p.bm_f = desc->bm_f;
   p.sched = desc->sched_b;
   p.status = desc->status;
-  p.lse = lse;
-  p.delta = static_cast<float*>(workspace);
-  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + row_floats);
+  p.lse = nullptr;
+  p.delta = const_cast<float*>(static_cast<const float*>(workspace));
+  p.lse2 = reinterpret_cast<float*>(const_cast<char*>(static_cast<const char*>(workspace)) +
+                                    row_floats_bytes(B, H, S));
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.B = B;
@@ -203,26 +248,64 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.check = g_interval_check.load();
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cm::launch_attn_bwd(p, d, q, k, v, o, d_o, st) != 0) return CM_ERR_CUDA;
+  p.wait_ns = g_wait_limit_ns.load();
+  return cm::launch_attn_dkdv(p, d, q, k, v, d_o, static_cast<cudaStream_t>(stream)) == 0
+             ? CM_OK
+             : CM_ERR_CUDA;
+}
+
+CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* k, const void* v,
+                          const void* d_o, void* dq, const void* workspace,
+                          size_t workspace_bytes, int B, int H, int S, int d, float scale,
+                          void* stream) {
+  int rc = check_attn(desc, B, H, S, d, scale);
+  if (rc != CM_OK) return rc;
+  rc = check_ptrs({q, k, v, d_o, dq});
+  if (rc != CM_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
+  if (rc != CM_OK) return rc;
   cm::DqParams g;
   g.itab = desc->itab_f;
   g.bm = desc->bm_f;
   g.sched = desc->sched_f;
   g.status = desc->status;
-  g.delta = p.delta;
-  g.lse2 = p.lse2;
+  g.delta = static_cast<const float*>(workspace);
+  g.lse2 = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
+                                          row_floats_bytes(B, H, S));
   g.dq = static_cast<__nv_bfloat16*>(dq);
   g.B = B;
   g.H = H;
   g.S = S;
-  g.NT = p.NT;
-  g.W = p.W;
+  g.NT = S / kTile;
+  g.W = (g.NT + 15) / 16;
   g.NI = desc->ni_f;
-  g.check = p.check;
+  g.check = g_interval_check.load();
   g.scale = scale;
-  g.scale_log2 = p.scale_log2;
-  return cm::launch_attn_dq(g, d, q, k, v, d_o, st) == 0 ? CM_OK : CM_ERR_CUDA;
+  g.scale_log2 = scale * 1.4426950408889634f;
+  g.wait_ns = g_wait_limit_ns.load();
+  return cm::launch_attn_dq(g, d, q, k, v, d_o, static_cast<cudaStream_t>(stream)) == 0
+             ? CM_OK
+             : CM_ERR_CUDA;
+}
+
+CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, const void* v,
+                       const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
+                       int d, float scale, void* stream) {
+  // every argument is checked before the first stage is queued
+  int rc = check_attn(desc, B, H, S, d, scale);
+  if (rc != CM_OK) return rc;
+  rc = check_ptrs({q, k, v, o, lse, d_o, dq, dk, dv});
+  if (rc != CM_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
+  if (rc != CM_OK) return rc;
+  rc = cm_attn_bwd_prologue(o, lse, d_o, workspace, workspace_bytes, B, H, S, d, stream);
+  if (rc != CM_OK) return rc;
+  rc = cm_attn_bwd_dkdv(desc, q, k, v, d_o, dk, dv, workspace, workspace_bytes, B, H, S, d, scale,
+                        stream);
+  if (rc != CM_OK) return rc;
+  return cm_attn_bwd_dq(desc, q, k, v, d_o, dq, workspace, workspace_bytes, B, H, S, d, scale,
+                        stream);
 }
 
 CM_API int cm_get_status(const cm_descriptor* desc, void* stream) {
@@ -231,8 +314,9 @@ CM_API int cm_get_status(const cm_descriptor* desc, void* stream) {
   int32_t v = 0;
   if (cudaMemcpy(&v, desc->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CM_ERR_CUDA;
   const int code = v >> 16;
-  if (code == 0) return CM_OK;
-  if (code == 1) return CM_ERR_TIMEOUT;
+  if (code == cm::kDevOk) return CM_OK;
+  if (code == cm::kDevTimeout) return CM_ERR_TIMEOUT;
+  if (code == cm::kDevDescMismatch) return CM_ERR_DESC_MISMATCH;
   return CM_ERR_DEVICE_CHECK;
 }
 

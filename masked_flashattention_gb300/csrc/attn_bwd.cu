@@ -89,7 +89,8 @@ enum {
   B_PDS = 7,       // compute warps wrote dS^T (TMEM) and read dP^T (8 arrivals)
   B_DONE = 8,      // every MMA of the CTA completed (dK, dV final)
   B_PREADY = 9,    // compute warps wrote P^T (TMEM) (8 arrivals)
-  B_COUNT = 10
+  B_DRAIN = 10,    // abort path only: every MMA issued so far has completed
+  B_COUNT = 11
 };
 
 
@@ -170,6 +171,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
   uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const WaitCtl wait{abort_flag, p.status, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -192,6 +194,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_PDS), kComputeWarps);
     mbar_init(bar(B_DONE), 1);
     mbar_init(bar(B_PREADY), kComputeWarps);
+    mbar_init(bar(B_DRAIN), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -216,6 +219,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   const int nt = *s_ntiles;
   const int row0 = bh * p.S;
+  // asynchronous work issued so far, for the abort path: query-tile slots armed (producer), any
+  // MMA issued (MMA thread)
+  int m_armed = 0;
+  bool mma_issued = false;
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
@@ -234,9 +241,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int slot = m & 1;
         const size_t r = static_cast<size_t>(row0) + qt * 128;
         // a slot is free once the dK MMA of the tile two back (its last reader) is done
-        if (m >= 2 && !mbar_wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, abort_flag, p.status, 0x201))
+        if (m >= 2 && !wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, 0x201))
           break;
         const uint32_t full = bar(B_QFULL + slot);
+        m_armed = m + 1;
         mbar_arrive_expect_tx(full, 2u * (L::kTileBytes + 512u));
         for (int x = 0; x < D / 64; ++x) {
           tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
@@ -255,10 +263,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
       // tile 0: S^T -> RA, dP^T -> RB
-      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, p.status, 0x202) &&
-                mbar_wait(bar(B_QFULL), 0, abort_flag, p.status, 0x203);
+      bool ok = wait(bar(B_KV), 0, 0x202) &&
+                wait(bar(B_QFULL), 0, 0x203);
       if (ok) {
         tc_fence_after();
+        mma_issued = true;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColRA, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sbase + L::kQ, kk, 16384u),
@@ -280,19 +289,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sdO = sbase + L::kdO + (m & 1) * L::kTileBytes;
         // dV += P^T dO as soon as P^T is in X, while the compute warps work on dS^T.
         // P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
-        if (!mbar_wait(bar(B_PREADY), m & 1, abort_flag, p.status, 0x210)) break;
+        if (!wait(bar(B_PREADY), m & 1, 0x210)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                   sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        if (!mbar_wait(bar(B_PDS), m & 1, abort_flag, p.status, 0x205)) break;
+        if (!wait(bar(B_PDS), m & 1, 0x205)) break;
         tc_fence_after();
         if (m + 1 < nt) {
           // the next tile's S^T into Y (its dP^T was consumed), so that its P can start while
           // the tensor pipe runs dK
           const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
-          if (!mbar_wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, abort_flag, p.status, 0x203))
+          if (!wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, 0x203))
             break;
           tc_fence_after();
 #pragma unroll
@@ -328,6 +337,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK)
     const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    if (warp == 0 && h == 0) {
+      // The backward descriptor must describe the transposed mask of the forward one: tile
+      // (kt, q) of this bitmap row has the state of tile (q, kt) of the forward bitmap.  Checked
+      // once per key tile (head 0); a mismatch (two MaskSpecs that do not describe the same
+      // mask) is recorded in the status word, the computation goes on.
+      bool bad = false;
+      for (int q = lane; q < p.NT; q += 32) {
+        const uint32_t cb = (bmrow[q >> 4] >> (2 * (q & 15))) & 3u;
+        const uint32_t cf =
+            (p.bm_f[(static_cast<size_t>(b) * p.NT + q) * p.W + (kt >> 4)] >> (2 * (kt & 15))) & 3u;
+        bad |= cb != cf;
+      }
+      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, kDevDescMismatch, kt);
+    }
     RowIntervals ri;
     load_row_intervals(p.itab, b, p.NI, p.S, j, p.check, ri);
     const float sl2 = p.scale_log2;
@@ -339,8 +362,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint32_t Y = (m & 1) ? kColRA : kColRB;
 
       // ---- P^T: S^T from X, written back in place as bf16 pairs; fp32 P kept for dS ----
-      bool ready = mbar_wait(bar(B_SFULL), m & 1, abort_flag, p.status, 0x206) &&
-                   mbar_wait(bar(B_QFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x207);
+      bool ready = wait(bar(B_SFULL), m & 1, 0x206) &&
+                   wait(bar(B_QFULL + (m & 1)), (m >> 1) & 1, 0x207);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -369,7 +392,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (lane == 0) mbar_arrive(bar(B_PREADY));
 
       // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T as bf16 pairs into X ----
-      ready = mbar_wait(bar(B_DPFULL), m & 1, abort_flag, p.status, 0x20e);
+      ready = wait(bar(B_DPFULL), m & 1, 0x20e);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -394,7 +417,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // ---- epilogue: dV, dK (scaled) -> bf16, this warp's half of the head dim ----
     __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
     __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
-    const bool done = nt > 0 && ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status, 0x20f);
+    const bool done = nt > 0 && ok && wait(bar(B_DONE), 0, 0x20f);
     __syncwarp();
     if (done) {
       tc_fence_after();
@@ -435,6 +458,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up.  Copies and MMAs already issued still land in shared memory and TMEM:
+    // wait for them before TMEM is freed and the CTA exits.
+    if (warp == kProducerWarp && lane == 0 && nt > 0) {
+      mbar_wait_drain(bar(B_KV), 0, p.status, 0x2f0);
+      for (int s = 0; s < 2 && s < m_armed; ++s)
+        mbar_wait_drain(bar(B_QFULL + s), ((m_armed - 1 - s) >> 1) & 1, p.status, 0x2f1);
+    }
+    if (warp == kMmaWarp && lane == 0 && mma_issued) {
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status, 0x2f2);
+    }
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
@@ -467,21 +504,23 @@ __global__ void __launch_bounds__(256) bwd_prologue_kernel(const __nv_bfloat16* 
 
 }  // namespace bwd
 
-int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
-                    const void* o, const void* d_o, cudaStream_t stream) {
+int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse, float* delta,
+                        float* lse2, size_t rows, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 128)
+    bwd::bwd_prologue_kernel<128><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, delta,
+        lse2, rows);
+  else
+    bwd::bwd_prologue_kernel<64><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, delta,
+        lse2, rows);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, const void* v,
+                     const void* d_o, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
-  {
-    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-    if (d == 128)
-      bwd::bwd_prologue_kernel<128><<<blocks, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
-          p.delta, p.lse2, rows);
-    else
-      bwd::bwd_prologue_kernel<64><<<blocks, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), p.lse,
-          p.delta, p.lse2, rows);
-    if (cudaGetLastError() != cudaSuccess) return -1;
-  }
   CUtensorMap mq, mk, mv, mdo;
   if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
       !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))

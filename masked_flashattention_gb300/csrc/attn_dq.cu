@@ -67,7 +67,8 @@ enum {
   B_DPFULL = 13,  // dP of the current tile computed
   B_DSFULL = 14,  // compute warps wrote dS and read dP (8 arrivals)
   B_DONE = 15,    // every MMA of the CTA completed
-  B_COUNT = 16
+  B_DRAIN = 16,   // abort path only: every MMA issued so far has completed
+  B_COUNT = 17
 };
 
 
@@ -88,6 +89,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
   uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const WaitCtl wait{abort_flag, p.status, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -115,6 +117,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_DSFULL), kComputeWarps);
     mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -138,6 +141,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nt = *s_ntiles;
+  // asynchronous work issued so far, for the abort path: K and V slots armed (producer), any MMA
+  // issued (MMA thread)
+  int nk_armed = 0, nv_armed = 0;
+  bool mma_issued = false;
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
@@ -155,15 +162,17 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
         const int sk = n % kKStages, sv = n % kVStages;
         if (n >= kKStages &&
-            !mbar_wait(bar(B_KEMPTY + sk), ((n / kKStages) - 1) & 1, abort_flag, p.status, 0x301))
+            !wait(bar(B_KEMPTY + sk), ((n / kKStages) - 1) & 1, 0x301))
           break;
+        nk_armed = n + 1;
         mbar_arrive_expect_tx(bar(B_KFULL + sk), L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kK + sk * L::kTileBytes + x * 16384u, &tmK, x * 64,
                       row0 + kt * 128, bar(B_KFULL + sk));
         if (n >= kVStages &&
-            !mbar_wait(bar(B_VEMPTY + sv), ((n / kVStages) - 1) & 1, abort_flag, p.status, 0x302))
+            !wait(bar(B_VEMPTY + sv), ((n / kVStages) - 1) & 1, 0x302))
           break;
+        nv_armed = n + 1;
         mbar_arrive_expect_tx(bar(B_VFULL + sv), L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sbase + L::kV + sv * L::kTileBytes + x * 16384u, &tmV, x * 64,
@@ -178,8 +187,9 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const uint32_t sQ = sbase + L::kQ, sdO = sbase + L::kdO;
       auto issue_s = [&](int n) -> bool {  // S(n) into buffer n % 2
         const int sk = n % kKStages;
-        if (!mbar_wait(bar(B_KFULL + sk), (n / kKStages) & 1, abort_flag, p.status, 0x303)) return false;
+        if (!wait(bar(B_KFULL + sk), (n / kKStages) & 1, 0x303)) return false;
         tc_fence_after();
+        mma_issued = true;
         const uint32_t sK = sbase + L::kK + sk * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -190,7 +200,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       };
       auto issue_dp = [&](int n) -> bool {  // dP(n); the compute warps have read dP(n-1)
         const int sv = n % kVStages;
-        if (!mbar_wait(bar(B_VFULL + sv), (n / kVStages) & 1, abort_flag, p.status, 0x304)) return false;
+        if (!wait(bar(B_VFULL + sv), (n / kVStages) & 1, 0x304)) return false;
         tc_fence_after();
         const uint32_t sV = sbase + L::kV + sv * L::kTileBytes;
 #pragma unroll
@@ -201,10 +211,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         umma_commit(bar(B_VEMPTY + sv));
         return true;
       };
-      bool ok = mbar_wait(bar(B_QDO), 0, abort_flag, p.status, 0x305) && issue_s(0) && issue_dp(0);
+      bool ok = wait(bar(B_QDO), 0, 0x305) && issue_s(0) && issue_dp(0);
       for (int n = 0; ok && n < nt; ++n) {
         if (n + 1 < nt && !issue_s(n + 1)) break;  // its buffer's dS(n-1) was read by dQ(n-1)
-        if (!mbar_wait(bar(B_DSFULL), n & 1, abort_flag, p.status, 0x306)) break;
+        if (!wait(bar(B_DSFULL), n & 1, 0x306)) break;
         tc_fence_after();
         // dP(n+1) first: the compute warps have read dP(n), and the next tile's dS waits for it,
         // while dQ(n) only feeds the accumulator
@@ -241,7 +251,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     for (int n = 0; ok && n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
       const int sb = n & 1;
       const uint32_t sS = tmem + lane_off + kColS + sb * 128 + 64 * hf;
-      bool ready = mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x307);
+      bool ready = wait(bar(B_SFULL + sb), (n >> 1) & 1, 0x307);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -268,7 +278,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         pf[c] = ex2_approx(x.x);
         pf[c + 1] = ex2_approx(x.y);
       }
-      ready = mbar_wait(bar(B_DPFULL), n & 1, abort_flag, p.status, 0x308);
+      ready = wait(bar(B_DPFULL), n & 1, 0x308);
       __syncwarp();
       if (!ready) { ok = false; break; }
       tc_fence_after();
@@ -295,7 +305,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
     // ---- epilogue: dQ = scale * accumulator -> bf16, this warp's half of the head dim ----
     __nv_bfloat16* qrow = p.dq + (static_cast<size_t>(row0) + i) * D + hf * kHalf;
-    const bool done = ok && nt > 0 && mbar_wait(bar(B_DONE), 0, abort_flag, p.status, 0x309);
+    const bool done = ok && nt > 0 && wait(bar(B_DONE), 0, 0x309);
     __syncwarp();
     if (done) {
       tc_fence_after();
@@ -325,6 +335,22 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up.  Copies and MMAs already issued still land in shared memory and TMEM:
+    // wait for them before TMEM is freed and the CTA exits.
+    if (warp == kProducerWarp && lane == 0 && nt > 0) {
+      mbar_wait_drain(bar(B_QDO), 0, p.status, 0x3f0);
+      for (int s = 0; s < kKStages && s < nk_armed; ++s)
+        mbar_wait_drain(bar(B_KFULL + s), ((nk_armed - 1 - s) / kKStages) & 1, p.status, 0x3f1);
+      for (int s = 0; s < kVStages && s < nv_armed; ++s)
+        mbar_wait_drain(bar(B_VFULL + s), ((nv_armed - 1 - s) / kVStages) & 1, p.status, 0x3f2);
+    }
+    if (warp == kMmaWarp && lane == 0 && mma_issued) {
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status, 0x3f3);
+    }
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }

@@ -76,7 +76,8 @@ enum {
   B_PFULL = 9,    // +buffer: P of a tile in that S buffer, both halves (8 arrivals)
   B_PAIR = 11,    // +quarter: merge exchange of a warp pair (2 arrivals, once)
   B_ALLDONE = 15, // every MMA of the CTA has completed (once)
-  B_COUNT = 16
+  B_DRAIN = 16,   // abort path only: every MMA issued so far has completed
+  B_COUNT = 17
 };
 
 template <int D>
@@ -95,6 +96,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
   uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const WaitCtl wait{abort_flag, p.status, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -119,6 +121,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int s = 0; s < 4; ++s) mbar_init(bar(B_PAIR + s), 2);
     mbar_init(bar(B_ALLDONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -142,6 +145,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nt = *s_ntiles;
+  // asynchronous work issued so far, for the abort path: K/V stages armed (producer), any MMA
+  // issued (MMA thread)
+  int n_armed = 0;
+  bool mma_issued = false;
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
@@ -157,9 +164,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
         const int st = n % kStages;
         if (n >= kStages &&
-            !mbar_wait(bar(B_KVEMPTY + st), ((n / kStages) - 1) & 1, abort_flag, p.status, 0x101))
+            !wait(bar(B_KVEMPTY + st), ((n / kStages) - 1) & 1, 0x101))
           break;
         const uint32_t sK = sbase + L::kKV + st * 2u * L::kTileBytes;
+        n_armed = n + 1;
         mbar_arrive_expect_tx(bar(B_KVFULL + st), 2u * L::kTileBytes);
         for (int x = 0; x < D / 64; ++x)
           tma_load_2d(sK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KVFULL + st));
@@ -174,14 +182,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // A = Q, B = K, both K-major
       constexpr uint32_t idO = make_idesc_bf16(128, D, 0, 1);    // A = P (TMEM), B = V MN-major
       const uint32_t dQ = sdesc_lo(sbase + L::kQ, 16u);
-      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, 0x102);
+      bool ok = wait(bar(B_Q), 0, 0x102);
       // O_h += P_h V_h for tile m: keys [64h, +64) are the K-steps kk = 4h .. 4h+3.  V(m) landed
       // before S(m) was issued (same barrier as K(m)).
       auto issue_pv = [&](int m) -> bool {
         const int st = m % kStages;
         // one barrier per S buffer: the softmax warps can be at most one tile ahead of this
         // wait, so a barrier never runs two phases ahead of its waiter
-        if (!mbar_wait(bar(B_PFULL + (m & 1)), (m >> 1) & 1, abort_flag, p.status, 0x103))
+        if (!wait(bar(B_PFULL + (m & 1)), (m >> 1) & 1, 0x103))
           return false;
         tc_fence_after();
         const uint32_t dV = sdesc_lo(sbase + L::kKV + st * 2u * L::kTileBytes + L::kTileBytes, 16384u);
@@ -202,9 +210,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // S(n) into buffer n % 2 = Q K(n)^T
       auto issue_s = [&](int n) -> bool {
         const int st = n % kStages;
-        if (!mbar_wait(bar(B_KVFULL + st), (n / kStages) & 1, abort_flag, p.status, 0x105))
+        if (!wait(bar(B_KVFULL + st), (n / kStages) & 1, 0x105))
           return false;
         tc_fence_after();
+        mma_issued = true;
         const uint32_t dK = sdesc_lo(sbase + L::kKV + st * 2u * L::kTileBytes, 16u);
         const uint32_t dS = tmem + kColS + (n & 1) * 128;
 #pragma unroll
@@ -239,7 +248,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     int kt = next_tile(bmrow, p.NT, 0);
     for (int n = 0; ok && n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
       const int sb = n & 1;
-      const bool s_ready = mbar_wait(bar(B_SFULL + sb), (n >> 1) & 1, abort_flag, p.status, 0x107);
+      const bool s_ready = wait(bar(B_SFULL + sb), (n >> 1) & 1, 0x107);
       __syncwarp();
       if (!s_ready) { ok = false; break; }
       tc_fence_after();
@@ -298,8 +307,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // rescale this half's O: PV(n-1) must be complete (PV(n-2) and earlier are, since S(n)
         // is).  Its stage barrier is at most one phase ahead of this wait: PV(n+2) needs this
         // warp's P(n+2).
-        const bool o_ready = mbar_wait(bar(B_KVEMPTY + (n - 1) % kStages), ((n - 1) / kStages) & 1,
-                                       abort_flag, p.status, 0x108);
+        const bool o_ready = wait(bar(B_KVEMPTY + (n - 1) % kStages), ((n - 1) / kStages) & 1, 0x108);
         __syncwarp();
         if (!o_ready) { ok = false; break; }
         tc_fence_after();
@@ -322,7 +330,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 
     // ---- epilogue: merge the two halves, O -> bf16, LSE (natural log) ----
-    bool o_final = ok && mbar_wait(bar(B_ALLDONE), 0, abort_flag, p.status, 0x109);
+    bool o_final = ok && wait(bar(B_ALLDONE), 0, 0x109);
     __syncwarp();
     // exchange (max, sum) with the warp of the other half through the Q tile, which no MMA
     // reads any more
@@ -333,7 +341,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       __syncwarp();
       const uint32_t pb = bar(B_PAIR + quarter);
       if (lane == 0) mbar_arrive(pb);
-      o_final = mbar_wait(pb, 0, abort_flag, p.status, 0x10b);
+      o_final = wait(pb, 0, 0x10b);
       __syncwarp();
       if (o_final) {
         const float2 ot = slot[(hf ^ 1) * 128 + r];
@@ -384,6 +392,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up.  Copies and MMAs already issued still land in shared memory and TMEM:
+    // wait for them before TMEM is freed and the CTA exits.
+    if (warp == kProducerWarp && lane == 0 && nt > 0) {
+      mbar_wait_drain(bar(B_Q), 0, p.status, 0x1f0);
+      for (int s = 0; s < kStages && s < n_armed; ++s)
+        mbar_wait_drain(bar(B_KVFULL + s), ((n_armed - 1 - s) / kStages) & 1, p.status, 0x1f1);
+    }
+    if (warp == kMmaWarp && lane == 0 && mma_issued) {
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status, 0x1f2);
+    }
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }

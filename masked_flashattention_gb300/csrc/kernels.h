@@ -25,11 +25,13 @@ struct FwdParams {
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale_log2;      // softmax scale * log2(e)
+  uint64_t wait_ns;      // limit of each bounded wait (ns)
 };
 
 struct BwdParams {
   const int32_t* itab;   // backward Interval Table [B][NI][S][2]
   const uint32_t* bm;    // backward bitmaps [B][NT][W]
+  const uint32_t* bm_f;  // forward bitmaps [B][NT][W], checked to be the transpose of bm
   const int32_t* sched;  // (b << 16 | k_tile), longest first
   int32_t* status;
   const float* lse;      // [B][H][S] natural log (forward output)
@@ -41,6 +43,7 @@ struct BwdParams {
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
+  uint64_t wait_ns;      // limit of each bounded wait (ns)
 };
 
 // dQ pass of the backward: traverses query tiles with the forward descriptor.
@@ -56,6 +59,7 @@ struct DqParams {
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
   float scale;
   float scale_log2;
+  uint64_t wait_ns;      // limit of each bounded wait (ns)
 };
 
 // Runs the generated kernels when both gen_fwd and gen_bwd are given, else the generic kernel.
@@ -66,9 +70,12 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_fw
                       cudaStream_t stream);
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream);
-// Prologue (D, LSE * log2(e)) and the dK/dV kernel; then launch_attn_dq for dQ.
-int launch_attn_bwd(const BwdParams& p, int d, const void* q, const void* k, const void* v,
-                    const void* o, const void* d_o, cudaStream_t stream);
+// Backward prologue: per row -D = -rowsum(dO * O) and -LSE * log2(e) (rows = B * H * S).
+int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse, float* delta,
+                        float* lse2, size_t rows, cudaStream_t stream);
+// dK and dV along key tiles (backward descriptor); reads the prologue's outputs.
+int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, const void* v,
+                     const void* d_o, cudaStream_t stream);
 int launch_attn_dq(const DqParams& p, int d, const void* q, const void* k, const void* v,
                    const void* d_o, cudaStream_t stream);
 

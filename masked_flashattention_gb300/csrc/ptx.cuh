@@ -22,6 +22,7 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,      // an mbarrier wait exceeded its limit
   kDevBadMeta = 2,      // segment metadata not monotone / not ending at S
+  kDevDescMismatch = 3, // backward Tile-State Bitmap is not the transposed forward bitmap
 };
 
 __device__ __forceinline__ void set_status(int* status, int code, int where) {
@@ -78,23 +79,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait.  `abort` (shared memory) lets one role that gave up release every other role of
-// the CTA quickly: once set, all later waits return false at once.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+// Bounded waits.  Every wait of a role on a phase that another role completes goes through
+// WaitCtl: it gives up after `limit_ns` (a kernel parameter; 2 s unless the host lowered it), sets
+// the CTA's `abort` flag (shared memory) and the status word, and returns false.  Once the flag is
+// set, every later WaitCtl wait of the CTA returns false at once, so all roles leave their loops
+// quickly.  Before the CTA frees TMEM and exits, the roles that issued asynchronous work (TMA
+// copies, tcgen05 MMAs) wait for it with mbar_wait_drain: that work completes by itself, whatever
+// the other roles did, so these waits end; they are bounded all the same.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
+struct WaitCtl {
+  volatile int* abort;
+  int* status;
+  uint64_t limit_ns;
+  __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity, int where) const {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        set_status(status, kDevTimeout, where);
+        return false;
+      }
+    }
+  }
+};
+
+// Wait for a phase whose completion needs no other role (copies or MMAs already issued by the
+// calling thread), ignoring the abort flag.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* status,
+                                                int where) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kDrainLimitNs) {
       set_status(status, kDevTimeout, where);
       return false;
     }
   }
+  return true;
 }
 
 // ----------------------------------------------------------------------------------------------

@@ -161,9 +161,44 @@ def test_attention_argument_validation_happens_on_the_host(B):
                                  None) == B.CM_ERR_INVALID_ARG
 
 
+def test_backward_stage_validation_happens_on_the_host(B):
+    """The three stages of the backward check their arguments like cm_attn_bwd does."""
+    L = B.lib()
+    p = ctypes.c_void_p(1 << 20)
+    d = _fake_desc(B, 1, 256)
+    need = B.cm_attn_bwd_workspace_size(1, 2, 256, 64)
+    # prologue: unsupported head dim, null tensor, short workspace, S not a multiple of the tile
+    assert L.cm_attn_bwd_prologue(p, p, p, p, need, 1, 2, 256, 96, None) == B.CM_ERR_UNSUPPORTED
+    assert L.cm_attn_bwd_prologue(None, p, p, p, need, 1, 2, 256, 64, None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_prologue(p, p, p, p, need - 1, 1, 2, 256, 64, None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_prologue(p, p, p, p, need, 1, 2, 200, 64, None) == B.CM_ERR_INVALID_ARG
+    # dK/dV and dQ stages: descriptor for another shape, misaligned output, short workspace
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert L.cm_attn_bwd_dkdv(ctypes.byref(d), p, p, p, p, p, p, p, need, 2, 2, 256, 64, 0.1,
+                              None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_dkdv(ctypes.byref(d), p, p, p, p, odd, p, p, need, 1, 2, 256, 64, 0.1,
+                              None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, need - 1, 1, 2, 256, 64, 0.1,
+                            None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, need, 1, 2, 256, 64,
+                            float("inf"), None) == B.CM_ERR_INVALID_ARG
+    # cm_attn_bwd checks everything before its first stage: a bad dq pointer is caught even
+    # though the prologue's own arguments are fine
+    assert L.cm_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, need, 1, 2, 256, 64,
+                         0.1, None) == B.CM_ERR_INVALID_ARG
+
+
+def test_wait_limit_validation(B):
+    L = B.lib()
+    assert L.cm_set_wait_limit_ns(61 * 10**9) == B.CM_ERR_INVALID_ARG
+    B.cm_set_wait_limit_ns(1)
+    B.cm_set_wait_limit_ns(0)  # back to the default
+
+
 def test_error_strings(B):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert B.cm_error_string(code)
+    assert "transpose" in B.cm_error_string(B.CM_ERR_DESC_MISMATCH)
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])

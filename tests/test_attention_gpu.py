@@ -125,8 +125,36 @@ def test_rows_and_columns_that_see_nothing():
     check_heads(0, seg, nseg, Q, K, V, dO, out, range(2), mask_fn=lambda r0, r1: dense[r0:r1])
 
 
+def check_row_blocks_every_head(wid, seg, nseg, Q, K, V, dO, out, row0s):
+    """Every (sample, head) on a few 128-row blocks of query rows, against the oracle run on
+    those rows only: O, LSE and dQ of the rows, and for the last block (rows [S - 128, S)) the
+    complete dK and dV of the last 128 keys, which no earlier row sees in these masks (every
+    rule here is causal: key j is visible only to rows i >= j)."""
+    o, lse, dq, dk, dv = out
+    Bn, H, S, d = Q.shape
+    for b in range(Bn):
+        n = int(nseg[b])
+        for r0 in row0s:
+            R = slice(r0, r0 + 128)
+            rows = np.arange(r0, r0 + 128)
+            dense = M.dense_mask(wid, seg[b], n, S, rows=rows)
+            assert not dense[:, rows[-1] + 1:].any()  # causal: nothing right of the block
+            for h in range(H):
+                ro, rl = A.attention_forward(Q[b, h, R], K[b, h], V[b, h], dense)
+                rq, rk, rv = A.attention_backward(Q[b, h, R], K[b, h], V[b, h], dO[b, h, R], dense)
+                _assert_close(f"O b{b}h{h} rows {r0}+", o[b, h, R], ro)
+                _assert_close(f"LSE b{b}h{h} rows {r0}+", lse[b, h, R], rl)
+                _assert_close(f"dQ b{b}h{h} rows {r0}+", dq[b, h, R], rq)
+                if r0 == S - 128:
+                    _assert_close(f"dK b{b}h{h} last keys", dk[b, h, R], rk[R])
+                    _assert_close(f"dV b{b}h{h} last keys", dv[b, h, R], rv[R])
+
+
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
 def test_full_size_sampled_heads(wid):
+    """Full size, in the benchmark's launch configuration.  Heads 0 and H-1 of every sample are
+    compared in full; every other head on its first, middle and last 128 query rows (and the
+    last 128 keys), so that each head's place in the kernels' grid is checked too."""
     from masked_flashattention_gb300 import specs
     B = _lib()
     w = W.WORKLOADS[wid]
@@ -135,6 +163,24 @@ def test_full_size_sampled_heads(wid):
     out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO)
     heads = range(w.H) if wid == 1 else sorted({0, w.H - 1})
     check_heads(wid, seg, nseg, Q, K, V, dO, out, heads)
+    if wid != 1:
+        check_row_blocks_every_head(wid, seg, nseg, Q, K, V, dO, out,
+                                    (0, (w.S // 256) * 128, w.S - 128))
+
+
+def test_every_head_of_every_sample_with_full_schedule_chunks():
+    """The kernels take the longest-first schedule in chunks of 128 work items and walk every
+    head inside a chunk (a different branch of the grid mapping than when the schedule holds
+    fewer than 128 items).  B * S/128 = 17 * 16 = 272 work items make two full chunks and a
+    partial one; every (sample, head) is compared with the oracle, element by element."""
+    from masked_flashattention_gb300 import specs
+    B = _lib()
+    wid, S, Bn, H, d = 1, 2048, 17, 4, 128
+    w = W.scaled(W.WORKLOADS[wid], S, B=Bn, H=H, d=d)
+    seg, nseg = W.segments(wid, w.B, S, seed=2024)
+    Q, K, V, dO = W.full_tensors(w, seed=99)
+    out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO)
+    check_heads(wid, seg, nseg, Q, K, V, dO, out, range(H))
 
 
 CHECKS = {"two_compare": 1, "masked": 2}

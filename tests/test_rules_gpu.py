@@ -139,6 +139,7 @@ def test_attention_on_custom_rule(rule):
     o, lse = B.attention_forward(desc, q, k, v)
     dq, dk, dv = B.attention_backward(desc, q, k, v, o, lse, do)
     torch.cuda.synchronize()
+    assert B.cm_get_status(desc) == B.CM_OK
     for b in range(2):
         dense = _dense(pred, seg[b], int(nseg[b]), S)
         for h in range(H):
