@@ -178,6 +178,26 @@ def interval_table_bwd(wid: int, seg_row: np.ndarray, nseg: int, S: int,
     return out
 
 
+def masked_runs_table(mask: np.ndarray, nslots: int) -> np.ndarray:
+    """int32 [nslots, R, 2]: the masked form of an Interval Table, the representation the paper's
+    section 4.4 compares its visible intervals with.  For every row of the dense bool mask
+    [R, C], the maximal runs of invisible columns as half-open (start, end) in increasing order,
+    then (0, 0) padding.  Reading (the pages give no layout): same slot-major layout as the
+    visible table, with one slot more than the rule's interval count, since NI disjoint visible
+    intervals leave at most NI + 1 gaps."""
+    R, C = mask.shape
+    out = np.zeros((nslots, R, 2), dtype=np.int32)
+    for r in range(R):
+        hidden = np.concatenate(([0], (~mask[r]).astype(np.int8), [0]))
+        edges = np.diff(hidden)
+        starts = np.flatnonzero(edges == 1)
+        ends = np.flatnonzero(edges == -1)
+        assert len(starts) <= nslots, (r, len(starts), nslots)
+        out[: len(starts), r, 0] = starts
+        out[: len(starts), r, 1] = ends
+    return out
+
+
 def intervals_to_mask(table: np.ndarray, S: int) -> np.ndarray:
     """Dense bool [S, S] of the union of each row's intervals (row r, column c)."""
     c = np.arange(S)[None, :]

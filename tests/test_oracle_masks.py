@@ -263,3 +263,49 @@ def test_interval_union_equals_dense_many_seeds(wid):
             dense = M.dense_mask(wid, sb, nb, S)
             assert np.array_equal(M.intervals_to_mask(M.interval_table_fwd(wid, sb, nb, S), S), dense)
             assert np.array_equal(M.intervals_to_mask(M.interval_table_bwd(wid, sb, nb, S), S), dense.T)
+
+
+# ------------------------------------------------------------------------------------------------
+# masked form of the Interval Table (the representation of the paper's section 4.4 ablation)
+# ------------------------------------------------------------------------------------------------
+def test_masked_runs_region_c_worked_example():
+    """Hand-derived masked runs of the Region C instance (fixture), forward and backward."""
+    g = json.load(open(os.path.join(GOLDEN, "region_c_example.json")))
+    seg, nseg, S = np.array(g["seg"]), g["nseg"], g["S"]
+    dense = M.dense_mask(3, seg, nseg, S)
+    assert M.masked_runs_table(dense, 3).transpose(1, 0, 2).tolist() == g["fwd_masked_runs"]
+    assert M.masked_runs_table(dense.T, 2).transpose(1, 0, 2).tolist() == g["bwd_masked_runs"]
+
+
+def test_masked_runs_are_maximal_and_cover_the_complement():
+    """Brute force on tiny random masks: the runs are increasing, disjoint, each bounded by a
+    visible cell or an edge on both sides, and together cover exactly the invisible cells."""
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        R, C = int(rng.integers(1, 6)), int(rng.integers(1, 40))
+        mask = rng.random((R, C)) < rng.uniform(0.1, 0.9)
+        t = M.masked_runs_table(mask, C)
+        for r in range(R):
+            runs = [tuple(x) for x in t[:, r].tolist() if x != [0, 0]]
+            covered = np.zeros(C, dtype=bool)
+            prev_end = -1
+            for s, e in runs:
+                assert s < e and s > prev_end          # increasing, disjoint, not adjacent
+                assert s == 0 or mask[r, s - 1]        # maximal on the left
+                assert e == C or mask[r, e]            # maximal on the right
+                covered[s:e] = True
+                prev_end = e
+            np.testing.assert_array_equal(covered, ~mask[r])
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
+def test_masked_runs_fit_one_slot_more(wid):
+    """NI visible intervals leave at most NI + 1 masked runs per row, for every workload rule
+    (forward and backward), so the masked table has NI + 1 slots."""
+    nif, nib = M.num_intervals(wid)
+    for S in (256, 640):
+        seg, nseg = W.segments(wid, 2, S, seed=17 + wid)
+        for b in range(2):
+            dense = M.dense_mask(wid, seg[b], int(nseg[b]), S)
+            M.masked_runs_table(dense, nif + 1)      # asserts the run count fits
+            M.masked_runs_table(dense.T, nib + 1)
