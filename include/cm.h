@@ -72,6 +72,11 @@ typedef struct cm_meta {
 
 /* Execution Descriptor (section 3.3.1), forward and backward halves.  All buffers are device
  * memory allocated by the caller with the sizes from cm_descriptor_sizes.
+ *   form    CM_FORM_VISIBLE (the paper's representation): the Interval Tables hold each row's
+ *           visible intervals, ni_f / ni_b = the specs' interval counts.  CM_FORM_MASKED (the
+ *           representation section 4.4 compares it with): they hold the maximal runs of
+ *           invisible indices of each row in increasing order, ni_f / ni_b = the specs' counts
+ *           + 1.  The bitmaps and schedules are the same in both forms.
  *   itab_f  int32 [B][ni_f][S][2]  (start, end) of each visible key interval of query row i,
  *           half open; unused slots and empty intervals are (0, 0)
  *   bm_f    uint32 [B][S/tile][ceil((S/tile)/16)]  2 bits per (q-tile, k-tile):
@@ -80,9 +85,12 @@ typedef struct cm_meta {
  *   bm_b    uint32 [B][S/tile][ceil((S/tile)/16)]  (k-tile, q-tile) states
  *   sched_f int32 [B * S/tile]  forward work order: (b << 16 | q_tile), most tiles first
  *   sched_b int32 [B * S/tile]  backward work order: (b << 16 | k_tile), most tiles first
- *   status  int32 [1]           device error word, cleared by cm_build_descriptor */
+ *   status  int32 [2 + 2 * (S/tile + 1)]  device error word (first element), then the preprocess
+ *           kernel's grid barrier and schedule histograms; cleared by cm_build_descriptor */
+#define CM_FORM_VISIBLE 0
+#define CM_FORM_MASKED 1
 typedef struct cm_descriptor {
-  int32_t B, S, tile, ni_f, ni_b;
+  int32_t B, S, tile, ni_f, ni_b, form;
   int32_t* itab_f;
   uint32_t* bm_f;
   int32_t* itab_b;
@@ -116,60 +124,74 @@ CM_API int cm_spec_num_intervals(const cm_spec* spec, int* ni_max);
  * NUL-terminated string; *needed (if not NULL) receives the full length + 1.  Host only. */
 CM_API int cm_spec_describe(const cm_spec* spec, char* buf, size_t len, size_t* needed);
 
-/* CUDA C++ source of the spec's mask-specific preprocess kernel (section 3.1: the compiler
- * generates a mask-specific preprocess kernel), written to buf as a NUL-terminated string;
- * *needed (if not NULL) receives the full length + 1.  The source includes the shared kernel body
- * "descriptor_core.cuh", which the library carries in itself.  Host only. */
-CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed);
+/* CUDA C++ source of the mask-specific preprocess kernel (section 3.1: the compiler generates a
+ * mask-specific preprocess kernel) of a (forward, backward) pair of specs: their two row
+ * evaluators and the shared kernel body "descriptor_core.cuh", which the library carries in
+ * itself; one launch of it builds both halves of the descriptor and both schedules.  Written to
+ * buf as a NUL-terminated string; *needed (if not NULL) receives the full length + 1.  Host
+ * only. */
+CM_API int cm_descriptor_kernel_source(const cm_spec* fwd, const cm_spec* bwd, char* buf,
+                                       size_t len, size_t* needed);
 
-/* Whether the spec's generated kernel can run.  load = 0: compile it with NVRTC only (host only,
+/* Whether the pair's generated kernel can run.  load = 0: compile it with NVRTC only (host only,
  * no GPU needed).  load = 1: compile it and load it into the current device context, which is
- * what cm_build_descriptor does on its first call with the spec (the result, good or bad, is
- * kept per spec; compiling takes a few tenths of a second).  Returns CM_OK on success,
+ * what cm_build_descriptor does on its first call with the pair (the result, good or bad, is kept
+ * with the forward spec; compiling takes a few tenths of a second).  Returns CM_OK on success,
  * CM_ERR_UNSUPPORTED when NVRTC (libnvrtc.so.13) cannot be opened, CM_ERR_CUDA when compiling or
  * loading failed.  The NVRTC log or the failing step goes to log as a NUL-terminated string (log
  * may be NULL). */
+CM_API int cm_descriptor_kernel_status(const cm_spec* fwd, const cm_spec* bwd, int load, char* log,
+                                       size_t log_len);
+
+/* cm_descriptor_kernel_source / _status with `spec` as both the forward and the backward spec
+ * (one spec's generated code on its own). */
+CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed);
 CM_API int cm_spec_kernel_status(const cm_spec* spec, int load, char* log, size_t log_len);
 
 /* ---- online descriptor construction (sections 3.3, 3.3.1) ---------------------------------- */
 
 /* Byte sizes of the descriptor buffers, in the order itab_f, bm_f, itab_b, bm_b, sched_f,
- * sched_b, status.  tile must be 128. */
+ * sched_b, status, for the given form (CM_FORM_VISIBLE or CM_FORM_MASKED).  tile must be 128.
+ * Use the status size as given: the status word may be followed by counters of the preprocess
+ * kernel. */
 CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, int S, int tile,
-                               size_t sizes[7]);
+                               int form, size_t sizes[7]);
 
-/* Which descriptor kernels cm_build_descriptor runs, for the whole process:
- * CM_PREPROCESS_GENERATED (default): the specs' generated kernels, one launch per direction; if
- *   either spec's kernel cannot be compiled or loaded (see cm_spec_kernel_status), the generic
- *   kernel runs instead;
- * CM_PREPROCESS_GENERIC: the generic kernel, which interprets the compiled endpoint programs and
- *   builds both directions in one launch.
+/* Which descriptor kernel cm_build_descriptor runs, for the whole process:
+ * CM_PREPROCESS_GENERATED (default): the generated kernel of the (forward, backward) spec pair;
+ *   if it cannot be compiled or loaded (see cm_descriptor_kernel_status), the generic kernel runs
+ *   instead;
+ * CM_PREPROCESS_GENERIC: the generic kernel, which interprets the compiled endpoint programs.
+ * Either way one cooperative launch builds both halves and both schedules.
  * Both are GPU kernels and build identical descriptors.  Returns CM_ERR_INVALID_ARG for any other
  * mode.  Not synchronised with builds in flight on other host threads. */
 #define CM_PREPROCESS_GENERATED 0
 #define CM_PREPROCESS_GENERIC 1
 CM_API int cm_set_preprocess_mode(int mode);
 
-/* Queue the preprocess kernels that evaluate both specs against `meta` and fill `desc`.
- * desc->B, S, tile, ni_f, ni_b must match the specs and sizes; its pointers must be set.
- * Clears desc->status first.  Asynchronous on `stream`. */
+/* Queue the preprocess kernel that evaluates both specs against `meta` and fills `desc`: a
+ * memset of desc->status (the status word and the kernel's counters), then one cooperative
+ * launch (all its blocks resident at once; they meet at one grid barrier before the schedules
+ * are written).  desc->B, S, tile, form, ni_f, ni_b must match the specs and sizes; its
+ * pointers must be set.  Asynchronous on `stream`. */
 CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_meta* meta,
                                int B, int S, cm_descriptor* desc, void* stream);
 
 /* ---- descriptor-guided attention (section 3.3.2) -------------------------------------------- */
 
-/* Form of the attention kernels' partial-tile check, for the whole process (the ablation of
- * section 4.4; full and empty tiles are unaffected):
- * CM_CHECK_UNSIGNED (default): key x is visible iff (uint32)(x - s) < (uint32)(e - s) for one of
- *   the row's visible intervals [s, e): one subtraction and one comparison per interval;
- * CM_CHECK_TWO_COMPARE: visible iff s <= x && x < e for one of them;
- * CM_CHECK_MASKED: the kernels turn the row's visible intervals into the masked intervals of
- *   their complement in [0, S) (the FlashMask form) and test x against those.
- * All three give the same results.  Returns CM_ERR_INVALID_ARG for any other mode.  Not
- * synchronised with launches in flight on other host threads. */
+/* Form of the attention kernels' partial-tile check, for the whole process (full and empty
+ * tiles never run one; the forms of section 4.4's ablation plus the default):
+ * CM_CHECK_UNSIGNED: per score, for each stored interval [s, e) one subtraction and one unsigned
+ *   comparison, (uint32)(x - s) < (uint32)(e - s) (the paper's test);
+ * CM_CHECK_TWO_COMPARE: per score, s <= x && x < e for each stored interval;
+ * CM_CHECK_RANGE_MASK (default): per row and 32 indices, each stored interval becomes a range
+ *   of bits of a 32-bit mask (clamped unsigned differences), and each score tests one bit.
+ * With a CM_FORM_MASKED descriptor an index is visible iff it lies in none of the stored
+ * intervals.  All forms give the same results.  Returns CM_ERR_INVALID_ARG for any other mode.
+ * Not synchronised with launches in flight on other host threads. */
 #define CM_CHECK_UNSIGNED 0
 #define CM_CHECK_TWO_COMPARE 1
-#define CM_CHECK_MASKED 2
+#define CM_CHECK_RANGE_MASK 3
 CM_API int cm_set_interval_check(int mode);
 
 /* Forward: o = softmax(scale * q k^T masked by desc) v; lse = natural-log row sums.

@@ -40,7 +40,7 @@ class cm_meta(ctypes.Structure):
 
 class cm_descriptor(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("tile", ctypes.c_int32),
-                ("ni_f", ctypes.c_int32), ("ni_b", ctypes.c_int32),
+                ("ni_f", ctypes.c_int32), ("ni_b", ctypes.c_int32), ("form", ctypes.c_int32),
                 ("itab_f", ctypes.c_void_p), ("bm_f", ctypes.c_void_p),
                 ("itab_b", ctypes.c_void_p), ("bm_b", ctypes.c_void_p),
                 ("sched_f", ctypes.c_void_p), ("sched_b", ctypes.c_void_p),
@@ -66,9 +66,11 @@ def lib() -> ctypes.CDLL:
         L.cm_spec_describe.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
         L.cm_spec_kernel_source.argtypes = [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
         L.cm_spec_kernel_status.argtypes = [vp, i32, ctypes.c_char_p, sz]
+        L.cm_descriptor_kernel_source.argtypes = [vp, vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]
+        L.cm_descriptor_kernel_status.argtypes = [vp, vp, i32, ctypes.c_char_p, sz]
         L.cm_set_preprocess_mode.argtypes = [i32]
         L.cm_set_interval_check.argtypes = [i32]
-        L.cm_descriptor_sizes.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(sz)]
+        L.cm_descriptor_sizes.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
         L.cm_build_descriptor.argtypes = [vp, vp, ctypes.POINTER(cm_meta), i32, i32,
                                           ctypes.POINTER(cm_descriptor), vp]
         L.cm_attn_fwd.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp,
@@ -157,6 +159,25 @@ def cm_spec_kernel_source(spec: Spec) -> str:
     return buf.value.decode()
 
 
+def cm_descriptor_kernel_source(fwd: Spec, bwd: Spec) -> str:
+    """CUDA C++ source of the mask-specific preprocess kernel of a (forward, backward) pair."""
+    need = ctypes.c_size_t()
+    _check(lib().cm_descriptor_kernel_source(fwd.handle, bwd.handle, None, 0, ctypes.byref(need)),
+           "cm_descriptor_kernel_source")
+    buf = ctypes.create_string_buffer(need.value)
+    _check(lib().cm_descriptor_kernel_source(fwd.handle, bwd.handle, buf, need.value, None),
+           "cm_descriptor_kernel_source")
+    return buf.value.decode()
+
+
+def cm_descriptor_kernel_status(fwd: Spec, bwd: Spec, load: bool = True) -> tuple[int, str]:
+    """(code, log) of the pair's generated kernel: compiled (load=False, host only) or compiled
+    and loaded on the current GPU (load=True), as cm_build_descriptor does on first use."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    rc = lib().cm_descriptor_kernel_status(fwd.handle, bwd.handle, 1 if load else 0, buf, len(buf))
+    return rc, buf.value.decode(errors="replace")
+
+
 def cm_spec_kernel_status(spec: Spec, load: bool = True) -> tuple[int, str]:
     """(code, log): CM_OK when the spec's generated preprocess kernel compiles (load=False, host
     only) or compiles and loads on the current GPU (load=True); otherwise the code and the reason."""
@@ -176,18 +197,23 @@ def cm_set_preprocess_mode(mode: int) -> None:
 
 CM_CHECK_UNSIGNED = 0
 CM_CHECK_TWO_COMPARE = 1
-CM_CHECK_MASKED = 2
+CM_CHECK_RANGE_MASK = 3
+
+CM_FORM_VISIBLE = 0
+CM_FORM_MASKED = 1
 
 
 def cm_set_interval_check(mode: int) -> None:
-    """Process-wide form of the attention kernels' partial-tile check (the paper's section 4.4
-    ablation): unsigned visible-interval test (default), two comparisons, or masked intervals."""
+    """Process-wide form of the attention kernels' partial-tile check: per-row range masks
+    (default), or per score the unsigned test or two comparisons (the paper's section 4.4
+    forms)."""
     _check(lib().cm_set_interval_check(mode), "cm_set_interval_check")
 
 
-def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE) -> list[int]:
+def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE,
+                        form: int = CM_FORM_VISIBLE) -> list[int]:
     sizes = (ctypes.c_size_t * 7)()
-    _check(lib().cm_descriptor_sizes(fwd.handle, bwd.handle, B, S, tile, sizes),
+    _check(lib().cm_descriptor_sizes(fwd.handle, bwd.handle, B, S, tile, form, sizes),
            "cm_descriptor_sizes")
     return list(sizes)
 
@@ -196,12 +222,15 @@ def cm_descriptor_sizes(fwd: Spec, bwd: Spec, B: int, S: int, tile: int = TILE) 
 # descriptor
 # ------------------------------------------------------------------------------------------------
 class Descriptor:
-    """Device buffers of an Execution Descriptor, allocated with torch on ``device``."""
+    """Device buffers of an Execution Descriptor, allocated with torch on ``device``.  ``form``:
+    CM_FORM_VISIBLE (visible intervals per row) or CM_FORM_MASKED (the masked runs)."""
 
-    def __init__(self, fwd: Spec, bwd: Spec, B: int, S: int, device="cuda"):
-        sizes = cm_descriptor_sizes(fwd, bwd, B, S)
-        self.fwd, self.bwd, self.B, self.S = fwd, bwd, B, S
-        self.ni_f, self.ni_b = cm_spec_num_intervals(fwd), cm_spec_num_intervals(bwd)
+    def __init__(self, fwd: Spec, bwd: Spec, B: int, S: int, device="cuda",
+                 form: int = CM_FORM_VISIBLE):
+        sizes = cm_descriptor_sizes(fwd, bwd, B, S, form=form)
+        self.fwd, self.bwd, self.B, self.S, self.form = fwd, bwd, B, S, form
+        self.ni_f = cm_spec_num_intervals(fwd) + form
+        self.ni_b = cm_spec_num_intervals(bwd) + form
         self.NT = S // TILE
         self.W = (self.NT + 15) // 16
         self.itab_f = torch.empty(sizes[0] // 4, dtype=torch.int32, device=device)
@@ -210,8 +239,8 @@ class Descriptor:
         self.bm_b = torch.empty(sizes[3] // 4, dtype=torch.int32, device=device)
         self.sched_f = torch.empty(sizes[4] // 4, dtype=torch.int32, device=device)
         self.sched_b = torch.empty(sizes[5] // 4, dtype=torch.int32, device=device)
-        self.status = torch.zeros(4, dtype=torch.int32, device=device)
-        self.c = cm_descriptor(B, S, TILE, self.ni_f, self.ni_b,
+        self.status = torch.zeros((sizes[6] + 3) // 4, dtype=torch.int32, device=device)
+        self.c = cm_descriptor(B, S, TILE, self.ni_f, self.ni_b, form,
                                self.itab_f.data_ptr(), self.bm_f.data_ptr(),
                                self.itab_b.data_ptr(), self.bm_b.data_ptr(),
                                self.sched_f.data_ptr(), self.sched_b.data_ptr(),
@@ -219,7 +248,7 @@ class Descriptor:
 
     def nbytes(self) -> int:
         return sum(t.numel() * 4 for t in (self.itab_f, self.bm_f, self.itab_b, self.bm_b,
-                                           self.sched_f, self.sched_b)) + 4
+                                           self.sched_f, self.sched_b, self.status))
 
     # host views for checking
     def interval_table_fwd(self):

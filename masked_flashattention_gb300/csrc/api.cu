@@ -22,7 +22,7 @@ constexpr int kMaxS = 131072;
 // which descriptor kernels cm_build_descriptor runs (cm_set_preprocess_mode)
 std::atomic<int> g_preprocess_mode{CM_PREPROCESS_GENERATED};
 // form of the attention kernels' partial-tile check (cm_set_interval_check)
-std::atomic<int> g_interval_check{CM_CHECK_UNSIGNED};
+std::atomic<int> g_interval_check{CM_CHECK_RANGE_MASK};
 // limit of each bounded wait inside the attention kernels (cm_set_wait_limit_ns)
 std::atomic<uint64_t> g_wait_limit_ns{cm::kDefaultWaitLimitNs};
 constexpr unsigned long long kMaxWaitLimitNs = 60ull * 1000000000ull;
@@ -39,7 +39,9 @@ int check_shape(int B, int S) {
 int check_desc(const cm_descriptor* d, int B, int S) {
   if (!d) return CM_ERR_INVALID_ARG;
   if (d->B != B || d->S != S || d->tile != kTile) return CM_ERR_INVALID_ARG;
-  if (d->ni_f < 1 || d->ni_f > cm::kMaxSlots || d->ni_b < 1 || d->ni_b > cm::kMaxSlots)
+  if (d->form != CM_FORM_VISIBLE && d->form != CM_FORM_MASKED) return CM_ERR_INVALID_ARG;
+  const int max_stored = cm::kMaxSlots + d->form;
+  if (d->ni_f < 1 || d->ni_f > max_stored || d->ni_b < 1 || d->ni_b > max_stored)
     return CM_ERR_INVALID_ARG;
   if (!d->itab_f || !d->bm_f || !d->itab_b || !d->bm_b || !d->sched_f || !d->sched_b || !d->status)
     return CM_ERR_INVALID_ARG;
@@ -100,27 +102,29 @@ CM_API const char* cm_error_string(int code) {
 }
 
 CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, int S, int tile,
-                               size_t sizes[7]) {
+                               int form, size_t sizes[7]) {
   if (!fwd || !bwd || !sizes) return CM_ERR_INVALID_ARG;
+  if (form != CM_FORM_VISIBLE && form != CM_FORM_MASKED) return CM_ERR_INVALID_ARG;
   if (tile != kTile) return CM_ERR_UNSUPPORTED;
   const int rc = check_shape(B, S);
   if (rc != CM_OK) return rc;
   const size_t NT = static_cast<size_t>(S / kTile);
   const size_t W = (NT + 15) / 16;
-  const size_t nif = static_cast<size_t>(cm::spec_program(fwd)->ni);
-  const size_t nib = static_cast<size_t>(cm::spec_program(bwd)->ni);
+  // stored slots per row: the spec's interval count, or one more for the masked runs
+  const size_t nif = static_cast<size_t>(cm::spec_program(fwd)->ni + form);
+  const size_t nib = static_cast<size_t>(cm::spec_program(bwd)->ni + form);
   sizes[0] = static_cast<size_t>(B) * nif * S * 8;
   sizes[1] = static_cast<size_t>(B) * NT * W * 4;
   sizes[2] = static_cast<size_t>(B) * nib * S * 8;
   sizes[3] = static_cast<size_t>(B) * NT * W * 4;
   sizes[4] = static_cast<size_t>(B) * NT * 4;
   sizes[5] = static_cast<size_t>(B) * NT * 4;
-  sizes[6] = 4;
+  sizes[6] = static_cast<size_t>(2 + 2 * (NT + 1)) * 4;  // status, barrier, histograms
   return CM_OK;
 }
 
 CM_API int cm_set_interval_check(int mode) {
-  if (mode != CM_CHECK_UNSIGNED && mode != CM_CHECK_TWO_COMPARE && mode != CM_CHECK_MASKED)
+  if (mode != CM_CHECK_UNSIGNED && mode != CM_CHECK_TWO_COMPARE && mode != CM_CHECK_RANGE_MASK)
     return CM_ERR_INVALID_ARG;
   g_interval_check.store(mode);
   return CM_OK;
@@ -140,21 +144,20 @@ CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_
   if (rc != CM_OK) return rc;
   rc = check_desc(desc, B, S);
   if (rc != CM_OK) return rc;
-  if (desc->ni_f != cm::spec_program(fwd)->ni || desc->ni_b != cm::spec_program(bwd)->ni)
+  if (desc->ni_f != cm::spec_program(fwd)->ni + desc->form ||
+      desc->ni_b != cm::spec_program(bwd)->ni + desc->form)
     return CM_ERR_INVALID_ARG;
   if (meta->nseg_max > 16384) return CM_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(desc->status, 0, 4, st) != cudaSuccess) return CM_ERR_CUDA;
-  const void* gen_f = nullptr;
-  const void* gen_b = nullptr;
-  if (g_preprocess_mode.load() == CM_PREPROCESS_GENERATED) {
-    gen_f = cm::spec_generated_kernel(fwd);
-    gen_b = gen_f != nullptr ? cm::spec_generated_kernel(bwd) : nullptr;
-  }
-  if (cm::launch_descriptor(*cm::spec_program(fwd), *cm::spec_program(bwd), gen_f, gen_b,
-                            meta->seg, meta->nseg, meta->nseg_max, B, S, desc->itab_f, desc->bm_f,
+  const size_t work_bytes = static_cast<size_t>(2 + 2 * (S / kTile + 1)) * 4;
+  if (cudaMemsetAsync(desc->status, 0, work_bytes, st) != cudaSuccess) return CM_ERR_CUDA;
+  const void* gen = g_preprocess_mode.load() == CM_PREPROCESS_GENERATED
+                        ? cm::pair_generated_kernel(fwd, bwd)
+                        : nullptr;
+  if (cm::launch_descriptor(*cm::spec_program(fwd), *cm::spec_program(bwd), gen, meta->seg,
+                            meta->nseg, meta->nseg_max, B, S, desc->itab_f, desc->bm_f,
                             desc->itab_b, desc->bm_b, desc->sched_f, desc->sched_b, desc->status,
-                            st) != 0)
+                            desc->form, cm::kDefaultWaitLimitNs, st) != 0)
     return CM_ERR_CUDA;
   return CM_OK;
 }
@@ -186,6 +189,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.W = (p.NT + 15) / 16;
   p.NI = desc->ni_f;
   p.check = g_interval_check.load();
+  p.masked = desc->form;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_limit_ns.load();
   return cm::launch_attn_fwd(p, d, q, k, v, static_cast<cudaStream_t>(stream)) == 0
@@ -246,6 +250,7 @@ CM_API int cm_attn_bwd_dkdv(const cm_descriptor* desc, const void* q, const void
   p.W = (p.NT + 15) / 16;
   p.NI = desc->ni_b;
   p.check = g_interval_check.load();
+  p.masked = desc->form;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_limit_ns.load();
@@ -280,6 +285,7 @@ CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* 
   g.W = (g.NT + 15) / 16;
   g.NI = desc->ni_f;
   g.check = g_interval_check.load();
+  g.masked = desc->form;
   g.scale = scale;
   g.scale_log2 = scale * 1.4426950408889634f;
   g.wait_ns = g_wait_limit_ns.load();

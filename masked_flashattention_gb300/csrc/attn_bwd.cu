@@ -154,7 +154,7 @@ __device__ __forceinline__ void ds_chunk(const float (&pf)[32], const uint32_t (
   }
 }
 
-template <int D>
+template <int D, int MAXNI>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -180,6 +180,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int item = p.sched[item_idx];
   const int b = item >> 16;
   const int kt = item & 0xFFFF;
+  if (b < 0 || b >= p.B || kt >= p.NT) {  // a schedule entry that no descriptor build wrote
+    if (threadIdx.x == 0) set_status(p.status, kDevBadSchedule, item_idx);
+    return;
+  }
   const int bh = b * p.H + h;
 
   if (threadIdx.x == 0) {
@@ -351,8 +355,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, kDevDescMismatch, kt);
     }
-    RowIntervals ri;
-    load_row_intervals(p.itab, b, p.NI, p.S, j, p.check, ri);
+    RowIntervals<MAXNI> ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, j, ri);
     const float sl2 = p.scale_log2;
     bool ok = true;
     int qt = next_tile(bmrow, p.NT, 0);
@@ -379,7 +383,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           p_chunk<true>(sr, lse2_base + q0 * 4u, sl2, 0u, pf[ch], pp);
         } else {
           const int i0 = qt * 128 + q0;
-          const uint32_t vis = visible_bits_any(i0, ri, p.NI, p.check);
+          const uint32_t vis = visible_bits_any(i0, ri, p.NI, p.check, p.masked != 0);
           p_chunk<false>(sr, lse2_base + q0 * 4u, sl2, vis, pf[ch], pp);
         }
         // P^T pairs into X columns this warp has already read: hf * 64 + ch * 16
@@ -518,6 +522,16 @@ int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse,
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+template <int D, int MAXNI>
+int bwd_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, const BwdParams& p) {
+  const uint32_t smem = bwd::Smem<D>::kAlloc;
+  if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<D, MAXNI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return -1;
+  bwd::attn_bwd_kernel<D, MAXNI><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, const void* v,
                      const void* d_o, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
@@ -526,20 +540,13 @@ int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, co
       !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
     return -1;
   const dim3 grid(p.B * p.NT * p.H);
+  // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
-    const uint32_t smem = bwd::Smem<128>::kAlloc;
-    if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
-  } else {
-    const uint32_t smem = bwd::Smem<64>::kAlloc;
-    if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (p.NI <= 4) return bwd_launch<128, 4>(grid, stream, mq, mk, mv, mdo, p);
+    return bwd_launch<128, 9>(grid, stream, mq, mk, mv, mdo, p);
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  if (p.NI <= 4) return bwd_launch<64, 4>(grid, stream, mq, mk, mv, mdo, p);
+  return bwd_launch<64, 9>(grid, stream, mq, mk, mv, mdo, p);
 }
 
 }  // namespace cm

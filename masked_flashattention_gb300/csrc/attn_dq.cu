@@ -72,7 +72,7 @@ enum {
 };
 
 
-template <int D>
+template <int D, int MAXNI>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -98,6 +98,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int item = p.sched[item_idx];
   const int b = item >> 16;
   const int qt = item & 0xFFFF;
+  if (b < 0 || b >= p.B || qt >= p.NT) {  // a schedule entry that no descriptor build wrote
+    if (threadIdx.x == 0) set_status(p.status, kDevBadSchedule, item_idx);
+    return;
+  }
   const int bh = b * p.H + h;
   const int row0 = bh * p.S;
 
@@ -238,8 +242,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    RowIntervals ri;
-    load_row_intervals(p.itab, b, p.NI, p.S, i, p.check, ri);
+    RowIntervals<MAXNI> ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, i, ri);
     // per-row constants from the backward prologue: -LSE * log2(e) (-inf for a row that sees
     // nothing) and -D
     const float lse2 = p.lse2[static_cast<size_t>(row0) + i];
@@ -269,7 +273,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
       if (!tile_is_full(bmrow, kt)) {
         const int j0 = kt * 128 + 64 * hf;
-        mask_cols_any(pf, j0, ri, p.NI, p.check);
+        mask_cols_any(pf, j0, ri, p.NI, p.check, p.masked != 0);
       }
       // P = exp2(s * scale*log2e - LSE*log2e); masked scores are -inf and give 0
 #pragma unroll
@@ -357,6 +361,16 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
 }  // namespace dq
 
+template <int D, int MAXNI>
+int dq_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, const DqParams& p) {
+  const uint32_t smem = dq::Smem<D>::kAlloc;
+  if (cudaFuncSetAttribute(dq::attn_dq_kernel<D, MAXNI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return -1;
+  dq::attn_dq_kernel<D, MAXNI><<<grid, dq::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_attn_dq(const DqParams& p, int d, const void* q, const void* k, const void* v,
                    const void* d_o, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
@@ -365,20 +379,13 @@ int launch_attn_dq(const DqParams& p, int d, const void* q, const void* k, const
       !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
     return -1;
   const dim3 grid(p.B * p.NT * p.H);
+  // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
-    const uint32_t smem = dq::Smem<128>::kAlloc;
-    if (cudaFuncSetAttribute(dq::attn_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    dq::attn_dq_kernel<128><<<grid, dq::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
-  } else {
-    const uint32_t smem = dq::Smem<64>::kAlloc;
-    if (cudaFuncSetAttribute(dq::attn_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    dq::attn_dq_kernel<64><<<grid, dq::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+    if (p.NI <= 4) return dq_launch<128, 4>(grid, stream, mq, mk, mv, mdo, p);
+    return dq_launch<128, 9>(grid, stream, mq, mk, mv, mdo, p);
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  if (p.NI <= 4) return dq_launch<64, 4>(grid, stream, mq, mk, mv, mdo, p);
+  return dq_launch<64, 9>(grid, stream, mq, mk, mv, mdo, p);
 }
 
 }  // namespace cm

@@ -80,7 +80,7 @@ enum {
   B_COUNT = 17
 };
 
-template <int D>
+template <int D, int MAXNI>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
@@ -105,6 +105,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int item = p.sched[item_idx];
   const int b = item >> 16;
   const int qt = item & 0xFFFF;
+  if (b < 0 || b >= p.B || qt >= p.NT) {  // a schedule entry that no descriptor build wrote
+    if (threadIdx.x == 0) set_status(p.status, kDevBadSchedule, item_idx);
+    return;
+  }
   const int bh = b * p.H + h;
 
   // ---- set-up: barriers, bitmap row, TMEM ---------------------------------------------------
@@ -239,8 +243,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t my_o = tmem + lane_off + kColO + 128 * hf;
-    RowIntervals ri;
-    load_row_intervals(p.itab, b, p.NI, p.S, i, p.check, ri);
+    RowIntervals<MAXNI> ri;
+    load_row_intervals(p.itab, b, p.NI, p.S, i, ri);
     bool ok = nt > 0;
     float m_run = -INFINITY;  // this half's running max (log2 domain)
     float l_run = 0.f;        // this half's running row sum
@@ -267,7 +271,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (!tile_is_full(bmrow, kt)) {
         const int j0 = kt * 128 + 64 * hf;
-        mask_cols_any(s, j0, ri, p.NI, p.check);
+        mask_cols_any(s, j0, ri, p.NI, p.check, p.masked != 0);
       }
       // row max of the 64 scores as a tree of 3-input maxima (depth 4: 64 -> 22 -> 8 -> 3 -> 1),
       // so the two softmax warps of an SMSP do not wait on one long dependent chain
@@ -412,6 +416,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 }  // namespace fwd
 
+template <int D, int MAXNI>
+int fwd_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p) {
+  const uint32_t smem = fwd::Smem<D>::kAlloc;
+  if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D, MAXNI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return -1;
+  fwd::attn_fwd_kernel<D, MAXNI><<<grid, fwd::kThreads, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
@@ -420,20 +434,13 @@ int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, con
       !make_bf16_tile_map(&mv, v, rows, d))
     return -1;
   const dim3 grid(p.B * p.NT * p.H);
+  // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
-    const uint32_t smem = fwd::Smem<128>::kAlloc;
-    if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    fwd::attn_fwd_kernel<128><<<grid, fwd::kThreads, smem, stream>>>(mq, mk, mv, p);
-  } else {
-    const uint32_t smem = fwd::Smem<64>::kAlloc;
-    if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return -1;
-    fwd::attn_fwd_kernel<64><<<grid, fwd::kThreads, smem, stream>>>(mq, mk, mv, p);
+    if (p.NI <= 4) return fwd_launch<128, 4>(grid, stream, mq, mk, mv, p);
+    return fwd_launch<128, 9>(grid, stream, mq, mk, mv, p);
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  if (p.NI <= 4) return fwd_launch<64, 4>(grid, stream, mq, mk, mv, p);
+  return fwd_launch<64, 9>(grid, stream, mq, mk, mv, p);
 }
 
 }  // namespace cm

@@ -25,8 +25,10 @@
 #include <climits>
 #include <cstdio>
 #include <cstring>
+#include <list>
 #include <map>
 #include <memory>
+#include <atomic>
 #include <mutex>
 #include <sstream>
 #include <stdexcept>
@@ -785,16 +787,46 @@ std::string bstr(const BP& b) {
 // ---------------------------------------------------------------------------------------------
 // the compiled spec
 // ---------------------------------------------------------------------------------------------
+// The mask-specific kernel of one (forward, backward) pair, compiled and loaded once, on first use.
+struct PairKernel {
+  uint64_t bwd_serial = 0;
+  const void* kernel = nullptr;
+  int rc = CM_OK;          // why kernel is null, if it is
+  std::string log;
+};
+
 struct SpecImpl {
   DevProg prog;
+  uint64_t serial = 0;     // identifies the spec in the pair cache of other specs
   std::string text;        // describe() output
-  std::string gen;         // CUDA C++ source of the mask-specific preprocess kernel
-  std::mutex mu;           // guards the four fields below
-  bool gen_tried = false;  // compiled and loaded once, on first use
-  const void* gen_kernel = nullptr;
-  int gen_rc = CM_OK;      // why gen_kernel is null, if it is
-  std::string gen_log;
+  std::string gen;         // body of the row evaluator of the mask-specific kernel (CUDA C++)
+  std::mutex mu;           // guards `pairs`
+  std::list<PairKernel> pairs;  // kernels with this spec as the forward one (stable addresses)
 };
+
+std::atomic<uint64_t> g_spec_serial{1};
+
+// CUDA C++ of a row evaluator struct named `name`.
+std::string evaluator_source(const SpecImpl& s, const std::string& name) {
+  return "struct " + name + " {\n"
+         "  __device__ __forceinline__ void row(int i, int ki, const int* seg, int nseg, int S,\n"
+         "                                      int* lo, int* hi) const {\n"
+         "    (void)i; (void)ki; (void)seg; (void)nseg; (void)S; (void)lo; (void)hi;\n" +
+         s.gen + "  }\n};\n";
+}
+
+// Source of the mask-specific preprocess kernel of a (forward, backward) pair of specs: the two
+// row evaluators and the shared kernel body, one launch for both halves of the descriptor.
+std::string pair_source(const SpecImpl& f, const SpecImpl& b) {
+  return "// Mask-specific preprocess kernel generated from a forward and a backward MaskSpec.\n"
+         "#include \"descriptor_core.cuh\"\n" +
+         evaluator_source(f, "EvalFwd") + evaluator_source(b, "EvalBwd") +
+         "extern \"C\" __global__ void __launch_bounds__(cmcore::kThreads)\n"
+         "cm_generated_descriptor(const __grid_constant__ cmcore::DescCore p) {\n"
+         "  cmcore::descriptor_kernel<" + std::to_string(f.prog.ni) + ", " +
+         std::to_string(b.prog.ni) + ">(p, EvalFwd(), EvalBwd());\n"
+         "}\n";
+}
 
 static int compile(const char* text, SpecImpl& out) {
   std::istringstream in(text);
@@ -928,26 +960,13 @@ static int compile(const char* text, SpecImpl& out) {
   P.nreg = nreg;
   for (size_t q = 0; q < em.code.size(); ++q) P.code[q] = em.code[q];
   out.text = "intervals " + std::to_string(P.ni) + "\n" + desc.str();
-  out.gen =
-      "// Mask-specific preprocess kernel generated from a MaskSpec.\n"
-      "#include \"descriptor_core.cuh\"\n"
-      "struct GenEval {\n"
-      "  __device__ __forceinline__ void row(int i, int ki, const int* seg, int nseg, int S,\n"
-      "                                      int* lo, int* hi) const {\n"
-      "    (void)i; (void)ki; (void)seg; (void)nseg; (void)S;\n" +
-      gen.str() +
-      "  }\n"
-      "};\n"
-      "extern \"C\" __global__ void __launch_bounds__(128)\n"
-      "cm_generated_descriptor(const __grid_constant__ cmcore::DescCore p) {\n"
-      "  cmcore::descriptor_tile<" + std::to_string(P.ni) +
-      ">(p, blockIdx.x / p.NT, blockIdx.x % p.NT, GenEval());\n"
-      "}\n";
+  out.gen = gen.str();
+  out.serial = g_spec_serial.fetch_add(1);
   return CM_OK;
 }
 
 const DevProg* spec_program(const cm_spec* s);
-const void* spec_generated_kernel(const cm_spec* s);
+const void* pair_generated_kernel(const cm_spec* fwd, const cm_spec* bwd);
 int compile_generated_kernel(const std::string& source, std::vector<char>* cubin, std::string* log);
 int load_generated_kernel(const std::string& source, const void** kernel, std::string* log);
 
@@ -959,14 +978,21 @@ struct cm_spec {
 
 const cm::DevProg* cm::spec_program(const cm_spec* s) { return &s->impl.prog; }
 
-const void* cm::spec_generated_kernel(const cm_spec* s) {
-  cm::SpecImpl& im = const_cast<cm_spec*>(s)->impl;
+// The pair's entry in the forward spec's cache, compiled and loaded on first use.
+static const cm::PairKernel& pair_kernel(const cm_spec* fwd, const cm_spec* bwd) {
+  cm::SpecImpl& im = const_cast<cm_spec*>(fwd)->impl;
   std::lock_guard<std::mutex> lock(im.mu);
-  if (!im.gen_tried) {
-    im.gen_tried = true;
-    im.gen_rc = cm::load_generated_kernel(im.gen, &im.gen_kernel, &im.gen_log);
-  }
-  return im.gen_kernel;
+  for (const cm::PairKernel& e : im.pairs)
+    if (e.bwd_serial == bwd->impl.serial) return e;
+  im.pairs.emplace_back();
+  cm::PairKernel& e = im.pairs.back();
+  e.bwd_serial = bwd->impl.serial;
+  e.rc = cm::load_generated_kernel(cm::pair_source(fwd->impl, bwd->impl), &e.kernel, &e.log);
+  return e;
+}
+
+const void* cm::pair_generated_kernel(const cm_spec* fwd, const cm_spec* bwd) {
+  return pair_kernel(fwd, bwd).kernel;
 }
 
 extern "C" {
@@ -995,31 +1021,39 @@ CM_API int cm_spec_num_intervals(const cm_spec* spec, int* ni_max) {
   return CM_OK;
 }
 
-CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed) {
-  if (!spec) return CM_ERR_INVALID_ARG;
-  const std::string& t = spec->impl.gen;
+CM_API int cm_descriptor_kernel_source(const cm_spec* fwd, const cm_spec* bwd, char* buf,
+                                       size_t len, size_t* needed) {
+  if (!fwd || !bwd) return CM_ERR_INVALID_ARG;
+  const std::string t = cm::pair_source(fwd->impl, bwd->impl);
   if (needed) *needed = t.size() + 1;
   if (buf && len) std::snprintf(buf, len, "%s", t.c_str());
   return CM_OK;
 }
 
-CM_API int cm_spec_kernel_status(const cm_spec* spec, int load, char* log, size_t log_len) {
+CM_API int cm_descriptor_kernel_status(const cm_spec* fwd, const cm_spec* bwd, int load, char* log,
+                                       size_t log_len) {
   if (log && log_len) log[0] = 0;
-  if (!spec) return CM_ERR_INVALID_ARG;
+  if (!fwd || !bwd) return CM_ERR_INVALID_ARG;
   int rc;
   std::string text;
   if (load) {
-    cm::spec_generated_kernel(spec);
-    cm::SpecImpl& im = const_cast<cm_spec*>(spec)->impl;
-    std::lock_guard<std::mutex> lock(im.mu);
-    rc = im.gen_rc;
-    text = im.gen_log;
+    const cm::PairKernel& e = pair_kernel(fwd, bwd);
+    rc = e.rc;
+    text = e.log;
   } else {
     std::vector<char> cubin;
-    rc = cm::compile_generated_kernel(spec->impl.gen, &cubin, &text);
+    rc = cm::compile_generated_kernel(cm::pair_source(fwd->impl, bwd->impl), &cubin, &text);
   }
   if (log && log_len) std::snprintf(log, log_len, "%s", text.c_str());
   return rc;
+}
+
+CM_API int cm_spec_kernel_source(const cm_spec* spec, char* buf, size_t len, size_t* needed) {
+  return cm_descriptor_kernel_source(spec, spec, buf, len, needed);
+}
+
+CM_API int cm_spec_kernel_status(const cm_spec* spec, int load, char* log, size_t log_len) {
+  return cm_descriptor_kernel_status(spec, spec, load, log, log_len);
 }
 
 CM_API int cm_spec_describe(const cm_spec* spec, char* buf, size_t len, size_t* needed) {

@@ -1,21 +1,30 @@
-// Body of the online preprocess kernel for one direction of the Execution Descriptor
-// (CompileMask sections 3.3 and 3.3.1).  It is shared by two kernels that differ only in the row
-// evaluator, a template parameter:
+// Body of the online preprocess kernel (CompileMask sections 3.3 and 3.3.1): one launch builds
+// both halves of the Execution Descriptor (forward: query rows; backward: key columns) and their
+// longest-first schedules.  It is shared by two kernels that differ only in their row evaluators
+// (template parameters):
 //   - the generic kernel, which interprets the compiled endpoint programs, and
-//   - the mask-specific kernels that the compiler generates from a MaskSpec and NVRTC builds at
-//     run time (section 3.1: the compiler generates a mask-specific preprocess kernel).
+//   - the mask-specific kernels that the compiler generates from a pair of MaskSpecs and NVRTC
+//     builds at run time (section 3.1: the compiler generates a mask-specific preprocess kernel).
 //
-// One block covers one 128-row tile of one sample; thread t owns row tile*128 + t:
+// Work is split into units of 4 tile rows (4 x 128 rows) of one (direction, sample); a block of
+// 4 warps takes units in turn (the grid is sized to be resident at once and launched
+// cooperatively).  Warp w of a unit owns one tile row, lane l its rows 4l .. 4l + 3:
 //   1. the sample's segment boundaries are staged in shared memory and validated;
-//   2. the evaluator gives each slot's raw endpoints; they are clamped to [0, S] and stored as
-//      (start, end), with (0, 0) for padding, failed conditions and empty intervals; stores are
-//      8-byte and coalesced (slot-major layout [b][slot][row]);
-//   3. tile states: each row adds its touched tile ranges ("any") and the tile ranges its merged
-//      intervals cover completely ("all") to two shared-memory difference arrays; a prefix sum
-//      over the tiles gives, per tile, empty (no row touches it), full (all 128 rows cover it)
-//      or partial.  A union of adjacent or overlapping slots counts as covering, so the states
-//      equal those of the dense mask exactly;
-//   4. the tile row's count of non-empty tiles goes to `rowcnt`, the input of the schedule.
+//   2. the evaluator gives each slot's raw endpoints per row; they are clamped to [0, S] and kept
+//      as (start, end), with (0, 0) for padding, failed conditions and empty intervals.  The
+//      visible form stores them as they are, the masked form the maximal runs of invisible
+//      indices; either way a lane writes each slot's 4 rows with two 16-byte stores (slot-major
+//      layout [b][slot][row], so a warp's stores cover 1 KB contiguously);
+//   3. tile states: each row's touched tile ranges (any slot) and fully covered tile ranges
+//      (merged intervals) go into one shared-memory difference array per warp, touched counts in
+//      the low 16 bits and covered counts in the high 16 bits.  Lanes whose 4 rows agree and share
+//      a range with other lanes add it once for all of them.  A prefix sum over the tiles gives,
+//      per tile, empty (no row touches it), full (all 128 rows cover it) or partial.  A union of
+//      adjacent or overlapping slots counts as covering, so the states equal the dense mask's;
+//   4. the tile row's count of non-empty tiles takes a ticket in a global histogram per
+//      direction.  After a grid barrier every block reads the histogram, and each tile row is
+//      placed at (rows with more tiles) + ticket: a counting sort, longest first, ties in any
+//      order.
 //
 // NVRTC compiles this header too, so it includes no standard-library header there.
 #pragma once
@@ -24,6 +33,7 @@
 typedef int int32_t;
 typedef unsigned int uint32_t;
 typedef unsigned char uint8_t;
+typedef unsigned long long uint64_t;
 #else
 #include <cstdint>
 #endif
@@ -31,18 +41,34 @@ typedef unsigned char uint8_t;
 namespace cmcore {
 
 constexpr int kTile = 128;
-constexpr int kSlots = 4;          // most slots a row can have (the compiler's limit)
-constexpr int kStatusBadMeta = 2;  // device status code: segment metadata failed validation
+constexpr int kSlots = 8;          // most slots a row can have (the compiler's limit)
+constexpr int kWarps = 4;          // tile rows per work unit, warps per block
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRowsPerLane = kTile / 32;
+constexpr int kStatusTimeout = 1;  // device status codes (first error wins)
+constexpr int kStatusBadMeta = 2;
+constexpr int kNone = 0x7FFFFFFF;
 
-// Kernel parameters of one direction (forward: query rows; backward: key columns).
+// One half of the descriptor.
+struct DescDir {
+  int32_t* itab;   // [B][ni][S][2]
+  uint32_t* bm;    // [B][NT][W]
+  int32_t* sched;  // [B * NT]
+  int ni;          // stored slots per row: the spec's slots (visible form) or one more (masked)
+};
+
+// Kernel parameters.
 struct DescCore {
-  int32_t* itab;        // [B][ni][S][2]
-  uint32_t* bm;         // [B][NT][W]
-  int32_t* rowcnt;      // [B][NT] non-empty tiles per tile row
-  const int32_t* seg;   // [B][nseg_max + 1]
-  const int32_t* nseg;  // [B]
-  int32_t* status;      // device error word (first error wins)
-  int nseg_max, B, S, NT, W, ni, dir;
+  DescDir dir[2];        // 0 forward, 1 backward
+  const int32_t* seg;    // [B][nseg_max + 1]
+  const int32_t* nseg;   // [B]
+  int32_t* work;         // zeroed before the launch: [0] status word, [1] grid barrier count,
+                         // [2 + d * (NT + 1) + c] tile rows of direction d with c non-empty tiles
+  int nseg_max, B, S, NT, W;
+  int groups;            // work units per (direction, sample): ceil(NT / kWarps)
+  int units_per_block;   // most units a block takes (sizes its list of tile rows)
+  int masked;            // 1: store the masked runs instead of the visible intervals
+  uint64_t wait_ns;      // limit of the grid barrier wait
 };
 
 __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
@@ -77,172 +103,349 @@ __device__ __forceinline__ int seg_end_at(const int* seg_s, int nseg, int k) {
   return seg_s[imin(imax(k, -1) + 1, nseg)];
 }
 
-// Adds v (+1 or -1; 0 for a lane with nothing to add) at index x of a shared-memory array.  The
-// rows of one warp mostly update the same tile index, so a warp whose active lanes agree on x
-// makes one atomic with their sum instead of up to 32 conflicting ones.  Call with the whole warp.
-__device__ __forceinline__ void warp_add(int* arr, int x, int v) {
-  const unsigned full = 0xFFFFFFFFu;
-  const int lo = __reduce_min_sync(full, v != 0 ? x : 0x7FFFFFFF);
-  const int hi = __reduce_max_sync(full, v != 0 ? x : -1);
-  if (lo == hi) {
-    const int sum = __reduce_add_sync(full, v);
-    if ((threadIdx.x & 31) == 0 && sum != 0) atomicAdd(&arr[lo], sum);
-  } else if (lo < hi && v != 0) {
-    atomicAdd(&arr[x], v);
+__device__ __forceinline__ void record_status(int32_t* work, int code, int where) {
+  atomicCAS(work, 0, (code << 16) | (where & 0xFFFF));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Every block of the (cooperative, fully resident) grid arrives, then waits until all have.  The
+// wait is bounded: past wait_ns it records a time-out and returns.
+__device__ __forceinline__ void grid_barrier(const DescCore& p) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&p.work[1], 1);
+    const int n = static_cast<int>(gridDim.x);
+    if (ld_acquire(&p.work[1]) < n) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire(&p.work[1]) < n) {
+        if (globaltimer_ns() - t0 > p.wait_ns) {
+          record_status(p.work, kStatusTimeout, 0x400);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// Adds `unit` rows over the tile range [key >> 16, key & 0xFFFF) of the warp's difference array
+// for each of the lane's 4 rows (key 0xFFFFFFFF: no range).  When the 4 rows agree, lanes with
+// the same range are added together by one leader.  Call with the whole warp.
+__device__ __forceinline__ void add_ranges(int* cnt, const uint32_t (&key)[kRowsPerLane], int unit) {
+  const bool same = key[1] == key[0] && key[2] == key[0] && key[3] == key[0];
+  const uint32_t k0 = same ? key[0] : 0xFFFFFFFEu;
+  const unsigned grp = __match_any_sync(0xFFFFFFFFu, k0);
+  const int lane = threadIdx.x & 31;
+  if (same) {
+    if (k0 != 0xFFFFFFFFu && lane == __ffs(grp) - 1) {
+      const int w = kRowsPerLane * __popc(grp) * unit;
+      atomicAdd(&cnt[k0 >> 16], w);
+      atomicAdd(&cnt[k0 & 0xFFFF], -w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < kRowsPerLane; ++q)
+      if (key[q] != 0xFFFFFFFFu) {
+        atomicAdd(&cnt[key[q] >> 16], unit);
+        atomicAdd(&cnt[key[q] & 0xFFFF], -unit);
+      }
   }
 }
 
-// Dynamic shared memory: (nseg_max + 1) + 2 * (NT + 1) ints + NT bytes.
-// NS: the slots the evaluator may fill, known at compile time; slots n >= p.ni are not stored.
-// Eval::row(i, seg_idx(i), seg, nseg, S, lo, hi) writes raw endpoints of the row's slots and
-// leaves lo = hi = 0 in slots the row does not have.
+// One tile row of one direction: Interval Table rows, bitmap row; returns the number of non-empty
+// tiles (in every lane).  NS: the slots the evaluator may fill, known at compile time; slots
+// n >= ni - masked are not part of the spec.  Eval::row(i, seg_idx(i), seg, nseg, S, lo, hi)
+// writes raw endpoints of the row's slots and leaves lo = hi = 0 in slots the row does not have.
 template <int NS, class Eval>
-__device__ __forceinline__ void descriptor_tile(const DescCore& p, int b, int tile, const Eval& ev) {
-  extern __shared__ int smem_i[];
-  __shared__ int s_bad;
-  __shared__ int s_wtot[3][kTile / 32];
-  int* seg_s = smem_i;                     // [nseg_max + 1]
-  int* cnt_any = smem_i + p.nseg_max + 1;  // [NT + 1] difference array: rows touching a tile
-  int* cnt_all = cnt_any + p.NT + 1;       // [NT + 1] difference array: rows covering a tile
-  uint8_t* code = reinterpret_cast<uint8_t*>(cnt_all + p.NT + 1);  // [NT] 2-bit state per tile
+__device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, int b, int tile,
+                                        const int* seg_s, int nseg, int* cnt, uint8_t* code,
+                                        const Eval& ev) {
+  const int lane = threadIdx.x & 31;
+  const int r0 = tile * kTile + lane * kRowsPerLane;
+  const int spec_slots = dd.ni - p.masked;
+  int lo[kRowsPerLane][NS], hi[kRowsPerLane][NS];
 
-  const int t = threadIdx.x;
-  const int lane = t & 31, warp = t >> 5;
-  int nseg = p.nseg[b];
-  if (t == 0) s_bad = (nseg < 1 || nseg > p.nseg_max);
-  nseg = imin(imax(nseg, 1), p.nseg_max);
-  for (int k = t; k <= p.nseg_max; k += blockDim.x) seg_s[k] = p.seg[b * (p.nseg_max + 1) + k];
-  for (int k = t; k < 2 * (p.NT + 1); k += blockDim.x) cnt_any[k] = 0;
-  __syncthreads();
-  // metadata validation: seg[0] = 0, strictly increasing, seg[nseg] = S
-  bool bad = false;
-  for (int k = t; k < nseg; k += blockDim.x) bad |= seg_s[k + 1] <= seg_s[k];
-  if (t == 0) bad |= seg_s[0] != 0 || seg_s[nseg] != p.S;
-  if (bad) s_bad = 1;
-  __syncthreads();
-  if (s_bad && t == 0 && tile == 0 && p.status != nullptr)
-    atomicCAS(p.status, 0, (kStatusBadMeta << 16) | p.dir);
-
-  // --- 1. endpoints ---------------------------------------------------------------------------
-  const int row = tile * kTile + t;
-  int lo[NS], hi[NS];
+  // --- 1. endpoints: segment of the first row by binary search, then one step at most per row
+  int k = seg_index(seg_s, nseg, r0);
 #pragma unroll
-  for (int n = 0; n < NS; ++n) {
-    lo[n] = 0;
-    hi[n] = 0;
-  }
-  ev.row(row, seg_index(seg_s, nseg, row), seg_s, nseg, p.S, lo, hi);
+  for (int q = 0; q < kRowsPerLane; ++q) {
+    const int i = r0 + q;
+    if (q > 0 && k + 1 < nseg && seg_s[k + 1] <= i) ++k;
 #pragma unroll
-  for (int n = 0; n < NS; ++n) {
-    int a = imin(imax(lo[n], 0), p.S);
-    int e = imin(imax(hi[n], 0), p.S);
-    if (n >= p.ni || e <= a) {
-      a = 0;
-      e = 0;
+    for (int n = 0; n < NS; ++n) {
+      lo[q][n] = 0;
+      hi[q][n] = 0;
     }
-    lo[n] = a;
-    hi[n] = e;
-    if (n < p.ni) {
-      int2* dst = reinterpret_cast<int2*>(p.itab) +
-                  (static_cast<unsigned long long>(b) * p.ni + n) * p.S + row;
-      *dst = make_int2(a, e);
+    ev.row(i, k, seg_s, nseg, p.S, lo[q], hi[q]);
+#pragma unroll
+    for (int n = 0; n < NS; ++n) {
+      const int a = imin(imax(lo[q][n], 0), p.S);
+      const int e = imin(imax(hi[q][n], 0), p.S);
+      const bool keep = n < spec_slots && e > a;
+      lo[q][n] = keep ? a : 0;
+      hi[q][n] = keep ? e : 0;
     }
   }
-
-  // --- 2. merged intervals (sorted by start; overlapping or adjacent ones joined) -------------
-  int ms[NS], me[NS];
+  if (!p.masked) {
 #pragma unroll
-  for (int n = 0; n < NS; ++n) {
-    ms[n] = hi[n] > lo[n] ? lo[n] : 0x7FFFFFFF;
-    me[n] = hi[n];
-  }
-#pragma unroll
-  for (int x = 0; x < NS; ++x)
-#pragma unroll
-    for (int y = 0; y + 1 < NS - x; ++y)
-      if (ms[y] > ms[y + 1]) {
-        int u = ms[y]; ms[y] = ms[y + 1]; ms[y + 1] = u;
-        u = me[y]; me[y] = me[y + 1]; me[y + 1] = u;
+    for (int n = 0; n < NS; ++n) {
+      if (n < dd.ni) {
+        int4* dst = reinterpret_cast<int4*>(
+            dd.itab + ((static_cast<unsigned long long>(b) * dd.ni + n) * p.S + r0) * 2);
+        dst[0] = make_int4(lo[0][n], hi[0][n], lo[1][n], hi[1][n]);
+        dst[1] = make_int4(lo[2][n], hi[2][n], lo[3][n], hi[3][n]);
       }
+    }
+  }
+
+  // --- 2. merged intervals per row (sorted by start; overlapping or adjacent ones joined) -----
+  int ms[kRowsPerLane][NS], me[kRowsPerLane][NS];
 #pragma unroll
-  for (int n = 1; n < NS; ++n) {
-    if (ms[n] != 0x7FFFFFFF && ms[n] <= me[n - 1] && ms[n - 1] != 0x7FFFFFFF) {
-      ms[n] = ms[n - 1];
-      me[n] = imax(me[n], me[n - 1]);
-      ms[n - 1] = 0x7FFFFFFF;  // absorbed
+  for (int q = 0; q < kRowsPerLane; ++q) {
+#pragma unroll
+    for (int n = 0; n < NS; ++n) {
+      ms[q][n] = hi[q][n] > lo[q][n] ? lo[q][n] : kNone;
+      me[q][n] = hi[q][n];
+    }
+#pragma unroll
+    for (int x = 0; x < NS; ++x)
+#pragma unroll
+      for (int y = 0; y + 1 < NS - x; ++y)
+        if (ms[q][y] > ms[q][y + 1]) {
+          int u = ms[q][y]; ms[q][y] = ms[q][y + 1]; ms[q][y + 1] = u;
+          u = me[q][y]; me[q][y] = me[q][y + 1]; me[q][y + 1] = u;
+        }
+#pragma unroll
+    for (int n = 1; n < NS; ++n) {
+      if (ms[q][n] != kNone && ms[q][n - 1] != kNone && ms[q][n] <= me[q][n - 1]) {
+        ms[q][n] = ms[q][n - 1];
+        me[q][n] = imax(me[q][n], me[q][n - 1]);
+        ms[q][n - 1] = kNone;  // absorbed
+      }
+    }
+  }
+
+  if (p.masked) {
+    // Masked form: the gaps of the merged intervals in [0, S), in increasing order, then (0, 0)
+    // padding (at most NS + 1 runs).
+    int gs[kRowsPerLane][NS + 1], ge[kRowsPerLane][NS + 1];
+#pragma unroll
+    for (int q = 0; q < kRowsPerLane; ++q) {
+      int cursor = 0;
+#pragma unroll
+      for (int n = 0; n < NS; ++n) {
+        const bool live = ms[q][n] != kNone;
+        gs[q][n] = live && ms[q][n] > cursor ? cursor : kNone;
+        ge[q][n] = live ? ms[q][n] : 0;
+        if (live) cursor = me[q][n];
+      }
+      gs[q][NS] = cursor < p.S ? cursor : kNone;
+      ge[q][NS] = p.S;
+      // the non-empty runs are already increasing: move the empty ones behind them
+#pragma unroll
+      for (int x = 0; x < NS + 1; ++x)
+#pragma unroll
+        for (int y = 0; y + 1 < NS + 1 - x; ++y)
+          if (gs[q][y] > gs[q][y + 1]) {
+            int u = gs[q][y]; gs[q][y] = gs[q][y + 1]; gs[q][y + 1] = u;
+            u = ge[q][y]; ge[q][y] = ge[q][y + 1]; ge[q][y + 1] = u;
+          }
+#pragma unroll
+      for (int n = 0; n < NS + 1; ++n)
+        if (gs[q][n] == kNone) {
+          gs[q][n] = 0;
+          ge[q][n] = 0;
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NS + 1; ++n) {
+      if (n < dd.ni) {
+        int4* dst = reinterpret_cast<int4*>(
+            dd.itab + ((static_cast<unsigned long long>(b) * dd.ni + n) * p.S + r0) * 2);
+        dst[0] = make_int4(gs[0][n], ge[0][n], gs[1][n], ge[1][n]);
+        dst[1] = make_int4(gs[2][n], ge[2][n], gs[3][n], ge[3][n]);
+      }
     }
   }
 
   // --- 3. tile states ---------------------------------------------------------------------------
-  // +1 / -1 at the ends of the row's touched tile ranges (any slot) and of its fully covered tile
-  // ranges (merged intervals, disjoint, so a row counts once per tile).  After the prefix sum a
-  // tile is touched iff its "any" count is > 0 and full iff its "all" count is 128.
 #pragma unroll
   for (int n = 0; n < NS; ++n) {
-    const bool touch = hi[n] > lo[n];
-    warp_add(cnt_any, lo[n] / kTile, touch ? 1 : 0);
-    warp_add(cnt_any, touch ? (hi[n] - 1) / kTile + 1 : 0, touch ? -1 : 0);
-    const bool merged = ms[n] != 0x7FFFFFFF;
-    const int a = merged ? (ms[n] + kTile - 1) / kTile : 0;
-    const int e = merged ? me[n] / kTile : 0;
-    const bool cover = merged && e > a;
-    warp_add(cnt_all, a, cover ? 1 : 0);
-    warp_add(cnt_all, e, cover ? -1 : 0);
+    uint32_t touch[kRowsPerLane], cover[kRowsPerLane];
+#pragma unroll
+    for (int q = 0; q < kRowsPerLane; ++q) {
+      // tiles [lo / 128, (hi - 1) / 128] touched by slot n
+      touch[q] = hi[q][n] > lo[q][n]
+                     ? (static_cast<uint32_t>(lo[q][n] >> 7) << 16) |
+                           static_cast<uint32_t>(((hi[q][n] - 1) >> 7) + 1)
+                     : 0xFFFFFFFFu;
+      // tiles [ceil(ms / 128), me / 128) covered by merged interval n
+      const int a = (ms[q][n] + kTile - 1) >> 7, e = me[q][n] >> 7;
+      cover[q] = ms[q][n] != kNone && e > a
+                     ? (static_cast<uint32_t>(a) << 16) | static_cast<uint32_t>(e)
+                     : 0xFFFFFFFFu;
+    }
+    add_ranges(cnt, touch, 1);
+    add_ranges(cnt, cover, 1 << 16);
   }
-  __syncthreads();
-  // block prefix sum: thread t owns tiles [t * per, (t + 1) * per)
-  const int per = (p.NT + kTile - 1) / kTile;
-  const int c0 = t * per;
-  int sa = 0, sf = 0;
-  for (int c = c0; c < c0 + per && c < p.NT; ++c) {
-    sa += cnt_any[c];
-    sf += cnt_all[c];
-  }
-  int ia = sa, iff = sf;
+  __syncwarp();
+  // prefix sum over the tiles: lane l owns tiles [l * per, (l + 1) * per); entries are cleared
+  // as they are read, so the array is zero again for the next tile row
+  const int per = (p.NT + 31) >> 5;
+  const int t0 = lane * per, t1 = imin(t0 + per, p.NT);
+  int run = 0;
+  for (int t = t0; t < t1; ++t) run += cnt[t];
+  int incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int ya = __shfl_up_sync(0xFFFFFFFFu, ia, o);
-    const int yf = __shfl_up_sync(0xFFFFFFFFu, iff, o);
-    if (lane >= o) {
-      ia += ya;
-      iff += yf;
-    }
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
   }
-  if (lane == 31) {
-    s_wtot[0][warp] = ia;
-    s_wtot[1][warp] = iff;
-  }
-  __syncthreads();
-  int run_a = ia - sa, run_f = iff - sf;  // exclusive prefix within the warp
-  for (int w = 0; w < warp; ++w) {
-    run_a += s_wtot[0][w];
-    run_f += s_wtot[1][w];
-  }
+  int acc = incl - run;
   int nonempty = 0;
-  for (int c = c0; c < c0 + per && c < p.NT; ++c) {
-    run_a += cnt_any[c];
-    run_f += cnt_all[c];
-    code[c] = run_a > 0 ? (run_f == kTile ? 2 : 1) : 0;
-    nonempty += run_a > 0 ? 1 : 0;
+  for (int t = t0; t < t1; ++t) {
+    acc += cnt[t];
+    cnt[t] = 0;
+    const int touched = acc & 0xFFFF;
+    const int covered = static_cast<int>(static_cast<uint32_t>(acc) >> 16);
+    code[t] = static_cast<uint8_t>(touched > 0 ? (covered == kTile ? 2 : 1) : 0);
+    nonempty += touched > 0 ? 1 : 0;
   }
+  if (lane == 0) cnt[p.NT] = 0;
   nonempty = __reduce_add_sync(0xFFFFFFFFu, nonempty);
-  if (lane == 0) s_wtot[2][warp] = nonempty;
-  __syncthreads();
-  if (t == 0) {
-    int total = 0;
-#pragma unroll
-    for (int w = 0; w < kTile / 32; ++w) total += s_wtot[2][w];
-    p.rowcnt[static_cast<unsigned long long>(b) * p.NT + tile] = total;
-  }
-  uint32_t* out = p.bm + (static_cast<unsigned long long>(b) * p.NT + tile) * p.W;
-  for (int ow = t; ow < p.W; ow += blockDim.x) {
+  __syncwarp();
+  uint32_t* out = dd.bm + (static_cast<unsigned long long>(b) * p.NT + tile) * p.W;
+  for (int w = lane; w < p.W; w += 32) {
     uint32_t word = 0;
     for (int q = 0; q < 16; ++q) {
-      const int c = ow * 16 + q;
-      if (c >= p.NT) break;
-      word |= static_cast<uint32_t>(code[c]) << (2 * q);
+      const int t = w * 16 + q;
+      if (t < p.NT) word |= static_cast<uint32_t>(code[t]) << (2 * q);
     }
-    out[ow] = word;
+    out[w] = word;
+  }
+  __syncwarp();
+  return nonempty;
+}
+
+// Dynamic shared memory of the kernel, in ints.
+__host__ __device__ __forceinline__ int seg_ints(int nseg_max) { return (nseg_max + 1 + 3) & ~3; }
+__host__ __device__ __forceinline__ int cnt_ints(int NT) { return (NT + 1 + 3) & ~3; }
+__host__ __device__ __forceinline__ int code_ints(int NT) { return (NT + 3) >> 2; }
+__host__ __device__ __forceinline__ int smem_ints(int nseg_max, int NT, int units_per_block) {
+  return seg_ints(nseg_max) + kWarps * (cnt_ints(NT) + code_ints(NT)) + 2 * kWarps * units_per_block;
+}
+
+template <int NSF, int NSB, class EvalF, class EvalB>
+__device__ __forceinline__ void descriptor_kernel(const DescCore& p, const EvalF& evf,
+                                                  const EvalB& evb) {
+  extern __shared__ int smem_i[];
+  __shared__ int s_bad;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* seg_s = smem_i;
+  int* cnt_all = seg_s + seg_ints(p.nseg_max);
+  int* cnt = cnt_all + warp * cnt_ints(p.NT);
+  uint8_t* code = reinterpret_cast<uint8_t*>(cnt_all + kWarps * cnt_ints(p.NT)) +
+                  warp * 4 * code_ints(p.NT);
+  int2* items = reinterpret_cast<int2*>(cnt_all + kWarps * (cnt_ints(p.NT) + code_ints(p.NT)));
+  int* hist = p.work + 2;
+
+  for (int t = lane; t < cnt_ints(p.NT); t += 32) cnt[t] = 0;
+
+  // ---- phase 1: tile rows ---------------------------------------------------------------------
+  const int per_dir = p.B * p.groups;
+  int cur_b = -1, nseg = 1, u = 0;
+  for (int unit = blockIdx.x; unit < 2 * per_dir; unit += gridDim.x, ++u) {
+    const int d = unit >= per_dir ? 1 : 0;
+    const int rem = unit - d * per_dir;
+    const int b = rem / p.groups, g = rem - b * p.groups;
+    if (b != cur_b) {
+      __syncthreads();  // no warp reads the previous sample's boundaries any more
+      const int ns = p.nseg[b];
+      nseg = imin(imax(ns, 1), p.nseg_max);
+      if (threadIdx.x == 0) s_bad = ns < 1 || ns > p.nseg_max;
+      for (int k = threadIdx.x; k <= p.nseg_max; k += kThreads)
+        seg_s[k] = p.seg[b * (p.nseg_max + 1) + k];
+      __syncthreads();
+      // metadata validation: seg[0] = 0, strictly increasing, seg[nseg] = S
+      bool bad = false;
+      for (int k = threadIdx.x; k < nseg; k += kThreads) bad |= seg_s[k + 1] <= seg_s[k];
+      if (threadIdx.x == 0) bad |= seg_s[0] != 0 || seg_s[nseg] != p.S;
+      if (bad) s_bad = 1;
+      __syncthreads();
+      if (s_bad && threadIdx.x == 0) record_status(p.work, kStatusBadMeta, d);
+      cur_b = b;
+    }
+    const int tile = g * kWarps + warp;
+    if (tile < p.NT) {
+      const int c = d == 0 ? tile_row<NSF>(p, p.dir[0], b, tile, seg_s, nseg, cnt, code, evf)
+                           : tile_row<NSB>(p, p.dir[1], b, tile, seg_s, nseg, cnt, code, evb);
+      if (lane == 0) {
+        const int ticket = atomicAdd(&hist[d * (p.NT + 1) + c], 1);
+        items[u * kWarps + warp] = make_int2(static_cast<int>((static_cast<uint32_t>(d) << 31) |
+                                                              (static_cast<uint32_t>(b) << 16) |
+                                                              static_cast<uint32_t>(tile)),
+                                             (c << 16) | ticket);
+      }
+    } else if (lane == 0) {
+      items[u * kWarps + warp] = make_int2(-1, 0);
+    }
+  }
+  const int n_items = u * kWarps;
+
+  // ---- phase 2: schedules ----------------------------------------------------------------------
+  grid_barrier(p);
+  // first position of each count: base[d][c] = tile rows of direction d with more than c tiles
+  // (the per-warp difference arrays are free now and hold the two histograms)
+  int* base = cnt_all;
+  const int n1 = p.NT + 1;
+  for (int x = threadIdx.x; x < 2 * n1; x += kThreads)
+    base[x] = ld_acquire(&hist[x]);
+  __syncthreads();
+  if (warp < 2) {
+    int* h = base + warp * n1;
+    // suffix sums from c = NT down: lane l owns counts [NT - (l + 1) * per + 1, NT - l * per]
+    const int per = (n1 + 31) >> 5;
+    int run = 0;
+    for (int q = 0; q < per; ++q) {
+      const int c = p.NT - lane * per - q;
+      if (c >= 0) run += h[c];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int acc = incl - run;  // rows with more tiles than this lane's first count
+    for (int q = 0; q < per; ++q) {
+      const int c = p.NT - lane * per - q;
+      if (c >= 0) {
+        const int v = h[c];
+        h[c] = acc;
+        acc += v;
+      }
+    }
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < n_items; x += kThreads) {
+    const int2 it = items[x];
+    if (it.x == -1) continue;
+    const int d = static_cast<int>(static_cast<uint32_t>(it.x) >> 31);
+    const int c = it.y >> 16, ticket = it.y & 0xFFFF;
+    const int pos = base[d * n1 + c] + ticket;
+    if (pos < p.B * p.NT) p.dir[d].sched[pos] = it.x & 0x7FFFFFFF;
   }
 }
 

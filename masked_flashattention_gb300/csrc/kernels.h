@@ -11,9 +11,10 @@ struct cm_spec;
 namespace cm {
 
 const DevProg* spec_program(const cm_spec* s);
-// The spec's mask-specific preprocess kernel (a cudaKernel_t), compiled with NVRTC and loaded
-// into the current context on first use; nullptr where that is not possible.
-const void* spec_generated_kernel(const cm_spec* s);
+// The mask-specific preprocess kernel of a (forward, backward) spec pair (a cudaKernel_t),
+// compiled with NVRTC and loaded into the current context on first use; nullptr where that is
+// not possible.
+const void* pair_generated_kernel(const cm_spec* fwd, const cm_spec* bwd);
 
 struct FwdParams {
   const int32_t* itab;   // forward Interval Table [B][NI][S][2]
@@ -24,6 +25,7 @@ struct FwdParams {
   float* lse;
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
+  int masked;            // 1: the Interval Table holds masked intervals (their complement)
   float scale_log2;      // softmax scale * log2(e)
   uint64_t wait_ns;      // limit of each bounded wait (ns)
 };
@@ -41,6 +43,7 @@ struct BwdParams {
   __nv_bfloat16* dv;
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
+  int masked;            // 1: the Interval Table holds masked intervals (their complement)
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
   uint64_t wait_ns;      // limit of each bounded wait (ns)
@@ -57,17 +60,21 @@ struct DqParams {
   __nv_bfloat16* dq;
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
+  int masked;            // 1: the Interval Table holds masked intervals (their complement)
   float scale;
   float scale_log2;
   uint64_t wait_ns;      // limit of each bounded wait (ns)
 };
 
-// Runs the generated kernels when both gen_fwd and gen_bwd are given, else the generic kernel.
-int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_fwd,
-                      const void* gen_bwd, const int32_t* seg, const int32_t* nseg, int nseg_max,
-                      int B, int S, int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b,
-                      uint32_t* bm_b, int32_t* sched_f, int32_t* sched_b, int32_t* status,
-                      cudaStream_t stream);
+// One cooperative launch that builds both halves of the descriptor and both schedules: the
+// generated kernel of the (forward, backward) spec pair when gen_kernel is given, else the generic
+// kernel.  `work` (zeroed by the caller) holds the status word, the grid barrier and the
+// histograms of the schedule.
+int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_kernel,
+                      const int32_t* seg, const int32_t* nseg, int nseg_max, int B, int S,
+                      int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b, uint32_t* bm_b,
+                      int32_t* sched_f, int32_t* sched_b, int32_t* work, int masked,
+                      uint64_t wait_ns, cudaStream_t stream);
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream);
 // Backward prologue: per row -D = -rowsum(dO * O) and -LSE * log2(e) (rows = B * H * S).

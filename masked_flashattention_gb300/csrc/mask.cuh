@@ -1,6 +1,6 @@
 // Helpers shared by the attention kernels: walking the non-empty tiles of a Tile-State Bitmap row
-// (CompileMask section 3.3.1) and the partial-tile visibility check of the kernels that traverse
-// query rows (the unsigned interval test of section 4.4).
+// (CompileMask section 3.3.1) and the partial-tile visibility check (section 3.3.2; the unsigned
+// interval test of section 4.4 and the other forms of its ablation).
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -42,147 +42,169 @@ __device__ __forceinline__ void cta_work(int q, int n_items, int H, int& item_id
   }
 }
 
-// Forms of the partial-tile visibility check (the ablation of CompileMask section 4.4):
-//   kCheckUnsigned    visible iff (u32)(x - s) < (u32)(e - s) for some visible interval [s, e):
-//                     one subtraction and one unsigned comparison per interval (the default);
-//   kCheckTwoCompare  visible iff s <= x && x < e for some visible interval;
-//   kCheckMasked      the complement of the visible intervals in [0, S) is used as a list of
-//                     masked intervals (the FlashMask form), each tested with the unsigned
-//                     comparison; visible iff x lies in none of them.
+// Forms of the partial-tile visibility check (full and empty tiles never run one):
+//   kCheckUnsigned    per score: for each stored interval [s, e) one subtraction and one unsigned
+//                     comparison, (u32)(x - s) < (u32)(e - s) (the paper's section 4.4 test);
+//   kCheckTwoCompare  per score: s <= x && x < e for each stored interval;
+//   kCheckRangeMask   per row and 32-index chunk [x0, x0 + 32): each stored interval becomes the
+//                     bit range [clamp(s - x0), clamp(e - x0)) of a 32-bit mask (two clamped
+//                     subtractions and two funnel shifts), and each score then tests one bit
+//                     (the default: the per-score cost no longer grows with the interval count).
+// The stored intervals are the row's visible intervals (visible form of the descriptor) or the
+// masked intervals of their complement in [0, S) (masked form, the representation the pages
+// compare against in section 4.4): in the masked form an index is visible iff it lies in none.
 constexpr int kCheckUnsigned = 0;
 constexpr int kCheckTwoCompare = 1;
-constexpr int kCheckMasked = 2;
+constexpr int kCheckRangeMask = 3;
 
-// One row's (or key column's) intervals in the form the check uses: start and length, and for
-// the two-compare form the end.  The masked form holds up to NI + 1 gaps.
+constexpr int kMaxStored = 9;  // up to 8 visible intervals, or the 9 gaps around them
+
+// A row's stored intervals in registers.  The kernels are compiled for two capacities, MAXNI = 4
+// (every workload here in the visible form) and 9, so that the common case keeps few registers.
+template <int MAXNI>
 struct RowIntervals {
-  int st[5];
-  int en[5];
-  uint32_t len[5];
+  int st[MAXNI];
+  int en[MAXNI];
 };
 
-// Loads the row's NI visible intervals from a slot-major Interval Table [b][NI][S][2]; for the
-// masked form turns them into the gaps of their union within [0, S) (zero-length when unused).
-__device__ __forceinline__ void load_row_intervals(const int32_t* itab, int b, int NI, int S, int row,
-                                                   int check, RowIntervals& ri) {
-  int s[4], e[4];
+// Loads the row's NI stored intervals from a slot-major Interval Table [b][NI][S][2] (unused
+// registers hold the empty interval (0, 0)).
+template <int MAXNI>
+__device__ __forceinline__ void load_row_intervals(const int32_t* itab, int b, int NI, int S,
+                                                   int row, RowIntervals<MAXNI>& ri) {
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    s[n] = 0;
-    e[n] = 0;
+  for (int n = 0; n < MAXNI; ++n) {
+    ri.st[n] = 0;
+    ri.en[n] = 0;
     if (n < NI) {
       const int2 iv = reinterpret_cast<const int2*>(itab)[(static_cast<size_t>(b) * NI + n) * S + row];
-      s[n] = iv.x;
-      e[n] = iv.y;
+      ri.st[n] = iv.x;
+      ri.en[n] = iv.y;
     }
   }
-#pragma unroll
-  for (int n = 0; n < 5; ++n) {
-    ri.st[n] = n < 4 ? s[n] : 0;
-    ri.en[n] = n < 4 ? e[n] : 0;
-  }
-  if (check == kCheckMasked) {
-    // sort the non-empty intervals by start (empty ones last), then walk the gaps
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-      if (e[n] <= s[n]) s[n] = 0x7FFFFFFF;
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int y = 0; y + 1 < 4 - x; ++y)
-        if (s[y] > s[y + 1]) {
-          int u = s[y]; s[y] = s[y + 1]; s[y + 1] = u;
-          u = e[y]; e[y] = e[y + 1]; e[y + 1] = u;
-        }
-    int cursor = 0;  // end of the visible union so far
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      const bool live = s[n] != 0x7FFFFFFF;
-      const int gs = cursor, ge = live ? (s[n] > cursor ? s[n] : cursor) : cursor;
-      ri.st[n] = gs;
-      ri.en[n] = ge;
-      if (live && e[n] > cursor) cursor = e[n];
-    }
-    ri.st[4] = cursor;
-    ri.en[4] = S;
-  }
-#pragma unroll
-  for (int n = 0; n < 5; ++n) ri.len[n] = static_cast<uint32_t>(ri.en[n] - ri.st[n]);
 }
 
-// true iff x (= x0 + c) is visible under the given form; NI = the number of stored intervals
-template <int NI, int CHECK>
-__device__ __forceinline__ bool visible_at(uint32_t c, int x0, const RowIntervals& ri) {
-  if (CHECK == kCheckMasked) {
-    bool hidden = false;
-#pragma unroll
-    for (int n = 0; n < NI + 1; ++n) {
-      const int k = n < NI ? n : 4;  // the gaps before each interval, then the tail gap
-      hidden |= (static_cast<uint32_t>(x0 - ri.st[k]) + c) < ri.len[k];
-    }
-    return !hidden;
-  }
-  bool vis = false;
+// ---- per-score forms ----------------------------------------------------------------------------
+// true iff x0 + c lies in one of the first NI stored intervals
+template <int NI, int CHECK, class RI>
+__device__ __forceinline__ bool in_any(uint32_t c, int x0, const RI& ri) {
+  bool in = false;
 #pragma unroll
   for (int n = 0; n < NI; ++n) {
     if (CHECK == kCheckTwoCompare) {
       const int x = x0 + static_cast<int>(c);
-      vis |= (x >= ri.st[n]) & (x < ri.en[n]);
+      in |= (x >= ri.st[n]) & (x < ri.en[n]);
     } else {
-      vis |= (static_cast<uint32_t>(x0 - ri.st[n]) + c) < ri.len[n];
+      in |= (static_cast<uint32_t>(x0 - ri.st[n]) + c) <
+            static_cast<uint32_t>(ri.en[n] - ri.st[n]);
     }
   }
-  return vis;
+  return in;
 }
 
 // Replace invisible scores by -inf: key j0 + c of the row (c < N).
-template <int NI, int CHECK, int N>
-__device__ __forceinline__ void mask_cols(float (&s)[N], int j0, const RowIntervals& ri) {
+template <int NI, int CHECK, int N, class RI>
+__device__ __forceinline__ void mask_cols(float (&s)[N], int j0, const RI& ri, bool masked) {
 #pragma unroll
-  for (int c = 0; c < N; ++c) s[c] = visible_at<NI, CHECK>(static_cast<uint32_t>(c), j0, ri) ? s[c] : -INFINITY;
+  for (int c = 0; c < N; ++c)
+    s[c] = (in_any<NI, CHECK>(static_cast<uint32_t>(c), j0, ri) != masked) ? s[c] : -INFINITY;
 }
 
-// Bit c set iff index i0 + c (c < 32) is visible (the key-column form of the backward).
-template <int NI, int CHECK>
-__device__ __forceinline__ uint32_t visible_bits(int i0, const RowIntervals& ri) {
+// Bit c set iff index i0 + c (c < 32) is visible.
+template <int NI, int CHECK, class RI>
+__device__ __forceinline__ uint32_t visible_bits(int i0, const RI& ri, bool masked) {
   uint32_t bits = 0;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) bits |= visible_at<NI, CHECK>(static_cast<uint32_t>(c), i0, ri) ? (1u << c) : 0u;
+  for (int c = 0; c < 32; ++c)
+    bits |= (in_any<NI, CHECK>(static_cast<uint32_t>(c), i0, ri) != masked) ? (1u << c) : 0u;
   return bits;
 }
 
-// Runtime dispatch over the interval count (1..4) and the check form.
-template <int N>
-__device__ __forceinline__ void mask_cols_any(float (&s)[N], int j0, const RowIntervals& ri, int NI,
-                                              int check) {
-#define CM_MASK_CASE(ni)                                                   \
-  case ni:                                                                 \
-    if (check == kCheckTwoCompare) mask_cols<ni, kCheckTwoCompare>(s, j0, ri); \
-    else if (check == kCheckMasked) mask_cols<ni, kCheckMasked>(s, j0, ri);     \
-    else mask_cols<ni, kCheckUnsigned>(s, j0, ri);                        \
+// ---- range-mask form -----------------------------------------------------------------------------
+// Bits [clamp(s - x0, 0, 32), clamp(e - x0, 0, 32)) of a 32-bit word: the indices of the chunk
+// [x0, x0 + 32) inside [s, e).  The funnel shift of 0xFFFFFFFF by n (clamped at 32) into a zero
+// high word gives the n lowest bits set.
+__device__ __forceinline__ uint32_t low_bits(int n) {
+  return __funnelshift_lc(0xFFFFFFFFu, 0u, static_cast<uint32_t>(n > 0 ? n : 0));
+}
+template <int MAXNI>
+__device__ __forceinline__ uint32_t range_bits(const RowIntervals<MAXNI>& ri, int NI, int x0,
+                                               bool masked) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int n = 0; n < MAXNI; ++n)
+    if (n < NI) m |= low_bits(ri.en[n] - x0) & ~low_bits(ri.st[n] - x0);
+  return masked ? ~m : m;
+}
+
+// Scores of 32 keys [j0, j0 + 32) whose bit in `vis` is clear become -inf.  The warp skips the
+// chunk when every lane's mask is full.
+__device__ __forceinline__ void apply_bits(float* s, uint32_t vis) {
+  if (__all_sync(0xFFFFFFFFu, vis == 0xFFFFFFFFu)) return;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) s[c] = (vis & (1u << c)) ? s[c] : -INFINITY;
+}
+
+// ---- dispatch ------------------------------------------------------------------------------------
+// Masks N (a multiple of 32) scores of keys [j0, j0 + N) of one row: NI stored intervals (1..9),
+// `check` one of the forms above, `masked` the descriptor form.
+template <int N, int MAXNI>
+__device__ __forceinline__ void mask_cols_any(float (&s)[N], int j0, const RowIntervals<MAXNI>& ri,
+                                              int NI, int check, bool masked) {
+  if (check == kCheckRangeMask) {
+#pragma unroll
+    for (int q = 0; q < N / 32; ++q) apply_bits(&s[32 * q], range_bits(ri, NI, j0 + 32 * q, masked));
+    return;
+  }
+#define CM_MASK_CASE(ni)                                                                  \
+  case ni:                                                                                \
+    if constexpr (ni <= MAXNI) {                                                          \
+      if (check == kCheckTwoCompare) mask_cols<ni, kCheckTwoCompare>(s, j0, ri, masked);   \
+      else mask_cols<ni, kCheckUnsigned>(s, j0, ri, masked);                              \
+    }                                                                                     \
     break;
   switch (NI) {
     CM_MASK_CASE(1)
     CM_MASK_CASE(2)
     CM_MASK_CASE(3)
+    CM_MASK_CASE(4)
+    CM_MASK_CASE(5)
+    CM_MASK_CASE(6)
+    CM_MASK_CASE(7)
+    CM_MASK_CASE(8)
+    CM_MASK_CASE(9)
     default:
-      CM_MASK_CASE(4)
+      break;
   }
 #undef CM_MASK_CASE
 }
-__device__ __forceinline__ uint32_t visible_bits_any(int i0, const RowIntervals& ri, int NI, int check) {
-#define CM_BITS_CASE(ni)                                                        \
-  case ni:                                                                      \
-    if (check == kCheckTwoCompare) return visible_bits<ni, kCheckTwoCompare>(i0, ri); \
-    if (check == kCheckMasked) return visible_bits<ni, kCheckMasked>(i0, ri);         \
-    return visible_bits<ni, kCheckUnsigned>(i0, ri);
+
+// Visibility bits of the 32 indices [i0, i0 + 32) (the key-column form of the backward).
+template <int MAXNI>
+__device__ __forceinline__ uint32_t visible_bits_any(int i0, const RowIntervals<MAXNI>& ri, int NI,
+                                                     int check, bool masked) {
+  if (check == kCheckRangeMask) return range_bits(ri, NI, i0, masked);
+#define CM_BITS_CASE(ni)                                                                     \
+  case ni:                                                                                   \
+    if constexpr (ni <= MAXNI) {                                                             \
+      if (check == kCheckTwoCompare) return visible_bits<ni, kCheckTwoCompare>(i0, ri, masked); \
+      return visible_bits<ni, kCheckUnsigned>(i0, ri, masked);                               \
+    }                                                                                        \
+    break;
   switch (NI) {
     CM_BITS_CASE(1)
     CM_BITS_CASE(2)
     CM_BITS_CASE(3)
+    CM_BITS_CASE(4)
+    CM_BITS_CASE(5)
+    CM_BITS_CASE(6)
+    CM_BITS_CASE(7)
+    CM_BITS_CASE(8)
+    CM_BITS_CASE(9)
     default:
-      CM_BITS_CASE(4)
+      break;
   }
+  return 0u;
 #undef CM_BITS_CASE
 }
 

@@ -1,13 +1,11 @@
 // Online preprocess: evaluate compiled interval endpoints against batch metadata and emit the
 // Execution Descriptor (CompileMask sections 3.3 and 3.3.1).
 //
-// The per-tile work (endpoints, clamping, Interval Table stores, tile classification) lives in
-// descriptor_core.cuh and is shared with the mask-specific kernels generated per MaskSpec.  This
-// file holds the generic kernel, whose row evaluator interprets the compiler's endpoint programs
-// (one launch for both directions), the schedule kernel, and the launcher that picks one of the
-// two descriptor kernels.
-//
-// The schedule orders tile rows longest first (LPT) for the attention kernels.
+// The whole kernel body (endpoints, clamping, Interval Table stores, tile classification, the
+// longest-first schedules) lives in descriptor_core.cuh and is shared with the mask-specific
+// kernels generated per pair of MaskSpecs.  This file holds the generic kernel, whose row
+// evaluators interpret the compiler's endpoint programs, and the launcher: one cooperative launch
+// builds both halves of the descriptor and both schedules.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -21,8 +19,8 @@ constexpr int kTile = cmcore::kTile;
 static_assert(cmcore::kSlots == kMaxSlots, "slot limits of the compiler and the kernel differ");
 
 struct PrepParams {
-  DevProg prog[2];           // 0: forward spec, 1: backward spec
-  cmcore::DescCore core[2];  // 0: forward, 1: backward
+  DevProg prog[2];  // 0: forward spec, 1: backward spec
+  cmcore::DescCore core;
 };
 
 // Evaluate one endpoint program.  Arithmetic wraps (unsigned) instead of overflowing.
@@ -106,113 +104,90 @@ struct InterpEval {
   }
 };
 
-// Both directions in one launch: block x covers tile row (x % (B*NT)) of direction x / (B*NT).
-__global__ void __launch_bounds__(kTile) descriptor_kernel(const __grid_constant__ PrepParams p) {
-  const int per_dir = p.core[0].B * p.core[0].NT;
-  const int dir = blockIdx.x / per_dir;
-  const int rem = blockIdx.x % per_dir;
-  cmcore::descriptor_tile<kMaxSlots>(p.core[dir], rem / p.core[0].NT, rem % p.core[0].NT,
-                                     InterpEval{&p.prog[dir]});
+// The generic kernel: both directions, both schedules, one cooperative launch.
+__global__ void __launch_bounds__(cmcore::kThreads) descriptor_kernel(
+    const __grid_constant__ PrepParams p) {
+  cmcore::descriptor_kernel<kMaxSlots, kMaxSlots>(p.core, InterpEval{&p.prog[0]},
+                                                  InterpEval{&p.prog[1]});
 }
 
-// Longest-first order of tile rows by counting sort on the number of non-empty tiles (0..NT),
-// which the descriptor kernel left in the schedule array itself: the counts are staged in shared
-// memory, histogrammed, scanned in descending order, and each row is placed.  Rows with equal
-// counts may come in any order.  One block of 1024 threads per direction; NT <= 1024 and B * NT <= 32768.
-__global__ void __launch_bounds__(1024) schedule_kernel(int32_t* sched_f, int32_t* sched_b, int B,
-                                                        int NT) {
-  extern __shared__ uint16_t s_cnt[];  // [B * NT]
-  __shared__ int hist[1025];
-  __shared__ int wsum[32];
-  int32_t* sched = blockIdx.x == 0 ? sched_f : sched_b;
-  const int n = B * NT;
-  const int t = threadIdx.x;
-  const int lane = t & 31, warp = t >> 5;
-  const unsigned full = 0xFFFFFFFFu;
-  for (int c = t; c <= NT; c += blockDim.x) hist[c] = 0;
-  for (int it = t; it < n; it += blockDim.x) s_cnt[it] = static_cast<uint16_t>(sched[it]);
-  __syncthreads();
-  for (int it = t; it < n; it += blockDim.x) atomicAdd(&hist[s_cnt[it]], 1);
-  __syncthreads();
-  // thread t owns count NT - t (t < NT): inclusive scan in descending count order
-  const int c = NT - t;
-  const int v = t < NT ? hist[c] : 0;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(full, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = wsum[lane];
-    int e = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(full, e, o);
-      if (lane >= o) e += y;
-    }
-    wsum[lane] = e - w;  // exclusive prefix of the warp totals
-  }
-  __syncthreads();
-  const int incl = x + wsum[warp];
-  __syncthreads();
-  if (t < NT) hist[c] = incl - v;   // first position of count c
-  if (t == NT - 1) hist[0] = incl;  // rows without tiles go last
-  __syncthreads();
-  for (int it = t; it < n; it += blockDim.x) {
-    const int pos = atomicAdd(&hist[s_cnt[it]], 1);
-    sched[pos] = ((it / NT) << 16) | (it % NT);
-  }
+namespace {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
 }
 
-int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_fwd,
-                      const void* gen_bwd, const int32_t* seg, const int32_t* nseg, int nseg_max,
-                      int B, int S, int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b,
-                      uint32_t* bm_b, int32_t* sched_f, int32_t* sched_b, int32_t* status,
-                      cudaStream_t stream) {
+}  // namespace
+
+int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_kernel,
+                      const int32_t* seg, const int32_t* nseg, int nseg_max, int B, int S,
+                      int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b, uint32_t* bm_b,
+                      int32_t* sched_f, int32_t* sched_b, int32_t* work, int masked,
+                      uint64_t wait_ns, cudaStream_t stream) {
   const int NT = S / kTile;
   const int W = (NT + 15) / 16;
   if (NT > 1024 || static_cast<long long>(B) * NT > 32768) return -1;
-  const cmcore::DescCore cf{itab_f, bm_f, sched_f, seg, nseg, status, nseg_max, B, S, NT, W, fwd.ni, 0};
-  const cmcore::DescCore cb{itab_b, bm_b, sched_b, seg, nseg, status, nseg_max, B, S, NT, W, bwd.ni, 1};
-  const size_t smem = static_cast<size_t>(nseg_max + 1) * 4 + static_cast<size_t>(2) * (NT + 1) * 4 +
-                      static_cast<size_t>(NT) + 16;
+  const int sms = sm_count();
+  if (sms <= 0) return -1;
+  cmcore::DescCore c;
+  c.dir[0] = cmcore::DescDir{itab_f, bm_f, sched_f, fwd.ni + masked};
+  c.dir[1] = cmcore::DescDir{itab_b, bm_b, sched_b, bwd.ni + masked};
+  c.seg = seg;
+  c.nseg = nseg;
+  c.work = work;
+  c.nseg_max = nseg_max;
+  c.B = B;
+  c.S = S;
+  c.NT = NT;
+  c.W = W;
+  c.groups = (NT + cmcore::kWarps - 1) / cmcore::kWarps;
+  c.masked = masked;
+  c.wait_ns = wait_ns;
+  const int units = 2 * B * c.groups;
+  const void* kernel = gen_kernel != nullptr ? gen_kernel
+                                             : reinterpret_cast<const void*>(descriptor_kernel);
+  // Size the shared memory for the most units a block can take when the grid is as small as it
+  // can be (one block per SM), then fill every SM with as many blocks as fit at that size: every
+  // block must be resident at once for the grid barrier (cooperative launch).
+  c.units_per_block = (units + sms - 1) / sms;
+  const size_t smem = static_cast<size_t>(cmcore::smem_ints(nseg_max, NT, c.units_per_block)) * 4;
   if (smem > 200 * 1024) return -1;
-  if (gen_fwd != nullptr && gen_bwd != nullptr) {
-    // the mask-specific kernels: one launch per direction
-    for (int dir = 0; dir < 2; ++dir) {
-      const void* k = dir == 0 ? gen_fwd : gen_bwd;
-      cmcore::DescCore c = dir == 0 ? cf : cb;
-      if (smem > 48 * 1024 &&
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess)
-        return -1;
-      void* args[] = {&c};
-      if (cudaLaunchKernel(k, dim3(B * NT), dim3(kTile), args, smem, stream) != cudaSuccess)
-        return -1;
-    }
-  } else {
-    PrepParams p;
-    p.prog[0] = fwd;
-    p.prog[1] = bwd;
-    p.core[0] = cf;
-    p.core[1] = cb;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(descriptor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return -1;
-    descriptor_kernel<<<2 * B * NT, kTile, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return -1;
-  }
-  const size_t sched_smem = static_cast<size_t>(B) * NT * sizeof(uint16_t);
-  if (sched_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sched_smem)) != cudaSuccess)
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
     return -1;
-  schedule_kernel<<<2, 1024, sched_smem, stream>>>(sched_f, sched_b, B, NT);
-  if (cudaGetLastError() != cudaSuccess) return -1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, cmcore::kThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int grid = units < per_sm * sms ? units : per_sm * sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(cmcore::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (gen_kernel != nullptr) {
+    void* args[] = {&c};
+    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) return -1;
+  } else {
+    PrepParams pp;
+    pp.prog[0] = fwd;
+    pp.prog[1] = bwd;
+    pp.core = c;
+    void* args[] = {&pp};
+    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) return -1;
+  }
   return 0;
 }
 

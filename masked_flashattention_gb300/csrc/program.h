@@ -12,7 +12,7 @@
 namespace cm {
 
 constexpr int kMaxRegions = 8;
-constexpr int kMaxSlots = 4;
+constexpr int kMaxSlots = 8;
 constexpr int kMaxCode = 448;
 constexpr int kMaxStack = 16;
 

@@ -23,6 +23,7 @@ enum : int {
   kDevTimeout = 1,      // an mbarrier wait exceeded its limit
   kDevBadMeta = 2,      // segment metadata not monotone / not ending at S
   kDevDescMismatch = 3, // backward Tile-State Bitmap is not the transposed forward bitmap
+  kDevBadSchedule = 4,  // a schedule entry names no tile row of the descriptor
 };
 
 __device__ __forceinline__ void set_status(int* status, int code, int where) {

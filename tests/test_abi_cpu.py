@@ -111,17 +111,25 @@ def test_descriptor_sizes(B):
     f, b = B.cm_compile_spec(specs.FWD[5]), B.cm_compile_spec(specs.BWD[5])
     sizes = B.cm_descriptor_sizes(f, b, 2, 32768)
     NT = 256
+    # status: the status word, the preprocess kernel's grid barrier and its two histograms of
+    # per-row tile counts (0..NT)
     assert sizes == [2 * 3 * 32768 * 8, 2 * NT * 16 * 4, 2 * 2 * 32768 * 8, 2 * NT * 16 * 4,
-                     2 * NT * 4, 2 * NT * 4, 4]
+                     2 * NT * 4, 2 * NT * 4, 4 * (2 + 2 * (NT + 1))]
+    # masked form: one more slot per row (the runs around ni visible intervals)
+    msizes = B.cm_descriptor_sizes(f, b, 2, 32768, form=B.CM_FORM_MASKED)
+    assert msizes[0] == 2 * 4 * 32768 * 8 and msizes[2] == 2 * 3 * 32768 * 8
+    assert msizes[1:2] == sizes[1:2] and msizes[3:] == sizes[3:]
+    with pytest.raises(B.CMError):
+        B.cm_descriptor_sizes(f, b, 2, 32768, form=2)
     with pytest.raises(B.CMError):
         B.cm_descriptor_sizes(f, b, 2, 1000)   # S not a multiple of 128
     with pytest.raises(B.CMError):
         B.cm_descriptor_sizes(f, b, 2, 32768, tile=64)
 
 
-def _fake_desc(B, Bn, S, ni_f=1, ni_b=1):
+def _fake_desc(B, Bn, S, ni_f=1, ni_b=1, form=0):
     p = 1 << 20  # never dereferenced: validation fails first
-    return B.cm_descriptor(Bn, S, 128, ni_f, ni_b, p, p, p, p, p, p, p)
+    return B.cm_descriptor(Bn, S, 128, ni_f, ni_b, form, p, p, p, p, p, p, p)
 
 
 def test_attention_argument_validation_happens_on_the_host(B):
@@ -210,11 +218,28 @@ def test_generated_preprocess_kernels_compile(B, wid):
         spec = B.cm_compile_spec(text)
         src = B.cm_spec_kernel_source(spec)
         assert 'extern "C" __global__' in src and "cm_generated_descriptor" in src
-        assert f"descriptor_tile<{B.cm_spec_num_intervals(spec)}>" in src
+        ni = B.cm_spec_num_intervals(spec)
+        assert f"descriptor_kernel<{ni}, {ni}>" in src
         rc, log = B.cm_spec_kernel_status(spec, load=False)
         if rc == B.CM_ERR_UNSUPPORTED:
             pytest.skip("NVRTC is not available here: " + log)
         assert rc == B.CM_OK, log
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5, 6])
+def test_generated_pair_kernels_compile(B, wid):
+    """The kernel cm_build_descriptor runs for a workload is generated from its forward and
+    backward specs together (one launch builds both halves); it compiles with NVRTC."""
+    from masked_flashattention_gb300 import specs
+    f, b = B.cm_compile_spec(specs.FWD[wid]), B.cm_compile_spec(specs.BWD[wid])
+    src = B.cm_descriptor_kernel_source(f, b)
+    nf, nb = B.cm_spec_num_intervals(f), B.cm_spec_num_intervals(b)
+    assert f"descriptor_kernel<{nf}, {nb}>" in src
+    assert "struct EvalFwd" in src and "struct EvalBwd" in src
+    rc, log = B.cm_descriptor_kernel_status(f, b, load=False)
+    if rc == B.CM_ERR_UNSUPPORTED:
+        pytest.skip("NVRTC is not available here: " + log)
+    assert rc == B.CM_OK, log
 
 
 def test_generated_source_follows_the_lowered_slots(B):
@@ -239,7 +264,19 @@ def test_preprocess_mode_validation(B):
 
 def test_interval_check_mode_validation(B):
     L = B.lib()
-    assert L.cm_set_interval_check(3) == B.CM_ERR_INVALID_ARG
+    assert L.cm_set_interval_check(4) == B.CM_ERR_INVALID_ARG
     assert L.cm_set_interval_check(-1) == B.CM_ERR_INVALID_ARG
-    for mode in (B.CM_CHECK_TWO_COMPARE, B.CM_CHECK_MASKED, B.CM_CHECK_UNSIGNED):
+    assert L.cm_set_interval_check(2) == B.CM_ERR_INVALID_ARG
+    for mode in (B.CM_CHECK_TWO_COMPARE, B.CM_CHECK_UNSIGNED, B.CM_CHECK_RANGE_MASK):
         B.cm_set_interval_check(mode)
+
+
+def test_interval_count_limit_is_eight(B):
+    """Rules may need up to 8 intervals per row; a ninth is refused with a parse error naming
+    the limit (the kernels keep the row's intervals in registers)."""
+    terms = ["j < 4"] + [f"(j >= {10 * m} && j < {10 * m + 3})" for m in range(1, 8)]
+    assert B.cm_spec_num_intervals(B.cm_compile_spec("region all : " + " || ".join(terms))) == 8
+    terms.append("(j >= 100 && j <= i)")
+    with pytest.raises(B.CMError) as e:
+        B.cm_compile_spec("region all : " + " || ".join(terms))
+    assert e.value.code == B.CM_ERR_PARSE and "limit 8" in str(e.value)

@@ -44,11 +44,11 @@ def _assert_close(name, got, want):
     return rel, mx
 
 
-def run_gpu(B, fwd_text, bwd_text, seg, nseg, Q, K, V, dO):
+def run_gpu(B, fwd_text, bwd_text, seg, nseg, Q, K, V, dO, form=0):
     f = B.cm_compile_spec(fwd_text)
     b = B.cm_compile_spec(bwd_text)
     Bn, H, S, d = Q.shape
-    desc = B.Descriptor(f, b, Bn, S)
+    desc = B.Descriptor(f, b, Bn, S, form=form)
     B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
     q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
     o, lse = B.attention_forward(desc, q, k, v)
@@ -183,41 +183,46 @@ def test_every_head_of_every_sample_with_full_schedule_chunks():
     check_heads(wid, seg, nseg, Q, K, V, dO, out, range(H))
 
 
-CHECKS = {"two_compare": 1, "masked": 2}
+# (check form, descriptor form) pairs other than the default (range masks, visible intervals):
+# the four arms of the paper's section 4.4 ablation and range masks over masked intervals
+ARMS = {"unsigned_visible": (0, 0), "two_compare_visible": (1, 0), "unsigned_masked": (0, 1),
+        "two_compare_masked": (1, 1), "range_masked": (3, 1)}
 
 
-@pytest.mark.parametrize("check", sorted(CHECKS))
+@pytest.mark.parametrize("arm", sorted(ARMS))
 @pytest.mark.parametrize("wid", [1, 3, 4, 5, 6])
-def test_interval_check_forms_small(wid, check):
-    """The two-compare and masked-interval forms of the partial-tile check (the paper's section
-    4.4 ablation) give the same attention as the oracle, on masks with 1 to 3 intervals per row."""
+def test_interval_check_forms_small(wid, arm):
+    """Every form of the partial-tile check, on visible and on masked Interval Tables, gives the
+    oracle's attention on masks with 1 to 3 intervals per row."""
     from masked_flashattention_gb300 import specs
     B = _lib()
+    check, form = ARMS[arm]
     S = 1024
     w = W.scaled(W.WORKLOADS[wid], S, B=2, H=2, d=128)
     seg, nseg = W.segments(wid, w.B, S, seed=31 + wid)
     Q, K, V, dO = W.full_tensors(w, seed=13 + wid)
-    B.cm_set_interval_check(CHECKS[check])
+    B.cm_set_interval_check(check)
     try:
-        out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO)
+        out = run_gpu(B, specs.FWD[wid], specs.BWD[wid], seg, nseg, Q, K, V, dO, form=form)
     finally:
-        B.cm_set_interval_check(B.CM_CHECK_UNSIGNED)
+        B.cm_set_interval_check(B.CM_CHECK_RANGE_MASK)
     check_heads(wid, seg, nseg, Q, K, V, dO, out, range(w.H))
 
 
-@pytest.mark.parametrize("check", sorted(CHECKS))
-def test_interval_check_forms_full_size_hstu(check):
-    """The ablation forms at the HSTU workload's full size (heads 0 and H-1 against the oracle)."""
+@pytest.mark.parametrize("arm", sorted(ARMS))
+def test_interval_check_forms_full_size_hstu(arm):
+    """The ablation arms at the HSTU workload's full size (heads 0 and H-1 against the oracle)."""
     from masked_flashattention_gb300 import specs
     B = _lib()
+    check, form = ARMS[arm]
     w = W.WORKLOADS[4]
     seg, nseg = W.segments(4, w.B, w.S)
     Q, K, V, dO = W.full_tensors(w)
-    B.cm_set_interval_check(CHECKS[check])
+    B.cm_set_interval_check(check)
     try:
-        out = run_gpu(B, specs.FWD[4], specs.BWD[4], seg, nseg, Q, K, V, dO)
+        out = run_gpu(B, specs.FWD[4], specs.BWD[4], seg, nseg, Q, K, V, dO, form=form)
     finally:
-        B.cm_set_interval_check(B.CM_CHECK_UNSIGNED)
+        B.cm_set_interval_check(B.CM_CHECK_RANGE_MASK)
     check_heads(4, seg, nseg, Q, K, V, dO, out, sorted({0, w.H - 1}))
 
 

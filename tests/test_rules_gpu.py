@@ -55,6 +55,35 @@ def _four_intervals(i, j, sg, n, S):
     return (j < 16) | ((j >= start[i]) & (j <= i)) | far
 
 
+def _heads_rule(p):
+    """Sink tokens [0, 16), the first 8 tokens of each of the p previous segments, and the own
+    segment causally: p + 2 visible intervals per row (CLEAR-style multi-interval rows)."""
+    fwd_terms = ["j < 16", "(j >= seg_start(i) && j <= i)"]
+    for m in range(1, p + 1):
+        fwd_terms.append(f"(j >= seg_start_at(seg_idx(i) - {m}) && "
+                         f"j < min(seg_start_at(seg_idx(i) - {m}) + 8, seg_end_at(seg_idx(i) - {m})))")
+    fwd = "region all : " + " || ".join(fwd_terms)
+    # key columns: sink keys are seen by every row; a key among the first 8 of its segment by the
+    # rows of the p following segments; every key by the later rows of its own segment
+    bwd = ("region i < 16 : j >= 0\n"
+           "region i < seg_start(i) + 8 : (j >= i && j < seg_end(i)) || "
+           f"(j >= seg_start_at(seg_idx(i) + 1) && j < seg_end_at(seg_idx(i) + {p}))\n"
+           "region all : j >= i && j < seg_end(i)")
+
+    def pred(i, j, sg, n, S):
+        k, start, _ = _seg_arrays(sg, n, S)
+        ki = k[i]
+        vis = (j < 16) | ((j >= start[i]) & (j <= i))
+        for m in range(1, p + 1):
+            km = ki - m
+            h0 = sg[np.clip(km, 0, n)]
+            h1 = np.minimum(h0 + 8, sg[np.clip(km + 1, 0, n)])
+            vis = vis | ((km >= 0) & (j >= h0) & (j < h1))
+        return vis
+
+    return (f"sink_{p}_previous_heads_and_own_segment", fwd, bwd, pred)
+
+
 RULES = [
     ("sliding_window_200",
      "region all : j > i - 200 && j <= i",
@@ -84,6 +113,10 @@ RULES = [
      "region i < seg_start(i) + 8 : (j >= i && j < seg_end(i)) || (j >= seg_start_at(seg_idx(i) + 1) && j < seg_end_at(seg_idx(i) + 2))\n"
      "region all : j >= i && j < seg_end(i)",
      _four_intervals),
+    # five, six and eight visible intervals per row (eight is the compiler's limit)
+    _heads_rule(3),
+    _heads_rule(4),
+    _heads_rule(6),
     ("causal_without_the_diagonal",
      "region i == 0 : j == 0\n"
      "region all : j < i",
@@ -113,7 +146,7 @@ def test_descriptor_matches_hand_predicate(rule, S):
     from masked_flashattention_gb300 import binding as B
     B.lib()
     name, ftxt, btxt, pred = rule
-    seg, nseg = W.random_segments(3, S, max_segs=6, seed=S + len(name))
+    seg, nseg = W.random_segments(3, S, max_segs=12, seed=S + len(name))
     desc = _build(B, ftxt, btxt, seg, nseg, S)
     itf, itb = desc.interval_table_fwd(), desc.interval_table_bwd()
     bmf, bmb = desc.bitmap_fwd(), desc.bitmap_bwd()
@@ -131,7 +164,7 @@ def test_attention_on_custom_rule(rule):
     B.lib()
     name, ftxt, btxt, pred = rule
     S, H, d = 1024, 2, 128
-    seg, nseg = W.random_segments(2, S, max_segs=5, seed=3)
+    seg, nseg = W.random_segments(2, S, max_segs=10, seed=3)
     desc = _build(B, ftxt, btxt, seg, nseg, S)
     w = W.Workload(0, name, 2, H, S, d)
     Q, K, V, dO = W.full_tensors(w, seed=11)
@@ -159,3 +192,57 @@ def test_four_interval_rule_uses_four_slots():
     rule = [r for r in RULES if r[0] == "sink_two_previous_heads_and_own_segment"][0]
     assert B.cm_spec_num_intervals(B.cm_compile_spec(rule[1])) == 4
     assert B.cm_spec_num_intervals(B.cm_compile_spec(rule[2])) == 2
+
+
+@pytest.mark.parametrize("p", [3, 4, 6])
+def test_multi_interval_rules_derive_their_interval_count(p):
+    """The compiler derives the interval count from the rule (no preset count): p previous-segment
+    heads, the sink and the own segment give p + 2 forward slots; the backward rule has 2."""
+    from masked_flashattention_gb300 import binding as B
+    B.lib()
+    _, ftxt, btxt, _ = _heads_rule(p)
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(ftxt)) == p + 2
+    assert B.cm_spec_num_intervals(B.cm_compile_spec(btxt)) == 2
+
+
+@pytest.mark.parametrize("rule", [r for r in RULES if r[0].startswith("sink_")],
+                         ids=lambda r: r[0])
+def test_multi_interval_rules_masked_form_and_per_score_checks(rule):
+    """Rules with 4 to 8 intervals per row (5 to 9 masked runs) with the per-score forms of the
+    check, on visible and on masked Interval Tables: attention equals the oracle."""
+    from masked_flashattention_gb300 import binding as B
+    B.lib()
+    name, ftxt, btxt, pred = rule
+    S, H, d = 1024, 1, 64
+    seg, nseg = W.random_segments(2, S, max_segs=12, seed=8)
+    f, b = B.cm_compile_spec(ftxt), B.cm_compile_spec(btxt)
+    w = W.Workload(0, name, 2, H, S, d)
+    Q, K, V, dO = W.full_tensors(w, seed=21)
+    q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
+    for check, form in ((B.CM_CHECK_UNSIGNED, B.CM_FORM_VISIBLE), (B.CM_CHECK_TWO_COMPARE, B.CM_FORM_MASKED),
+                        (B.CM_CHECK_RANGE_MASK, B.CM_FORM_MASKED)):
+        desc = B.Descriptor(f, b, 2, S, form=form)
+        B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
+        B.cm_set_interval_check(check)
+        try:
+            o, lse = B.attention_forward(desc, q, k, v)
+            dq, dk, dv = B.attention_backward(desc, q, k, v, o, lse, do)
+            torch.cuda.synchronize()
+        finally:
+            B.cm_set_interval_check(B.CM_CHECK_RANGE_MASK)
+        assert B.cm_get_status(desc) == B.CM_OK
+        for bb in range(2):
+            dense = _dense(pred, seg[bb], int(nseg[bb]), S)
+            if form == B.CM_FORM_MASKED:
+                nif = B.cm_spec_num_intervals(f)
+                np.testing.assert_array_equal(desc.interval_table_fwd()[bb],
+                                              M.masked_runs_table(dense, nif + 1))
+            ro, rl = A.attention_forward(Q[bb, 0], K[bb, 0], V[bb, 0], dense)
+            rq, rk, rv = A.attention_backward(Q[bb, 0], K[bb, 0], V[bb, 0], dO[bb, 0], dense)
+            for nm, got, want in (("O", o, ro), ("LSE", lse, rl), ("dQ", dq, rq), ("dK", dk, rk),
+                                  ("dV", dv, rv)):
+                g = got[bb, 0].double().cpu()
+                fin = torch.isfinite(want)
+                rel = ((g[fin] - want[fin]).norm() / want[fin].norm()).item()
+                mx = (g[fin] - want[fin]).abs().max().item()
+                assert rel <= 1e-2 and mx <= 3e-2, f"{name} {check}/{form} {nm} b{bb}: {rel:.3e} {mx:.3e}"
