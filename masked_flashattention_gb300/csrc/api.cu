@@ -180,6 +180,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.bm = desc->bm_f;
   p.sched = desc->sched_f;
   p.status = desc->status;
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.B = B;
@@ -192,7 +193,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.masked = desc->form;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_limit_ns.load();
-  return cm::launch_attn_fwd(p, d, q, k, v, static_cast<cudaStream_t>(stream)) == 0
+  return cm::launch_attn_fwd(p, d, k, v, static_cast<cudaStream_t>(stream)) == 0
              ? CM_OK
              : CM_ERR_CUDA;
 }
@@ -277,6 +278,8 @@ CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* 
   g.delta = static_cast<const float*>(workspace);
   g.lse2 = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
                                           row_floats_bytes(B, H, S));
+  g.q = static_cast<const __nv_bfloat16*>(q);
+  g.d_o = static_cast<const __nv_bfloat16*>(d_o);
   g.dq = static_cast<__nv_bfloat16*>(dq);
   g.B = B;
   g.H = H;
@@ -289,7 +292,7 @@ CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* 
   g.scale = scale;
   g.scale_log2 = scale * 1.4426950408889634f;
   g.wait_ns = g_wait_limit_ns.load();
-  return cm::launch_attn_dq(g, d, q, k, v, d_o, static_cast<cudaStream_t>(stream)) == 0
+  return cm::launch_attn_dq(g, d, k, v, static_cast<cudaStream_t>(stream)) == 0
              ? CM_OK
              : CM_ERR_CUDA;
 }

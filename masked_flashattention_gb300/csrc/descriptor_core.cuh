@@ -7,8 +7,8 @@
 //     builds at run time (section 3.1: the compiler generates a mask-specific preprocess kernel).
 //
 // Work is split into units of 4 tile rows (4 x 128 rows) of one (direction, sample); a block of
-// 4 warps takes units in turn (the grid is sized to be resident at once and launched
-// cooperatively).  Warp w of a unit owns one tile row, lane l its rows 4l .. 4l + 3:
+// 4 warps takes a contiguous range of units (the grid is sized to be resident at once and
+// launched cooperatively).  Warp w of a unit owns one tile row, lane l its rows 4l .. 4l + 3:
 //   1. the sample's segment boundaries are staged in shared memory and validated;
 //   2. the evaluator gives each slot's raw endpoints per row; they are clamped to [0, S] and kept
 //      as (start, end), with (0, 0) for padding, failed conditions and empty intervals.  The
@@ -170,8 +170,7 @@ __device__ __forceinline__ void add_ranges(int* cnt, const uint32_t (&key)[kRows
 // writes raw endpoints of the row's slots and leaves lo = hi = 0 in slots the row does not have.
 template <int NS, class Eval>
 __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, int b, int tile,
-                                        const int* seg_s, int nseg, int* cnt, uint8_t* code,
-                                        const Eval& ev) {
+                                        const int* seg_s, int nseg, int* cnt, const Eval& ev) {
   const int lane = threadIdx.x & 31;
   const int r0 = tile * kTile + lane * kRowsPerLane;
   const int spec_slots = dd.ni - p.masked;
@@ -301,12 +300,15 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
     add_ranges(cnt, cover, 1 << 16);
   }
   __syncwarp();
-  // prefix sum over the tiles: lane l owns tiles [l * per, (l + 1) * per); entries are cleared
-  // as they are read, so the array is zero again for the next tile row
-  const int per = (p.NT + 31) >> 5;
-  const int t0 = lane * per, t1 = imin(t0 + per, p.NT);
+  // prefix sum over the tiles: lane l owns tiles [l * per, (l + 1) * per), per a power of two;
+  // entries are cleared as they are read, so the array is zero again for the next tile row
+  int per = 1;
+  while (per * 32 < p.NT) per <<= 1;
+  const int t0 = lane * per;
   int run = 0;
-  for (int t = t0; t < t1; ++t) run += cnt[t];
+#pragma unroll 4
+  for (int q = 0; q < per; ++q)
+    if (t0 + q < p.NT) run += cnt[t0 + q];
   int incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -315,25 +317,35 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
   }
   int acc = incl - run;
   int nonempty = 0;
-  for (int t = t0; t < t1; ++t) {
-    acc += cnt[t];
-    cnt[t] = 0;
-    const int touched = acc & 0xFFFF;
-    const int covered = static_cast<int>(static_cast<uint32_t>(acc) >> 16);
-    code[t] = static_cast<uint8_t>(touched > 0 ? (covered == kTile ? 2 : 1) : 0);
-    nonempty += touched > 0 ? 1 : 0;
+  uint32_t frag_lo = 0, frag_hi = 0;  // 2-bit codes of this lane's tiles
+#pragma unroll 4
+  for (int q = 0; q < per; ++q) {
+    const int t = t0 + q;
+    if (t < p.NT) {
+      acc += cnt[t];
+      cnt[t] = 0;
+      const int touched = acc & 0xFFFF;
+      const int covered = static_cast<int>(static_cast<uint32_t>(acc) >> 16);
+      const uint32_t c = touched > 0 ? (covered == kTile ? 2u : 1u) : 0u;
+      if (q < 16) frag_lo |= c << (2 * q);
+      else frag_hi |= c << (2 * (q - 16));
+      nonempty += touched > 0 ? 1 : 0;
+    }
   }
   if (lane == 0) cnt[p.NT] = 0;
   nonempty = __reduce_add_sync(0xFFFFFFFFu, nonempty);
-  __syncwarp();
+  // bitmap words: 16 tiles each, from the lanes' code fragments
   uint32_t* out = dd.bm + (static_cast<unsigned long long>(b) * p.NT + tile) * p.W;
-  for (int w = lane; w < p.W; w += 32) {
-    uint32_t word = 0;
-    for (int q = 0; q < 16; ++q) {
-      const int t = w * 16 + q;
-      if (t < p.NT) word |= static_cast<uint32_t>(code[t]) << (2 * q);
-    }
-    out[w] = word;
+  if (per >= 16) {
+    const int w0 = t0 >> 4;
+    if (w0 < p.W) out[w0] = frag_lo;
+    if (per == 32 && w0 + 1 < p.W) out[w0 + 1] = frag_hi;
+  } else {
+    const int lanes = 16 / per;  // lanes per word (a power of two)
+    uint32_t word = frag_lo << (2 * per * (lane & (lanes - 1)));
+    for (int o = 1; o < lanes; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
+    const int w = lane / lanes;
+    if ((lane & (lanes - 1)) == 0 && w < p.W) out[w] = word;
   }
   __syncwarp();
   return nonempty;
@@ -342,9 +354,8 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
 // Dynamic shared memory of the kernel, in ints.
 __host__ __device__ __forceinline__ int seg_ints(int nseg_max) { return (nseg_max + 1 + 3) & ~3; }
 __host__ __device__ __forceinline__ int cnt_ints(int NT) { return (NT + 1 + 3) & ~3; }
-__host__ __device__ __forceinline__ int code_ints(int NT) { return (NT + 3) >> 2; }
 __host__ __device__ __forceinline__ int smem_ints(int nseg_max, int NT, int units_per_block) {
-  return seg_ints(nseg_max) + kWarps * (cnt_ints(NT) + code_ints(NT)) + 2 * kWarps * units_per_block;
+  return seg_ints(nseg_max) + kWarps * cnt_ints(NT) + 2 * kWarps * units_per_block;
 }
 
 template <int NSF, int NSB, class EvalF, class EvalB>
@@ -356,17 +367,19 @@ __device__ __forceinline__ void descriptor_kernel(const DescCore& p, const EvalF
   int* seg_s = smem_i;
   int* cnt_all = seg_s + seg_ints(p.nseg_max);
   int* cnt = cnt_all + warp * cnt_ints(p.NT);
-  uint8_t* code = reinterpret_cast<uint8_t*>(cnt_all + kWarps * cnt_ints(p.NT)) +
-                  warp * 4 * code_ints(p.NT);
-  int2* items = reinterpret_cast<int2*>(cnt_all + kWarps * (cnt_ints(p.NT) + code_ints(p.NT)));
+  int2* items = reinterpret_cast<int2*>(cnt_all + kWarps * cnt_ints(p.NT));
   int* hist = p.work + 2;
 
   for (int t = lane; t < cnt_ints(p.NT); t += 32) cnt[t] = 0;
 
   // ---- phase 1: tile rows ---------------------------------------------------------------------
+  // block x takes the contiguous units [x * units_per_block, ...): consecutive units mostly share
+  // a sample, so its segment boundaries are staged once for many tile rows
   const int per_dir = p.B * p.groups;
+  const int u_begin = blockIdx.x * p.units_per_block;
+  const int u_end = imin(u_begin + p.units_per_block, 2 * per_dir);
   int cur_b = -1, nseg = 1, u = 0;
-  for (int unit = blockIdx.x; unit < 2 * per_dir; unit += gridDim.x, ++u) {
+  for (int unit = u_begin; unit < u_end; ++unit, ++u) {
     const int d = unit >= per_dir ? 1 : 0;
     const int rem = unit - d * per_dir;
     const int b = rem / p.groups, g = rem - b * p.groups;
@@ -388,21 +401,26 @@ __device__ __forceinline__ void descriptor_kernel(const DescCore& p, const EvalF
       cur_b = b;
     }
     const int tile = g * kWarps + warp;
+    int2 it = make_int2(-1, 0);
     if (tile < p.NT) {
-      const int c = d == 0 ? tile_row<NSF>(p, p.dir[0], b, tile, seg_s, nseg, cnt, code, evf)
-                           : tile_row<NSB>(p, p.dir[1], b, tile, seg_s, nseg, cnt, code, evb);
-      if (lane == 0) {
-        const int ticket = atomicAdd(&hist[d * (p.NT + 1) + c], 1);
-        items[u * kWarps + warp] = make_int2(static_cast<int>((static_cast<uint32_t>(d) << 31) |
-                                                              (static_cast<uint32_t>(b) << 16) |
-                                                              static_cast<uint32_t>(tile)),
-                                             (c << 16) | ticket);
-      }
-    } else if (lane == 0) {
-      items[u * kWarps + warp] = make_int2(-1, 0);
+      const int c = d == 0 ? tile_row<NSF>(p, p.dir[0], b, tile, seg_s, nseg, cnt, evf)
+                           : tile_row<NSB>(p, p.dir[1], b, tile, seg_s, nseg, cnt, evb);
+      it = make_int2(static_cast<int>((static_cast<uint32_t>(d) << 31) |
+                                      (static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(tile)),
+                     c);
     }
+    if (lane == 0) items[u * kWarps + warp] = it;
   }
   const int n_items = u * kWarps;
+  // tickets in the per-direction histograms, taken together so that their latencies overlap
+  __syncthreads();
+  for (int x = threadIdx.x; x < n_items; x += kThreads) {
+    const int2 it = items[x];
+    if (it.x == -1) continue;
+    const int d = static_cast<int>(static_cast<uint32_t>(it.x) >> 31);
+    const int ticket = atomicAdd(&hist[d * (p.NT + 1) + it.y], 1);
+    items[x].y = (it.y << 16) | ticket;
+  }
 
   // ---- phase 2: schedules ----------------------------------------------------------------------
   grid_barrier(p);

@@ -152,8 +152,8 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_ke
   // Size the shared memory for the most units a block can take when the grid is as small as it
   // can be (one block per SM), then fill every SM with as many blocks as fit at that size: every
   // block must be resident at once for the grid barrier (cooperative launch).
-  c.units_per_block = (units + sms - 1) / sms;
-  const size_t smem = static_cast<size_t>(cmcore::smem_ints(nseg_max, NT, c.units_per_block)) * 4;
+  const int upb_max = (units + sms - 1) / sms;
+  const size_t smem = static_cast<size_t>(cmcore::smem_ints(nseg_max, NT, upb_max)) * 4;
   if (smem > 200 * 1024) return -1;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -166,7 +166,9 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_ke
     cudaGetLastError();
     per_sm = 1;
   }
-  const int grid = units < per_sm * sms ? units : per_sm * sms;
+  int grid = units < per_sm * sms ? units : per_sm * sms;
+  c.units_per_block = (units + grid - 1) / grid;  // <= upb_max, since grid >= min(units, sms)
+  grid = (units + c.units_per_block - 1) / c.units_per_block;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(cmcore::kThreads);
