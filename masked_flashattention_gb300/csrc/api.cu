@@ -180,7 +180,6 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.bm = desc->bm_f;
   p.sched = desc->sched_f;
   p.status = desc->status;
-  p.q = static_cast<const __nv_bfloat16*>(q);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.B = B;
@@ -193,7 +192,7 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
   p.masked = desc->form;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_limit_ns.load();
-  return cm::launch_attn_fwd(p, d, k, v, static_cast<cudaStream_t>(stream)) == 0
+  return cm::launch_attn_fwd(p, d, q, k, v, static_cast<cudaStream_t>(stream)) == 0
              ? CM_OK
              : CM_ERR_CUDA;
 }

@@ -21,7 +21,6 @@ struct FwdParams {
   const uint32_t* bm;    // forward bitmaps [B][NT][W]
   const int32_t* sched;  // (b << 16 | q_tile), longest first
   int32_t* status;
-  const __nv_bfloat16* q;  // read once per CTA into TMEM
   __nv_bfloat16* o;
   float* lse;
   int B, H, S, NT, W, NI;
@@ -78,7 +77,8 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_ke
                       int32_t* itab_f, uint32_t* bm_f, int32_t* itab_b, uint32_t* bm_b,
                       int32_t* sched_f, int32_t* sched_b, int32_t* work, int masked,
                       uint64_t wait_ns, cudaStream_t stream);
-int launch_attn_fwd(const FwdParams& p, int d, const void* k, const void* v, cudaStream_t stream);
+int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
+                    cudaStream_t stream);
 // Backward prologue: per row -D = -rowsum(dO * O) and -LSE * log2(e) (rows = B * H * S).
 int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse, float* delta,
                         float* lse2, size_t rows, cudaStream_t stream);
