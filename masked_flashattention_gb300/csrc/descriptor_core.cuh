@@ -140,6 +140,10 @@ __device__ __forceinline__ void grid_barrier(const DescCore& p) {
   __syncthreads();
 }
 
+// Index of tile entry t in a warp's difference array: one padding word per 32 entries, so that the
+// prefix pass (lane l walks entries [l * per, (l + 1) * per)) reads 32 different banks.
+__device__ __forceinline__ int cidx(int t) { return t + (t >> 5); }
+
 // Adds `unit` rows over the tile range [key >> 16, key & 0xFFFF) of the warp's difference array
 // for each of the lane's 4 rows (key 0xFFFFFFFF: no range).  When the 4 rows agree, lanes with
 // the same range are added together by one leader.  Call with the whole warp.
@@ -151,15 +155,15 @@ __device__ __forceinline__ void add_ranges(int* cnt, const uint32_t (&key)[kRows
   if (same) {
     if (k0 != 0xFFFFFFFFu && lane == __ffs(grp) - 1) {
       const int w = kRowsPerLane * __popc(grp) * unit;
-      atomicAdd(&cnt[k0 >> 16], w);
-      atomicAdd(&cnt[k0 & 0xFFFF], -w);
+      atomicAdd(&cnt[cidx(k0 >> 16)], w);
+      atomicAdd(&cnt[cidx(k0 & 0xFFFF)], -w);
     }
   } else {
 #pragma unroll
     for (int q = 0; q < kRowsPerLane; ++q)
       if (key[q] != 0xFFFFFFFFu) {
-        atomicAdd(&cnt[key[q] >> 16], unit);
-        atomicAdd(&cnt[key[q] & 0xFFFF], -unit);
+        atomicAdd(&cnt[cidx(key[q] >> 16)], unit);
+        atomicAdd(&cnt[cidx(key[q] & 0xFFFF)], -unit);
       }
   }
 }
@@ -308,7 +312,7 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
   int run = 0;
 #pragma unroll 4
   for (int q = 0; q < per; ++q)
-    if (t0 + q < p.NT) run += cnt[t0 + q];
+    if (t0 + q < p.NT) run += cnt[cidx(t0 + q)];
   int incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -322,8 +326,8 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
   for (int q = 0; q < per; ++q) {
     const int t = t0 + q;
     if (t < p.NT) {
-      acc += cnt[t];
-      cnt[t] = 0;
+      acc += cnt[cidx(t)];
+      cnt[cidx(t)] = 0;
       const int touched = acc & 0xFFFF;
       const int covered = static_cast<int>(static_cast<uint32_t>(acc) >> 16);
       const uint32_t c = touched > 0 ? (covered == kTile ? 2u : 1u) : 0u;
@@ -332,7 +336,7 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
       nonempty += touched > 0 ? 1 : 0;
     }
   }
-  if (lane == 0) cnt[p.NT] = 0;
+  if (lane == 0) cnt[cidx(p.NT)] = 0;
   nonempty = __reduce_add_sync(0xFFFFFFFFu, nonempty);
   // bitmap words: 16 tiles each, from the lanes' code fragments
   uint32_t* out = dd.bm + (static_cast<unsigned long long>(b) * p.NT + tile) * p.W;
@@ -353,7 +357,7 @@ __device__ __forceinline__ int tile_row(const DescCore& p, const DescDir& dd, in
 
 // Dynamic shared memory of the kernel, in ints.
 __host__ __device__ __forceinline__ int seg_ints(int nseg_max) { return (nseg_max + 1 + 3) & ~3; }
-__host__ __device__ __forceinline__ int cnt_ints(int NT) { return (NT + 1 + 3) & ~3; }
+__host__ __device__ __forceinline__ int cnt_ints(int NT) { return (NT + 1 + (NT >> 5) + 3) & ~3; }
 __host__ __device__ __forceinline__ int smem_ints(int nseg_max, int NT, int units_per_block) {
   return seg_ints(nseg_max) + kWarps * cnt_ints(NT) + 2 * kWarps * units_per_block;
 }
