@@ -19,13 +19,15 @@
 //              scale*log2e - LSE*log2e) stays in registers while dP is computed into the same
 //              TMEM columns, then dS = P * (dP - D) is written back there as bf16 pairs.
 //   warp 8     TMA producer: K through a 3-slot ring, V through a 2-slot ring.
-//   warp 9     MMA issuer (one thread).
+//   warps 9-10 MMA issuers, one thread each: the thread of warp 9 + t issues S(n), dP(n) and
+//              dQ(n) of the key tiles n with n % 2 == t.  A thread that issues tcgen05 MMAs
+//              stalls on every barrier wait, and the tensor pipe holds too few queued 128 x 128
+//              MMAs to cover the stall: with two issuers one thread's MMAs run while the other
+//              waits.
 // TMEM (512 columns): X0 [0,128), X1 [128,256) (key tile n uses X(n % 2) for S(n), then dP(n),
-// then dS(n)), dQ [256, 256+d), Q [384, 384+d/2), dO [448, 448+d/2).  The MMA issues, once dS(n)
-// is written: dQ(n), then dP(n+1) (when S(n+1) has been read), then S(n+2) into X(n % 2), so the
-// tensor pipe has the next tile's dP queued while the compute warps form dS.  A buffer is
-// rewritten only by MMAs issued after the ones that read it: tcgen05 MMAs of one thread run in
-// issue order.
+// then dS(n)), dQ [256, 256+d), Q [384, 384+d/2), dO [448, 448+d/2).  Buffer X(t) belongs to the
+// tiles of issuer t, which rewrites it only with MMAs issued after the ones that read it
+// (tcgen05 MMAs of one thread run in issue order).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -40,8 +42,8 @@ namespace dq {
 
 constexpr int kComputeWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 9;  // and 10
+constexpr int kThreads = 352;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 
@@ -72,9 +74,9 @@ enum {
   B_SREAD = 13,   // +buffer (2): compute warps hold S in registers (8 arrivals)
   B_DPFULL = 15,  // +buffer (2): dP of the buffer's tile computed
   B_DSFULL = 17,  // +buffer (2): compute warps wrote dS (8 arrivals)
-  B_DONE = 19,    // every MMA of the CTA completed
-  B_DRAIN = 20,   // abort path only: every MMA issued so far has completed
-  B_COUNT = 21
+  B_DONE = 19,    // every MMA of the CTA completed (one commit per issuer)
+  B_DRAIN = 20,   // +issuer, abort path only: every MMA the issuer issued has completed
+  B_COUNT = 22
 };
 
 // Row `row` of a [rows][D] bf16 matrix, this warp's half of its bf16 pairs, into TMEM at `taddr`.
@@ -156,8 +158,9 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(bar(B_DPFULL + s), 1);
       mbar_init(bar(B_DSFULL + s), kComputeWarps);
     }
-    mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_DONE), 2);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -208,9 +211,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                       row0 + kt * 128, bar(B_VFULL + sv));
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ---------------------------------------------------------------- MMA issuers
+    const int par = warp - kMmaWarp;  // this thread's key tiles: n % 2 == par, buffer X(par)
+    if (lane == 0 && nt > par) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t idQ = make_idesc_bf16(128, D, 0, 1);    // dQ += dS K
       auto issue_s = [&](int n) -> bool {  // S(n) into X(n % 2)
@@ -240,12 +244,15 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         umma_commit(bar(B_VEMPTY + sv));
         return true;
       };
-      bool ok = wait(bar(B_QDO), 0, 0x305);
-      if (ok) tc_fence_after();
-      ok = ok && issue_s(0) && (nt < 2 || issue_s(1)) && issue_dp(0);
-      for (int n = 0; ok && n < nt; ++n) {
-        // dQ += dS(n) K(n): dS pairs of keys [0,64) at X columns [0,32), [64,128) at [64,96)
-        if (!wait(bar(B_DSFULL + (n & 1)), (n >> 1) & 1, 0x307)) break;
+      // dQ += dS(n) K(n): dS pairs of keys [0,64) at X columns [0,32), [64,128) at [64,96).
+      // dQ(n-1) was issued by the other thread: dQ(n) waits until it has completed (its K slot's
+      // release), so the accumulations never overlap.  That barrier cannot run a phase ahead of
+      // this wait: dQ(n+2) needs dQ(n+1), which needs dQ(n).
+      auto issue_dq = [&](int n) -> bool {
+        if (!wait(bar(B_DSFULL + (n & 1)), (n >> 1) & 1, 0x307)) return false;
+        if (n >= 1 &&
+            !wait(bar(B_KEMPTY + (n - 1) % kKStages), ((n - 1) / kKStages) & 1, 0x30a))
+          return false;
         tc_fence_after();
         const int sk = n % kKStages;
         const uint32_t dK = sdesc_lo(sbase + L::kK + sk * L::kTileBytes, 16384u);
@@ -255,11 +262,16 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           umma_ts_lo(tmem + kColDQ, sX + 64 * (kk >> 2) + 8 * (kk & 3), dK + kstep_mnmajor(kk), idQ,
                      (n > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_KEMPTY + sk));
-        // the next tile's dP before S(n+2): the compute warps are waiting for it
-        if (n + 1 < nt && !issue_dp(n + 1)) break;
-        if (n + 2 < nt && !issue_s(n + 2)) break;
-        if (n + 1 == nt) umma_commit(bar(B_DONE));
-      }
+        return true;
+      };
+      bool ok = wait(bar(B_QDO), 0, 0x305);
+      if (ok) tc_fence_after();
+      // own tiles in order: S(n), dP(n) once S(n) is read, dQ(n) once dS(n) is written; S(n+2)
+      // reuses X(par) after dQ(n) read it (tcgen05 MMAs of one thread run in issue order)
+      for (int n = par; ok && n < nt; n += 2) ok = issue_s(n) && issue_dp(n) && issue_dq(n);
+      if (ok) umma_commit(bar(B_DONE));
+    } else if (lane == 0 && nt > 0) {
+      umma_commit(bar(B_DONE));  // a second issuer with no tile (nt == 1) still signs off
     }
   } else {
     // ---------------------------------------------------------------- compute warps 0-7
@@ -387,9 +399,9 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       for (int s = 0; s < kVStages && s < nv_armed; ++s)
         mbar_wait_drain(bar(B_VFULL + s), ((nv_armed - 1 - s) / kVStages) & 1, p.status, 0x3f2);
     }
-    if (warp == kMmaWarp && lane == 0 && mma_issued) {
-      umma_commit(bar(B_DRAIN));
-      mbar_wait_drain(bar(B_DRAIN), 0, p.status, 0x3f3);
+    if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0 && mma_issued) {
+      umma_commit(bar(B_DRAIN + warp - kMmaWarp));
+      mbar_wait_drain(bar(B_DRAIN + warp - kMmaWarp), 0, p.status, 0x3f3);
     }
     __syncthreads();
   }

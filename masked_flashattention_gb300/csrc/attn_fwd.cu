@@ -21,12 +21,19 @@
 //              running max moved, and at the end merges the halves and writes O and the LSE.
 //   warp 8     TMA producer: Q once, then K and V of each visited key tile into one of 3 stages
 //              (one barrier for both tiles; the stage frees when the tile's PV MMAs completed).
-//   warp 9     MMA issuer (one thread): S = Q K^T (Q and K from shared memory) and, per half,
-//              O_h += P_h V_h with P_h read from TMEM.
+//   warps 9-10 MMA issuers, one thread each: the thread of warp 9 + t issues the MMAs of the key
+//              tiles n with n % 2 == t: S(n) = Q K(n)^T (Q and K from shared memory) and, per
+//              half, O_h += P_h(n) V_h(n) with P_h read from TMEM.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O_0 [256, 256+d), O_1 [384, 384+d).  P of tile n
 // lives in S buffer n % 2: keys [0,64) in columns [0,32), keys [64,128) in [64,96).
-// Ordering without extra barriers: the MMA issues S(n+2) into a buffer only after it saw P(n) and
-// issued PV(n), which reads P(n) from that buffer; tcgen05 MMAs of one thread run in issue order.
+// Why two issuers: a thread that issues tcgen05 MMAs stalls on every barrier wait (even on a phase
+// that is already complete), and the tensor pipe holds too few queued 128 x 128 MMAs to cover
+// the stall, so a single issuer leaves a gap in the pipe at each wait.  With the tiles dealt by
+// parity, one thread's MMAs run while the other waits.
+// Ordering: a thread issues S(n+2) into a buffer right after PV(n), which reads P(n) from that
+// buffer (tcgen05 MMAs of one thread run in issue order).  PV(n) accumulates into the O_h that
+// PV(n-1) of the other thread updates, so it is issued only after PV(n-1) has completed (the
+// stage barrier of tile n-1): the accumulations never overlap.
 // The softmax warps wait for PV(n-1) (its stage's release) only when they must rescale O: the
 // completion of S(n), which they wait for anyway, already covers every PV issued before it (up to
 // PV(n-2)).
@@ -46,8 +53,8 @@ namespace fwd {
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 9;   // and 10
+constexpr int kThreads = 352;
 constexpr int kStages = 3;  // K ring and V ring depth
 
 constexpr uint32_t kColS = 0;
@@ -65,19 +72,17 @@ struct Smem {
 };
 static_assert(Smem<128>::kAlloc <= 232448, "forward shared memory exceeds 227 KB");
 
-// The MMA thread waits twice per key tile (P ready, next K/V landed) and commits twice (S ready,
-// PV done): every wait of the issuing thread leaves a gap in the tensor pipe, so the barriers are
-// shared where the ordering allows it.
 enum {
   B_Q = 0,        // Q tile in shared memory (TMA)
   B_KVFULL = 1,   // +stage: K and V of a key tile landed (TMA, 2 tiles of bytes)
-  B_KVEMPTY = 4,  // +stage: S and PV of the stage's tile have completed (also "O is up to date")
+  B_KVEMPTY = 4,  // +stage: S and PV of the stage's tile have completed (also "O is up to date",
+                  // and the other issuer's go-ahead for the next PV)
   B_SFULL = 7,    // +buffer
   B_PFULL = 9,    // +buffer: P of a tile in that S buffer, both halves (8 arrivals)
   B_PAIR = 11,    // +quarter: merge exchange of a warp pair (2 arrivals, once)
-  B_ALLDONE = 15, // every MMA of the CTA has completed (once)
-  B_DRAIN = 16,   // abort path only: every MMA issued so far has completed
-  B_COUNT = 17
+  B_ALLDONE = 15, // every MMA of the CTA has completed (once; one commit per issuer)
+  B_DRAIN = 16,   // +issuer, abort path only: every MMA the issuer issued so far has completed
+  B_COUNT = 18
 };
 
 template <int D, int MAXNI>
@@ -124,8 +129,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar(B_PFULL + s), kSoftmaxWarps);
     }
     for (int s = 0; s < 4; ++s) mbar_init(bar(B_PAIR + s), 2);
-    mbar_init(bar(B_ALLDONE), 1);
+    mbar_init(bar(B_ALLDONE), 2);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -180,9 +186,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                       bar(B_KVFULL + st));
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ---------------------------------------------------------------- MMA issuers
+    const int par = warp - kMmaWarp;  // this thread's key tiles: n % 2 == par
+    if (lane == 0 && nt > par) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // A = Q, B = K, both K-major
       constexpr uint32_t idO = make_idesc_bf16(128, D, 0, 1);    // A = P (TMEM), B = V MN-major
       const uint32_t dQ = sdesc_lo(sbase + L::kQ, 16u);
@@ -194,6 +201,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // one barrier per S buffer: the softmax warps can be at most one tile ahead of this
         // wait, so a barrier never runs two phases ahead of its waiter
         if (!wait(bar(B_PFULL + (m & 1)), (m >> 1) & 1, 0x103))
+          return false;
+        // PV(m-1), issued by the other thread, has completed.  Its stage barrier cannot run a
+        // phase ahead of this wait: PV(m+2) of that stage needs PV(m+1), which needs PV(m).
+        if (m >= 1 &&
+            !wait(bar(B_KVEMPTY + (m - 1) % kStages), ((m - 1) / kStages) & 1, 0x104))
           return false;
         tc_fence_after();
         const uint32_t dV = sdesc_lo(sbase + L::kKV + st * 2u * L::kTileBytes + L::kTileBytes, 16384u);
@@ -226,14 +238,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         umma_commit(bar(B_SFULL + (n & 1)));
         return true;
       };
-      // Both S buffers first; then per tile: PV(n) as soon as its P is written, and S(n+2) into
-      // the buffer PV(n) reads, right behind it.  The thread waits for P with nothing queued
-      // behind the wait, so it issues PV the moment P arrives.
-      ok = ok && issue_s(0) && (nt < 2 || issue_s(1));
-      for (int n = 0; ok && n < nt; ++n) {
+      // S(par) first; then per own tile n: PV(n) once P(n) is written and PV(n-1) is done, and
+      // S(n+2) into the buffer PV(n) reads, right behind it.
+      ok = ok && issue_s(par);
+      for (int n = par; ok && n < nt; n += 2) {
         ok = issue_pv(n) && (n + 2 >= nt || issue_s(n + 2));
       }
       if (ok) umma_commit(bar(B_ALLDONE));
+    } else if (lane == 0 && nt > 0) {
+      umma_commit(bar(B_ALLDONE));  // a second issuer with no tile (nt == 1) still signs off
     }
   } else {
     // ---------------------------------------------------------------- softmax warps 0-7
@@ -404,9 +417,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int s = 0; s < kStages && s < n_armed; ++s)
         mbar_wait_drain(bar(B_KVFULL + s), ((n_armed - 1 - s) / kStages) & 1, p.status, 0x1f1);
     }
-    if (warp == kMmaWarp && lane == 0 && mma_issued) {
-      umma_commit(bar(B_DRAIN));
-      mbar_wait_drain(bar(B_DRAIN), 0, p.status, 0x1f2);
+    if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0 && mma_issued) {
+      umma_commit(bar(B_DRAIN + warp - kMmaWarp));
+      mbar_wait_drain(bar(B_DRAIN + warp - kMmaWarp), 0, p.status, 0x1f2);
     }
     __syncthreads();
   }
