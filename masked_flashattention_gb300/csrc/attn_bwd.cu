@@ -266,6 +266,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
+      // low words of the shared-memory descriptors (the split form keeps the issue loop short:
+      // the issuing thread shares its SM sub-partition with two compute warps, and every
+      // instruction it needs between MMAs leaves the tensor pipe waiting longer)
+      const uint32_t dK0 = sdesc_lo(sK, 16u), dV0 = sdesc_lo(sV, 16u);
+      const uint32_t dQ0 = sdesc_lo(sbase + L::kQ, 16u), ddO0 = sdesc_lo(sbase + L::kdO, 16u);
       // tile 0: S^T -> RA, dP^T -> RB
       bool ok = wait(bar(B_KV), 0, 0x202) &&
                 wait(bar(B_QFULL), 0, 0x203);
@@ -274,16 +279,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_issued = true;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColRA, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sbase + L::kQ, kk, 16384u),
-                  idSS, kk > 0 ? 1u : 0u);
+          umma_ss_lo(tmem + kColRA, dK0 + kstep_kmajor(kk), dQ0 + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL));
       }
       if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColRB, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sbase + L::kdO, kk, 16384u),
-                  idSS, kk > 0 ? 1u : 0u);
+          umma_ss_lo(tmem + kColRB, dV0 + kstep_kmajor(kk), ddO0 + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_DPFULL));
       }
       for (int m = 0; ok && m < nt; ++m) {
@@ -297,8 +300,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                  sdesc_mnmajor(sdO, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_lo(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                     sdesc_lo(sdO, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
         if (!wait(bar(B_PDS), m & 1, 0x205)) break;
         tc_fence_after();
         if (m + 1 < nt) {
@@ -310,15 +313,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + Y, sdesc_kmajor(sK, kk, 16384u), sdesc_kmajor(sQn, kk, 16384u), idSS,
-                    kk > 0 ? 1u : 0u);
+            umma_ss_lo(tmem + Y, dK0 + kstep_kmajor(kk), sdesc_lo(sQn, 16u) + kstep_kmajor(kk), idSS,
+                       kk > 0 ? 1u : 0u);
           umma_commit(bar(B_SFULL));
         }
         // dK += dS^T Q with dS^T read from X: queries [64h + 32c, +32) at columns 64h + 32 + 16c
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDK, tmem + X + 64 * (kk >> 2) + 32 + 8 * (kk & 3),
-                  sdesc_mnmajor(sQ, kk, 16384u), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_lo(tmem + kColDK, tmem + X + 64 * (kk >> 2) + 32 + 8 * (kk & 3),
+                     sdesc_lo(sQ, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_QEMPTY + (m & 1)));
         if (m + 1 < nt) {
           // dP^T of the next tile into X, after dV and dK above have read P^T and dS^T from it
@@ -326,8 +329,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + X, sdesc_kmajor(sV, kk, 16384u), sdesc_kmajor(sdOn, kk, 16384u), idSS,
-                    kk > 0 ? 1u : 0u);
+            umma_ss_lo(tmem + X, dV0 + kstep_kmajor(kk), sdesc_lo(sdOn, 16u) + kstep_kmajor(kk), idSS,
+                       kk > 0 ? 1u : 0u);
           umma_commit(bar(B_DPFULL));
         } else {
           umma_commit(bar(B_DONE));
