@@ -428,29 +428,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
     if (done) {
       tc_fence_after();
+      const float sc = p.scale;
+      // dV, then dK (scaled), as bf16 pairs of this row's columns, stored a warp's 32 rows at a
+      // time with coalesced stores
 #pragma unroll
-      for (int c = 0; c < kHalf; c += 32) {
-        uint32_t a[32], k2[32];
-        tmem_ld32(tmem + lane_off + kColDV + hf * kHalf + c, a);
-        tmem_ld32(tmem + lane_off + kColDK + hf * kHalf + c, k2);
-        tmem_wait_ld();
-        uint4* dva = reinterpret_cast<uint4*>(dvrow + c);
-        uint4* dka = reinterpret_cast<uint4*>(dkrow + c);
-        const float sc = p.scale;
+      for (int x = 0; x < 2; ++x) {
+        uint32_t ob[kHalf / 2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 x, y;
-          x.x = pack_bf16x2(__uint_as_float(a[8 * q + 0]), __uint_as_float(a[8 * q + 1]));
-          x.y = pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3]));
-          x.z = pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5]));
-          x.w = pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7]));
-          y.x = pack_bf16x2(__uint_as_float(k2[8 * q + 0]) * sc, __uint_as_float(k2[8 * q + 1]) * sc);
-          y.y = pack_bf16x2(__uint_as_float(k2[8 * q + 2]) * sc, __uint_as_float(k2[8 * q + 3]) * sc);
-          y.z = pack_bf16x2(__uint_as_float(k2[8 * q + 4]) * sc, __uint_as_float(k2[8 * q + 5]) * sc);
-          y.w = pack_bf16x2(__uint_as_float(k2[8 * q + 6]) * sc, __uint_as_float(k2[8 * q + 7]) * sc);
-          dva[q] = x;
-          dka[q] = y;
+        for (int c = 0; c < kHalf; c += 32) {
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_off + (x == 0 ? kColDV : kColDK) + hf * kHalf + c, a);
+          tmem_wait_ld();
+          const float f = x == 0 ? 1.f : sc;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            ob[(c + e) / 2] = pack_bf16x2(__uint_as_float(a[e]) * f, __uint_as_float(a[e + 1]) * f);
         }
+        __nv_bfloat16* rowp = x == 0 ? dvrow : dkrow;
+        store_rows_coalesced<kHalf / 8>(
+            ob, reinterpret_cast<char*>(rowp - static_cast<size_t>(lane) * D), D * 2u, lane);
       }
     } else {
       uint4* dva = reinterpret_cast<uint4*>(dvrow);

@@ -365,22 +365,19 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (done) {
       tc_fence_after();
       const float sc = p.scale;
+      uint32_t ob[kHalf / 2];  // this row's dQ columns as bf16 pairs
 #pragma unroll
       for (int c = 0; c < kHalf; c += 32) {
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + kColDQ + hf * kHalf + c, a);
         tmem_wait_ld();
-        uint4* dst = reinterpret_cast<uint4*>(qrow + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 x;
-          x.x = pack_bf16x2(__uint_as_float(a[8 * q + 0]) * sc, __uint_as_float(a[8 * q + 1]) * sc);
-          x.y = pack_bf16x2(__uint_as_float(a[8 * q + 2]) * sc, __uint_as_float(a[8 * q + 3]) * sc);
-          x.z = pack_bf16x2(__uint_as_float(a[8 * q + 4]) * sc, __uint_as_float(a[8 * q + 5]) * sc);
-          x.w = pack_bf16x2(__uint_as_float(a[8 * q + 6]) * sc, __uint_as_float(a[8 * q + 7]) * sc);
-          dst[q] = x;
-        }
+        for (int e = 0; e < 32; e += 2)
+          ob[(c + e) / 2] = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
       }
+      // rows quarter*32 .. +31 of the tile, this warp's dQ columns
+      store_rows_coalesced<kHalf / 8>(
+          ob, reinterpret_cast<char*>(qrow - static_cast<size_t>(lane) * D), D * 2u, lane);
     } else {
       uint4* dst = reinterpret_cast<uint4*>(qrow);
       for (int q = 0; q < kHalf / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);

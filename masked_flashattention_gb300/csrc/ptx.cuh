@@ -351,6 +351,46 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ----------------------------------------------------------------------------------------------
+// coalesced row stores
+// ----------------------------------------------------------------------------------------------
+// A warp holds 32 consecutive rows of a tile, one per lane (lane t: row t), each as NC 16-byte
+// chunks in w[4c .. 4c+3].  Stored as they are, every store instruction would touch 32 rows (32
+// memory segments).  Instead, within each group of NC lanes the chunks are transposed with three
+// (NC = 8) or two (NC = 4) rounds of butterfly shuffles: at distance d, lane pairs (l, l ^ d)
+// swap the chunks whose index differs from their lane in bit d.  Afterwards lane NC*G + c holds
+// chunk c of rows NC*G + q in w[4q .. 4q+3], and one store instruction writes 32/NC whole row
+// segments of NC * 16 bytes.  `base` is the address of row 0's first chunk for this warp.
+template <int NC>
+__device__ __forceinline__ void store_rows_coalesced(uint32_t (&w)[4 * NC], char* base,
+                                                     size_t row_stride, int lane) {
+  static_assert(NC == 4 || NC == 8, "chunks per row segment");
+#pragma unroll
+  for (int d = 1; d < NC; d <<= 1) {
+    const bool up = (lane & d) != 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (j & d) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t x = up ? w[4 * j + e] : w[4 * (j | d) + e];
+        const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, d);
+        if (up) {
+          w[4 * j + e] = y;
+        } else {
+          w[4 * (j | d) + e] = y;
+        }
+      }
+    }
+  }
+  const int c = lane % NC, g0 = lane - c;  // chunk of this lane, first row of its group
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    uint4* dst = reinterpret_cast<uint4*>(base + static_cast<size_t>(g0 + q) * row_stride) + c;
+    *dst = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------
 // small numeric helpers
 // ----------------------------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
