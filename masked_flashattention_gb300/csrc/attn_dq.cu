@@ -79,32 +79,19 @@ enum {
   B_COUNT = 22
 };
 
-// Row `row` of a [rows][D] bf16 matrix, this warp's half of its bf16 pairs, into TMEM at `taddr`.
+// Rows `row0 .. row0+31` (one per lane) of a [rows][D] bf16 matrix, this warp's half of their bf16
+// pairs, into TMEM at `taddr` (coalesced loads; see load_rows_coalesced).
 template <int D>
-__device__ __forceinline__ void row_to_tmem(const __nv_bfloat16* m, size_t row, int hf,
-                                            uint32_t taddr) {
-  const uint4* src = reinterpret_cast<const uint4*>(m + row * D + hf * (D / 2));
+__device__ __forceinline__ void rows_to_tmem(const __nv_bfloat16* m, size_t row0, int hf, int lane,
+                                             uint32_t taddr) {
+  const char* base = reinterpret_cast<const char*>(m + row0 * D + hf * (D / 2));
   if constexpr (D == 128) {
     uint32_t w[32];
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const uint4 v = src[x];
-      w[4 * x] = v.x;
-      w[4 * x + 1] = v.y;
-      w[4 * x + 2] = v.z;
-      w[4 * x + 3] = v.w;
-    }
+    load_rows_coalesced<8>(w, base, D * 2u, lane);
     tmem_st32(taddr, w);
   } else {
     uint32_t w[16];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint4 v = src[x];
-      w[4 * x] = v.x;
-      w[4 * x + 1] = v.y;
-      w[4 * x + 2] = v.z;
-      w[4 * x + 3] = v.w;
-    }
+    load_rows_coalesced<4>(w, base, D * 2u, lane);
     tmem_st16(taddr, w);
   }
 }
@@ -281,9 +268,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     if (nt > 0) {
-      row_to_tmem<D>(p.q, static_cast<size_t>(row0) + i, hf, tmem + lane_off + kColQ + hf * (D / 4));
-      row_to_tmem<D>(p.d_o, static_cast<size_t>(row0) + i, hf,
-                     tmem + lane_off + kColDO + hf * (D / 4));
+      // the warp's 32 rows start at query row qt*128 + quarter*32
+      const size_t r0 = static_cast<size_t>(row0) + i - lane;
+      rows_to_tmem<D>(p.q, r0, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
+      rows_to_tmem<D>(p.d_o, r0, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

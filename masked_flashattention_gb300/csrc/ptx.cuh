@@ -354,15 +354,15 @@ __device__ __forceinline__ void tmem_wait_st() {
 // coalesced row stores
 // ----------------------------------------------------------------------------------------------
 // A warp holds 32 consecutive rows of a tile, one per lane (lane t: row t), each as NC 16-byte
-// chunks in w[4c .. 4c+3].  Stored as they are, every store instruction would touch 32 rows (32
-// memory segments).  Instead, within each group of NC lanes the chunks are transposed with three
-// (NC = 8) or two (NC = 4) rounds of butterfly shuffles: at distance d, lane pairs (l, l ^ d)
-// swap the chunks whose index differs from their lane in bit d.  Afterwards lane NC*G + c holds
-// chunk c of rows NC*G + q in w[4q .. 4q+3], and one store instruction writes 32/NC whole row
-// segments of NC * 16 bytes.  `base` is the address of row 0's first chunk for this warp.
+// chunks in w[4c .. 4c+3].  Read or written as they are, every memory instruction would touch 32
+// rows (32 memory segments).  transpose_chunks swaps the roles of lane and chunk index within each
+// group of NC lanes with three (NC = 8) or two (NC = 4) rounds of butterfly shuffles: at distance
+// d, lane pairs (l, l ^ d) exchange the chunks whose index differs from their lane in bit d.  So
+// "lane NC*G + t holds chunk c of row NC*G + t in w[4c..]" becomes "lane NC*G + c holds chunk c of
+// row NC*G + q in w[4q..]", and back: one memory instruction then covers 32/NC whole row segments
+// of NC * 16 bytes.
 template <int NC>
-__device__ __forceinline__ void store_rows_coalesced(uint32_t (&w)[4 * NC], char* base,
-                                                     size_t row_stride, int lane) {
+__device__ __forceinline__ void transpose_chunks(uint32_t (&w)[4 * NC], int lane) {
   static_assert(NC == 4 || NC == 8, "chunks per row segment");
 #pragma unroll
   for (int d = 1; d < NC; d <<= 1) {
@@ -382,12 +382,33 @@ __device__ __forceinline__ void store_rows_coalesced(uint32_t (&w)[4 * NC], char
       }
     }
   }
+}
+// Stores the warp's 32 rows; `base` is the address of row 0's first chunk for this warp.
+template <int NC>
+__device__ __forceinline__ void store_rows_coalesced(uint32_t (&w)[4 * NC], char* base,
+                                                     size_t row_stride, int lane) {
+  transpose_chunks<NC>(w, lane);
   const int c = lane % NC, g0 = lane - c;  // chunk of this lane, first row of its group
 #pragma unroll
   for (int q = 0; q < NC; ++q) {
     uint4* dst = reinterpret_cast<uint4*>(base + static_cast<size_t>(g0 + q) * row_stride) + c;
     *dst = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   }
+}
+// Loads the warp's 32 rows (lane t gets row t) with the same coalesced pattern.
+template <int NC>
+__device__ __forceinline__ void load_rows_coalesced(uint32_t (&w)[4 * NC], const char* base,
+                                                    size_t row_stride, int lane) {
+  const int c = lane % NC, g0 = lane - c;
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const uint4 v = *(reinterpret_cast<const uint4*>(base + static_cast<size_t>(g0 + q) * row_stride) + c);
+    w[4 * q] = v.x;
+    w[4 * q + 1] = v.y;
+    w[4 * q + 2] = v.z;
+    w[4 * q + 3] = v.w;
+  }
+  transpose_chunks<NC>(w, lane);
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -398,37 +419,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// paired fp32 arithmetic (one instruction for two lanes of data): d = a * b + c, a + b, a * b
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
+// paired fp32 arithmetic (one instruction for two lanes of data): d = a * b + c, a + b, a * b.
+// The compiler's own paired-float builtins, so that it places the operand pairs in registers
+// itself (no moves into and out of 64-bit pairs around each instruction).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 // three-input maximum
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
