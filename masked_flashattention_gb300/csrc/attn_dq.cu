@@ -4,30 +4,38 @@
 // and dP = dO V^T.  The main backward kernel walks key tiles (it owns dK and dV); accumulating dQ
 // there would need an fp32 read-modify-write of every (key tile, query tile) partial in L2, and on
 // GB300 that traffic limits the whole backward.  This kernel walks query tiles instead, like the
-// forward: one CTA owns one 128-row query tile of one (sample, head), visits the key tiles of the
-// forward bitmap row (empty tiles skipped, full tiles unmasked, partial tiles checked against the
-// forward Interval Table), recomputes S and dP, and keeps dQ in TMEM.  It writes dQ once, in
+// forward: a work item is one 128-row query tile of one (sample, head); it visits the key tiles of
+// the forward bitmap row (empty tiles skipped, full tiles unmasked, partial tiles checked against
+// the forward Interval Table), recomputes S and dP, and keeps dQ in TMEM.  It writes dQ once, in
 // bf16, with no atomics.
 //
-// Q and dO stay in TMEM for the whole CTA (the compute warps read their rows from global memory
+// Persistent CTAs: one CTA per SM takes the work items j = blockIdx.x, + gridDim.x, ... of the
+// longest-first schedule.  Barrier phases, K/V slots and TMEM buffers run on across items (global
+// tile counter g), so the next item's K/V tiles load and its first S MMAs run while the compute
+// warps write the previous item's dQ.
+//
+// Q and dO stay in TMEM for a whole item (the compute warps load their rows from global memory
 // once), so all three MMAs of a key tile take their A operand from TMEM and read only K or V from
 // shared memory: S = Q K^T, dP = dO V^T, dQ += dS K.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (query rows 32*(w%4) ..) and
 //              column half w / 4 of each 128-key tile: it reads S, then P = exp2(S *
 //              scale*log2e - LSE*log2e) stays in registers while dP is computed into the same
 //              TMEM columns, then dS = P * (dP - D) is written back there as bf16 pairs.
-//   warp 8     TMA producer: K through a 3-slot ring, V through a 2-slot ring.
-//   warps 9-10 MMA issuers, one thread each: the thread of warp 9 + t issues S(n), dP(n) and
-//              dQ(n) of the key tiles n with n % 2 == t.  A thread that issues tcgen05 MMAs
+//   warp 8     producer: per item, stages the bitmap row in shared memory (the whole warp), then
+//              lane 0 loads K through a 3-slot ring and V through a 2-slot ring.
+//   warps 9-10 MMA issuers, one thread each: the thread of warp 9 + t issues S(g), dP(g) and
+//              dQ(g) of the key tiles g with g % 2 == t.  A thread that issues tcgen05 MMAs
 //              stalls on every barrier wait, and the tensor pipe holds too few queued 128 x 128
 //              MMAs to cover the stall: with two issuers one thread's MMAs run while the other
 //              waits.
-// TMEM (512 columns): X0 [0,128), X1 [128,256) (key tile n uses X(n % 2) for S(n), then dP(n),
-// then dS(n)), dQ [256, 256+d), Q [384, 384+d/2), dO [448, 448+d/2).  Buffer X(t) belongs to the
+// TMEM (512 columns): X0 [0,128), X1 [128,256) (key tile g uses X(g % 2) for S(g), then dP(g),
+// then dS(g)), dQ [256, 256+d), Q [384, 384+d/2), dO [448, 448+d/2).  Buffer X(t) belongs to the
 // tiles of issuer t, which rewrites it only with MMAs issued after the ones that read it
-// (tcgen05 MMAs of one thread run in issue order).
+// (tcgen05 MMAs of one thread run in issue order).  The compute warps store the next item's Q and
+// dO once they have read the current item's last dP (every S and dP MMA of the item is then
+// done), and the first dQ MMA of an item overwrites dQ once they have read the previous one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -52,20 +60,25 @@ constexpr uint32_t kColDQ = 256;
 constexpr uint32_t kColQ = 384;
 constexpr uint32_t kColDO = 448;
 
+// Dynamic shared memory starts on a 1024-byte boundary here (no static shared memory); the kernel
+// checks it and reports a device check failure otherwise.
 template <int D>
 struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kK = 0;                                 // kKStages slots
   static constexpr uint32_t kV = kK + kKStages * kTileBytes;        // kVStages slots
   static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
-  static constexpr uint32_t kRow = kBar + 256u;                     // bitmap row (<= 64 words)
-  static constexpr uint32_t kTotal = kRow + 256u;
-  static constexpr uint32_t kAlloc = kTotal + 1024u;                // slack for 1024-byte alignment
+  // per item (two buffers): the bitmap row (at most 64 words, NT <= 1024) and the item's
+  // description {b << 16 | q_tile (or -1 for an invalid schedule entry), head, tile count}
+  static constexpr uint32_t kRow = kBar + 256u;
+  static constexpr uint32_t kInfo = kRow + 2u * 256u;
+  static constexpr uint32_t kTotal = kInfo + 32u;
+  static constexpr uint32_t kAlloc = kTotal;
 };
 static_assert(Smem<128>::kAlloc <= 232448, "dQ kernel shared memory exceeds 227 KB");
 
 enum {
-  B_QDO = 0,      // Q and dO stored in TMEM by the compute warps (8 arrivals)
+  B_QDO = 0,      // Q and dO of the item stored in TMEM by the compute warps (8 arrivals)
   B_KFULL = 1,    // +slot (3)
   B_KEMPTY = 4,   // +slot (3): the dQ MMA that last read the K slot is done
   B_VFULL = 7,    // +slot (2)
@@ -74,9 +87,12 @@ enum {
   B_SREAD = 13,   // +buffer (2): compute warps hold S in registers (8 arrivals)
   B_DPFULL = 15,  // +buffer (2): dP of the buffer's tile computed
   B_DSFULL = 17,  // +buffer (2): compute warps wrote dS (8 arrivals)
-  B_DONE = 19,    // every MMA of the CTA completed (one commit per issuer)
+  B_DONE = 19,    // every MMA of the item completed (one commit per issuer per item)
   B_DRAIN = 20,   // +issuer, abort path only: every MMA the issuer issued has completed
-  B_COUNT = 22
+  B_DQFREE = 22,  // the compute warps have read the item's dQ (8 arrivals)
+  B_ROWFULL = 23, // +buffer: the producer staged an item's bitmap row and description
+  B_ROWEMPTY = 25,// +buffer: its readers are done with it (8 compute warps + 2 issuers)
+  B_COUNT = 27
 };
 
 // Rows `row0 .. row0+31` (one per lane) of a [rows][D] bf16 matrix, this warp's half of their bf16
@@ -102,31 +118,22 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                const __grid_constant__ DqParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;  // dQ columns per compute warp
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if ((sbase & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment (see Smem)
+    if (threadIdx.x == 0) set_status(p.status, kDevBadMeta, 0x3ff);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
-  int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
-  uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
+  int4* info = reinterpret_cast<int4*>(smem + L::kInfo);  // [2]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const WaitCtl wait{abort_flag, p.status, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
-  cta_work(blockIdx.x, p.B * p.NT, p.H, item_idx, h);
-  const int item = p.sched[item_idx];
-  const int b = item >> 16;
-  const int qt = item & 0xFFFF;
-  if (b < 0 || b >= p.B || qt >= p.NT) {  // a schedule entry that no descriptor build wrote
-    if (threadIdx.x == 0) set_status(p.status, kDevBadSchedule, item_idx);
-    return;
-  }
-  const int bh = b * p.H + h;
-  const int row0 = bh * p.S;
+  const int n_items = p.B * p.NT * p.H;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -144,23 +151,14 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(bar(B_SREAD + s), kComputeWarps);
       mbar_init(bar(B_DPFULL + s), 1);
       mbar_init(bar(B_DSFULL + s), kComputeWarps);
+      mbar_init(bar(B_ROWFULL + s), 1);
+      mbar_init(bar(B_ROWEMPTY + s), kComputeWarps + 2);
     }
     mbar_init(bar(B_DONE), 2);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
+    mbar_init(bar(B_DQFREE), kComputeWarps);
     fence_barrier_init();
-  }
-  if (warp == 0) {
-    // this CTA's forward bitmap row (W <= 64 words) and its count of non-empty key tiles
-    const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + qt) * p.W;
-    int cnt = 0;
-    for (int w = lane; w < p.W; w += 32) {
-      const uint32_t x = row[w];
-      bmrow[w] = x;
-      cnt += __popc((x | (x >> 1)) & 0x55555555u);
-    }
-    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
-    if (lane == 0) *s_ntiles = cnt;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -170,80 +168,128 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nt = *s_ntiles;
   // asynchronous work issued so far, for the abort path: K and V slots armed (producer), any MMA
-  // issued (MMA thread)
-  int nk_armed = 0, nv_armed = 0;
+  // issued (issuers)
+  int gk_armed = 0, gv_armed = 0;
   bool mma_issued = false;
 
   if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && nt > 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int kt = next_tile(bmrow, p.NT, 0);
-      for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
-        const int sk = n % kKStages, sv = n % kVStages;
-        if (n >= kKStages && !wait(bar(B_KEMPTY + sk), ((n / kKStages) - 1) & 1, 0x301)) break;
-        nk_armed = n + 1;
-        mbar_arrive_expect_tx(bar(B_KFULL + sk), L::kTileBytes);
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kK + sk * L::kTileBytes + x * 16384u, &tmK, x * 64,
-                      row0 + kt * 128, bar(B_KFULL + sk));
-        if (n >= kVStages && !wait(bar(B_VEMPTY + sv), ((n / kVStages) - 1) & 1, 0x302)) break;
-        nv_armed = n + 1;
-        mbar_arrive_expect_tx(bar(B_VFULL + sv), L::kTileBytes);
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_2d(sbase + L::kV + sv * L::kTileBytes + x * 16384u, &tmV, x * 64,
-                      row0 + kt * 128, bar(B_VFULL + sv));
+    }
+    bool ok = true;
+    int gbase = 0;
+    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+      const int rb = k & 1;
+      // the row buffer is free once its readers are done with item k - 2
+      if (k >= 2) {
+        const bool free_ = wait(bar(B_ROWEMPTY + rb), ((k >> 1) - 1) & 1, 0x300);
+        __syncwarp();
+        if (!free_) { ok = false; break; }
       }
+      int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
+      cta_work(j, n_items / p.H, p.H, item_idx, h);
+      const int item = p.sched[item_idx];
+      const int b = item >> 16, qt = item & 0xFFFF;
+      const bool valid = b >= 0 && b < p.B && qt < p.NT;
+      uint32_t* row = reinterpret_cast<uint32_t*>(smem + L::kRow + rb * 256u);
+      int cnt = 0;
+      if (valid) {
+        const uint32_t* src = p.bm + (static_cast<size_t>(b) * p.NT + qt) * p.W;
+        for (int w = lane; w < p.W; w += 32) {
+          const uint32_t x = src[w];
+          row[w] = x;
+          cnt += __popc((x | (x >> 1)) & 0x55555555u);
+        }
+      }
+      cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+      if (lane == 0) {
+        if (!valid) set_status(p.status, kDevBadSchedule, item_idx);  // nothing is computed
+        info[rb] = make_int4(valid ? item : -1, h, cnt, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ROWFULL + rb));
+      if (lane == 0 && cnt > 0) {
+        const int row0 = (b * p.H + h) * p.S;
+        int kt = next_tile(row, p.NT, 0);
+        for (int n = 0; n < cnt; ++n, kt = next_tile(row, p.NT, kt + 1)) {
+          const int g = gbase + n, sk = g % kKStages, sv = g % kVStages;
+          if (g >= kKStages && !wait(bar(B_KEMPTY + sk), ((g / kKStages) - 1) & 1, 0x301)) {
+            ok = false;
+            break;
+          }
+          gk_armed = g + 1;
+          mbar_arrive_expect_tx(bar(B_KFULL + sk), L::kTileBytes);
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_2d(sbase + L::kK + sk * L::kTileBytes + x * 16384u, &tmK, x * 64,
+                        row0 + kt * 128, bar(B_KFULL + sk));
+          if (g >= kVStages && !wait(bar(B_VEMPTY + sv), ((g / kVStages) - 1) & 1, 0x302)) {
+            ok = false;
+            break;
+          }
+          gv_armed = g + 1;
+          mbar_arrive_expect_tx(bar(B_VFULL + sv), L::kTileBytes);
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_2d(sbase + L::kV + sv * L::kTileBytes + x * 16384u, &tmV, x * 64,
+                        row0 + kt * 128, bar(B_VFULL + sv));
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      gbase += cnt;
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
-    const int par = warp - kMmaWarp;  // this thread's key tiles: n % 2 == par, buffer X(par)
-    if (lane == 0 && nt > par) {
+    const int par = warp - kMmaWarp;  // this thread's key tiles: g % 2 == par, buffer X(par)
+    if (lane == 0) {
       constexpr uint32_t idS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t idQ = make_idesc_bf16(128, D, 0, 1);    // dQ += dS K
-      auto issue_s = [&](int n) -> bool {  // S(n) into X(n % 2)
-        const int sk = n % kKStages;
-        if (!wait(bar(B_KFULL + sk), (n / kKStages) & 1, 0x303)) return false;
+      int gbase = 0, kq = 0;  // key tiles and computed items before the current one
+      auto issue_s = [&](int g) -> bool {  // S(g) into X(g % 2)
+        const int sk = g % kKStages;
+        if (!wait(bar(B_KFULL + sk), (g / kKStages) & 1, 0x303)) return false;
         tc_fence_after();
         mma_issued = true;
         const uint32_t dK = sdesc_lo(sbase + L::kK + sk * L::kTileBytes, 16u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ts_lo(tmem + kColX + (n & 1) * 128, tmem + kColQ + 8 * kk, dK + kstep_kmajor(kk), idS,
+          umma_ts_lo(tmem + kColX + (g & 1) * 128, tmem + kColQ + 8 * kk, dK + kstep_kmajor(kk), idS,
                      kk > 0 ? 1u : 0u);
-        umma_commit(bar(B_SFULL + (n & 1)));
+        umma_commit(bar(B_SFULL + (g & 1)));
         return true;
       };
-      auto issue_dp = [&](int n) -> bool {  // dP(n) into X(n % 2), once S(n) has been read
-        const int sv = n % kVStages;
-        if (!wait(bar(B_SREAD + (n & 1)), (n >> 1) & 1, 0x306)) return false;
-        if (!wait(bar(B_VFULL + sv), (n / kVStages) & 1, 0x304)) return false;
+      auto issue_dp = [&](int g) -> bool {  // dP(g) into X(g % 2), once S(g) has been read
+        const int sv = g % kVStages;
+        if (!wait(bar(B_SREAD + (g & 1)), (g >> 1) & 1, 0x306)) return false;
+        if (!wait(bar(B_VFULL + sv), (g / kVStages) & 1, 0x304)) return false;
         tc_fence_after();
         const uint32_t dV = sdesc_lo(sbase + L::kV + sv * L::kTileBytes, 16u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ts_lo(tmem + kColX + (n & 1) * 128, tmem + kColDO + 8 * kk, dV + kstep_kmajor(kk),
+          umma_ts_lo(tmem + kColX + (g & 1) * 128, tmem + kColDO + 8 * kk, dV + kstep_kmajor(kk),
                      idS, kk > 0 ? 1u : 0u);
-        umma_commit(bar(B_DPFULL + (n & 1)));
+        umma_commit(bar(B_DPFULL + (g & 1)));
         umma_commit(bar(B_VEMPTY + sv));
         return true;
       };
-      // dQ += dS(n) K(n): dS pairs of keys [0,64) at X columns [0,32), [64,128) at [64,96).
-      // dQ(n-1) was issued by the other thread: dQ(n) waits until it has completed (its K slot's
-      // release), so the accumulations never overlap.  That barrier cannot run a phase ahead of
-      // this wait: dQ(n+2) needs dQ(n+1), which needs dQ(n).
-      auto issue_dq = [&](int n) -> bool {
-        if (!wait(bar(B_DSFULL + (n & 1)), (n >> 1) & 1, 0x307)) return false;
-        if (n >= 1 &&
-            !wait(bar(B_KEMPTY + (n - 1) % kKStages), ((n - 1) / kKStages) & 1, 0x30a))
+      // dQ += dS(g) K(g): dS pairs of keys [0,64) at X columns [0,32), [64,128) at [64,96).
+      // Within an item, dQ(g-1) was issued by the other thread: dQ(g) waits until it has
+      // completed (its K slot's release), so the accumulations never overlap; that barrier cannot
+      // run a phase ahead of this wait (dQ(g+2) needs dQ(g+1), which needs dQ(g)).  The first dQ
+      // of an item overwrites the accumulator once the compute warps have read the previous one.
+      auto issue_dq = [&](int g, int n) -> bool {
+        if (!wait(bar(B_DSFULL + (g & 1)), (g >> 1) & 1, 0x307)) return false;
+        if (n >= 1) {
+          if (!wait(bar(B_KEMPTY + (g - 1) % kKStages), ((g - 1) / kKStages) & 1, 0x30a))
+            return false;
+        } else if (kq >= 1 && !wait(bar(B_DQFREE), (kq - 1) & 1, 0x30b)) {
           return false;
+        }
         tc_fence_after();
-        const int sk = n % kKStages;
+        const int sk = g % kKStages;
         const uint32_t dK = sdesc_lo(sbase + L::kK + sk * L::kTileBytes, 16384u);
-        const uint32_t sX = tmem + kColX + (n & 1) * 128;
+        const uint32_t sX = tmem + kColX + (g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts_lo(tmem + kColDQ, sX + 64 * (kk >> 2) + 8 * (kk & 3), dK + kstep_mnmajor(kk), idQ,
@@ -251,106 +297,156 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         umma_commit(bar(B_KEMPTY + sk));
         return true;
       };
-      bool ok = wait(bar(B_QDO), 0, 0x305);
-      if (ok) tc_fence_after();
-      // own tiles in order: S(n), dP(n) once S(n) is read, dQ(n) once dS(n) is written; S(n+2)
-      // reuses X(par) after dQ(n) read it (tcgen05 MMAs of one thread run in issue order)
-      for (int n = par; ok && n < nt; n += 2) ok = issue_s(n) && issue_dp(n) && issue_dq(n);
-      if (ok) umma_commit(bar(B_DONE));
-    } else if (lane == 0 && nt > 0) {
-      umma_commit(bar(B_DONE));  // a second issuer with no tile (nt == 1) still signs off
+      bool ok = true;
+      for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+        const int rb = k & 1;
+        if (!wait(bar(B_ROWFULL + rb), (k >> 1) & 1, 0x305)) break;
+        const int nt = info[rb].z;
+        mbar_arrive(bar(B_ROWEMPTY + rb));
+        if (nt == 0) continue;
+        ok = wait(bar(B_QDO), kq & 1, 0x308);
+        if (ok) tc_fence_after();
+        // own tiles in order: S(g), dP(g) once S(g) is read, dQ(g) once dS(g) is written; S(g+2)
+        // reuses X(par) after dQ(g) read it (tcgen05 MMAs of one thread run in issue order)
+        for (int n = (par - gbase) & 1; ok && n < nt; n += 2) {
+          const int g = gbase + n;
+          ok = issue_s(g) && issue_dp(g) && issue_dq(g, n);
+        }
+        if (ok) umma_commit(bar(B_DONE));
+        gbase += nt;
+        ++kq;
+      }
     }
   } else {
     // ---------------------------------------------------------------- compute warps 0-7
     const int quarter = warp & 3;
     const int hf = warp >> 2;           // column half of the key tile, and of dQ
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
-    const int i = qt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    if (nt > 0) {
-      // the warp's 32 rows start at query row qt*128 + quarter*32
-      const size_t r0 = static_cast<size_t>(row0) + i - lane;
-      rows_to_tmem<D>(p.q, r0, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
-      rows_to_tmem<D>(p.d_o, r0, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_QDO));
-    }
-    RowIntervals<MAXNI> ri;
-    load_row_intervals(p.itab, b, p.NI, p.S, i, ri);
-    // per-row constants from the backward prologue: -LSE * log2(e) (-inf for a row that sees
-    // nothing) and -D
-    const float lse2 = p.lse2[static_cast<size_t>(row0) + i];
-    const float negd = p.delta[static_cast<size_t>(row0) + i];
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
-    const float2 lse2x2 = make_float2(lse2, lse2), negd2 = make_float2(negd, negd);
     bool ok = true;
-    int kt = next_tile(bmrow, p.NT, 0);
-    for (int n = 0; ok && n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
-      const int xb = n & 1;
-      const uint32_t sX = tmem + lane_off + kColX + xb * 128 + 64 * hf;
-      bool ready = wait(bar(B_SFULL + xb), (n >> 1) & 1, 0x308);
+    int gbase = 0, kq = 0;
+    // An item's description, this row's intervals and constants are fetched one item ahead, and
+    // its Q and dO are stored into TMEM before the previous item's epilogue, so that the issuers
+    // can start on it while this warp writes the previous dQ.
+    struct Item {
+      int4 it;
+      RowIntervals<MAXNI> ri;
+      float lse2, negd;  // -LSE * log2(e) (-inf for a row that sees nothing) and -D, per row
+    };
+    auto fetch = [&](int kf, Item& x) -> bool {
+      const bool ready = wait(bar(B_ROWFULL + (kf & 1)), (kf >> 1) & 1, 0x310);
       __syncwarp();
-      if (!ready) { ok = false; break; }
-      tc_fence_after();
-      float pf[64];
-      {
-        uint32_t t0[32], t1[32];
-        tmem_ld32(sX, t0);
-        tmem_ld32(sX + 32, t1);
-        tmem_wait_ld();
+      if (!ready) return false;
+      x.it = info[kf & 1];
+      if (x.it.x < 0) return true;
+      const int b = x.it.x >> 16, qt = x.it.x & 0xFFFF;
+      const size_t row = static_cast<size_t>(b * p.H + x.it.y) * p.S + qt * 128 + r;
+      load_row_intervals(p.itab, b, p.NI, p.S, qt * 128 + r, x.ri);
+      x.lse2 = p.lse2[row];
+      x.negd = p.delta[row];
+      if (x.it.z > 0) {
+        // the warp's 32 rows of Q and dO into TMEM.  The previous item's S and dP MMAs, which
+        // read them, are done: this warp has read the last dP of that item.
+        rows_to_tmem<D>(p.q, row - lane, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
+        rows_to_tmem<D>(p.d_o, row - lane, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_QDO));
+      }
+      return true;
+    };
+    Item cur;
+    cur.it = make_int4(-1, 0, 0, 0);
+    if (static_cast<int>(blockIdx.x) < n_items) ok = fetch(0, cur);
+    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+      const int rb = k & 1;
+      const uint32_t* bmrow = reinterpret_cast<const uint32_t*>(smem + L::kRow + rb * 256u);
+      const int nt = cur.it.z;
+      const int b = cur.it.x >> 16, qt = cur.it.x & 0xFFFF;
+      const size_t row0 = static_cast<size_t>(b * p.H + cur.it.y) * p.S;
+      const int i = qt * 128 + r;
+      const float2 lse2x2 = make_float2(cur.lse2, cur.lse2), negd2 = make_float2(cur.negd, cur.negd);
+      int kt = next_tile(bmrow, p.NT, 0);
+      for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
+        const int g = gbase + n, xb = g & 1;
+        const uint32_t sX = tmem + lane_off + kColX + xb * 128 + 64 * hf;
+        bool ready = wait(bar(B_SFULL + xb), (g >> 1) & 1, 0x311);
+        __syncwarp();
+        if (!ready) { ok = false; break; }
+        tc_fence_after();
+        float pf[64];
+        {
+          uint32_t t0[32], t1[32];
+          tmem_ld32(sX, t0);
+          tmem_ld32(sX + 32, t1);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pf[c] = __uint_as_float(t0[c]);
-          pf[32 + c] = __uint_as_float(t1[c]);
+          for (int c = 0; c < 32; ++c) {
+            pf[c] = __uint_as_float(t0[c]);
+            pf[32 + c] = __uint_as_float(t1[c]);
+          }
         }
-      }
-      // S is in registers: dP may now overwrite these columns
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SREAD + xb));
-      if (!tile_is_full(bmrow, kt)) {
-        const int j0 = kt * 128 + 64 * hf;
-        mask_cols_any(pf, j0, ri, p.NI, p.check, p.masked != 0);
-      }
-      // P = exp2(s * scale*log2e - LSE*log2e); masked scores are -inf and give 0
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float2 x = fma2(make_float2(pf[c], pf[c + 1]), scale2, lse2x2);
-        pf[c] = ex2_approx(x.x);
-        pf[c + 1] = ex2_approx(x.y);
-      }
-      ready = wait(bar(B_DPFULL + xb), (n >> 1) & 1, 0x309);
-      __syncwarp();
-      if (!ready) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[32];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dpr[32];
-        tmem_ld32(sX + 32 * ch, dpr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 g = add2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])), negd2);
-          const float2 ds = mul2(make_float2(pf[32 * ch + c], pf[32 * ch + c + 1]), g);
-          pk[16 * ch + c / 2] = pack_bf16x2(ds.x, ds.y);
+        // S is in registers: dP may now overwrite these columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SREAD + xb));
+        if (!tile_is_full(bmrow, kt)) {
+          const int j0 = kt * 128 + 64 * hf;
+          mask_cols_any(pf, j0, cur.ri, p.NI, p.check, p.masked != 0);
         }
+        // P = exp2(s * scale*log2e - LSE*log2e); masked scores are -inf and give 0
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x = fma2(make_float2(pf[c], pf[c + 1]), scale2, lse2x2);
+          pf[c] = ex2_approx(x.x);
+          pf[c + 1] = ex2_approx(x.y);
+        }
+        ready = wait(bar(B_DPFULL + xb), (g >> 1) & 1, 0x312);
+        __syncwarp();
+        if (!ready) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pk[32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t dpr[32];
+          tmem_ld32(sX + 32 * ch, dpr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 gg = add2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])), negd2);
+            const float2 ds = mul2(make_float2(pf[32 * ch + c], pf[32 * ch + c + 1]), gg);
+            pk[16 * ch + c / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+        }
+        // dS over the columns this warp has read: keys [64*hf, +64) -> columns [64*hf, +32)
+        tmem_st32(sX, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DSFULL + xb));
       }
-      // dS over the columns this warp has read: keys [64*hf, +64) -> columns [64*hf, +32)
-      tmem_st32(sX, pk);
-      tmem_wait_st();
-      tc_fence_before();
+      // the bitmap row and the item description are no longer needed
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSFULL + xb));
-    }
-
-    // ---- epilogue: dQ = scale * accumulator -> bf16, this warp's half of the head dim ----
-    __nv_bfloat16* qrow = p.dq + (static_cast<size_t>(row0) + i) * D + hf * kHalf;
-    const bool done = ok && nt > 0 && wait(bar(B_DONE), 0, 0x30a);
-    __syncwarp();
-    if (done) {
+      if (lane == 0) mbar_arrive(bar(B_ROWEMPTY + rb));
+      if (!ok) break;
+      // the next item: description, intervals, constants, and its Q and dO into TMEM
+      const Item done_item = cur;
+      if (j + static_cast<int>(gridDim.x) < n_items) {
+        if (!fetch(k + 1, cur)) { ok = false; break; }
+      }
+      if (done_item.it.x < 0) continue;  // an invalid schedule entry: nothing to write
+      __nv_bfloat16* qrow = p.dq + (row0 + i) * D + hf * kHalf;
+      if (nt == 0) {  // a query tile that sees no key
+        uint4* dst = reinterpret_cast<uint4*>(qrow);
+        for (int q = 0; q < kHalf / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      // ---- epilogue: dQ = scale * accumulator -> bf16, this warp's half of the head dim ----
+      const bool fin = wait(bar(B_DONE), kq & 1, 0x313);
+      __syncwarp();
+      if (!fin) { ok = false; break; }
       tc_fence_after();
       const float sc = p.scale;
       uint32_t ob[kHalf / 2];  // this row's dQ columns as bf16 pairs
@@ -363,12 +459,15 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         for (int e = 0; e < 32; e += 2)
           ob[(c + e) / 2] = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
       }
+      // the accumulator is free for the next item
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DQFREE));
       // rows quarter*32 .. +31 of the tile, this warp's dQ columns
       store_rows_coalesced<kHalf / 8>(
           ob, reinterpret_cast<char*>(qrow - static_cast<size_t>(lane) * D), D * 2u, lane);
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(qrow);
-      for (int q = 0; q < kHalf / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+      gbase += nt;
+      ++kq;
     }
   }
 
@@ -378,11 +477,13 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   if (*abort_flag) {
     // A wait gave up.  Copies and MMAs already issued still land in shared memory and TMEM:
     // wait for them before TMEM is freed and the CTA exits.
-    if (warp == kProducerWarp && lane == 0 && nt > 0) {
-      for (int s = 0; s < kKStages && s < nk_armed; ++s)
-        mbar_wait_drain(bar(B_KFULL + s), ((nk_armed - 1 - s) / kKStages) & 1, p.status, 0x3f1);
-      for (int s = 0; s < kVStages && s < nv_armed; ++s)
-        mbar_wait_drain(bar(B_VFULL + s), ((nv_armed - 1 - s) / kVStages) & 1, p.status, 0x3f2);
+    if (warp == kProducerWarp && lane == 0) {
+      for (int g = gk_armed - kKStages; g < gk_armed; ++g)
+        if (g >= 0)
+          mbar_wait_drain(bar(B_KFULL + g % kKStages), (g / kKStages) & 1, p.status, 0x3f1);
+      for (int g = gv_armed - kVStages; g < gv_armed; ++g)
+        if (g >= 0)
+          mbar_wait_drain(bar(B_VFULL + g % kVStages), (g / kVStages) & 1, p.status, 0x3f2);
     }
     if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0 && mma_issued) {
       umma_commit(bar(B_DRAIN + warp - kMmaWarp));
@@ -411,7 +512,13 @@ int launch_attn_dq(const DqParams& p, int d, const void* k, const void* v, cudaS
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
   CUtensorMap mk, mv;
   if (!make_bf16_tile_map(&mk, k, rows, d) || !make_bf16_tile_map(&mv, v, rows, d)) return -1;
-  const dim3 grid(p.B * p.NT * p.H);
+  // persistent: one CTA per SM (one fits: 160 KB of shared memory, all 512 TMEM columns)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return -1;
+  const int items = p.B * p.NT * p.H;
+  const dim3 grid(items < sms ? items : sms);
   // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
     if (p.NI <= 4) return dq_launch<128, 4>(grid, stream, mk, mv, p);
