@@ -85,8 +85,12 @@ typedef struct cm_meta {
  *   bm_b    uint32 [B][S/tile][ceil((S/tile)/16)]  (k-tile, q-tile) states
  *   sched_f int32 [B * S/tile]  forward work order: (b << 16 | q_tile), most tiles first
  *   sched_b int32 [B * S/tile]  backward work order: (b << 16 | k_tile), most tiles first
- *   status  int32 [2 + 2 * (S/tile + 1)]  device error word (first element), then the preprocess
- *           kernel's grid barrier and schedule histograms; cleared by cm_build_descriptor */
+ *   status  int32 [2 + 2 * (S/tile + 1) + 6]  device error word (first element), then the
+ *           preprocess kernel's grid barrier and schedule histograms, then the work queues of
+ *           the three attention kernels (a next-item counter and a finished-CTA counter each,
+ *           returned to zero by the last CTA of every launch); cleared by cm_build_descriptor.
+ *           Attention calls that use one descriptor must therefore run one after another (one
+ *           stream, or ordered by events), never at the same time. */
 #define CM_FORM_VISIBLE 0
 #define CM_FORM_MASKED 1
 typedef struct cm_descriptor {

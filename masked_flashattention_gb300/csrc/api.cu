@@ -119,7 +119,7 @@ CM_API int cm_descriptor_sizes(const cm_spec* fwd, const cm_spec* bwd, int B, in
   sizes[3] = static_cast<size_t>(B) * NT * W * 4;
   sizes[4] = static_cast<size_t>(B) * NT * 4;
   sizes[5] = static_cast<size_t>(B) * NT * 4;
-  sizes[6] = static_cast<size_t>(2 + 2 * (NT + 1)) * 4;  // status, barrier, histograms
+  sizes[6] = static_cast<size_t>(2 + 2 * (NT + 1) + 6) * 4;  // status, barrier, histograms, queues
   return CM_OK;
 }
 
@@ -149,7 +149,7 @@ CM_API int cm_build_descriptor(const cm_spec* fwd, const cm_spec* bwd, const cm_
     return CM_ERR_INVALID_ARG;
   if (meta->nseg_max > 16384) return CM_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t work_bytes = static_cast<size_t>(2 + 2 * (S / kTile + 1)) * 4;
+  const size_t work_bytes = static_cast<size_t>(2 + 2 * (S / kTile + 1) + 6) * 4;
   if (cudaMemsetAsync(desc->status, 0, work_bytes, st) != cudaSuccess) return CM_ERR_CUDA;
   const void* gen = g_preprocess_mode.load() == CM_PREPROCESS_GENERATED
                         ? cm::pair_generated_kernel(fwd, bwd)

@@ -73,24 +73,33 @@ struct Smem {
   static constexpr uint32_t kLse2 = 6 * kTileBytes;    // [2 slots][128 floats]: -LSE * log2(e)
   static constexpr uint32_t kDelta = kLse2 + 1024u;    // [2 slots][128 floats]: -D
   static constexpr uint32_t kBar = kDelta + 1024u;
-  static constexpr uint32_t kRow = kBar + 256u;        // bitmap row: at most 64 words (NT <= 1024)
-  static constexpr uint32_t kTotal = kRow + 256u;
-  static constexpr uint32_t kAlloc = kTotal + 1024u;  // + slack to align the base to 1024 bytes
+  // per item (two buffers): the bitmap row (at most 64 words, NT <= 1024) and the item's
+  // description {b << 16 | k_tile (or -1 for an invalid schedule entry), head, tile count}
+  static constexpr uint32_t kRow = kBar + 256u;
+  static constexpr uint32_t kInfo = kRow + 2u * 256u;
+  static constexpr uint32_t kTotal = kInfo + 32u;
+  // no alignment slack: dynamic shared memory starts on a 1024-byte boundary here (no static
+  // shared memory); the kernel checks it and reports a device check failure otherwise
+  static constexpr uint32_t kAlloc = kTotal;
 };
 static_assert(Smem<128>::kAlloc <= 232448, "backward shared memory exceeds 227 KB");
 
 enum {
-  B_KV = 0,        // K and V loaded
+  B_KV = 0,        // K and V of the item loaded
   B_QFULL = 1,     // +slot: Q, dO, LSE*log2e and D of a query tile loaded (one barrier: each
                    // wait of the MMA thread leaves a gap in the tensor pipe)
   B_QEMPTY = 3,    // +slot: the dK MMA (last reader of the slot, after dV) is done
   B_SFULL = 5,     // S^T of the current tile computed
   B_DPFULL = 6,    // dP^T of the current tile computed
   B_PDS = 7,       // compute warps wrote dS^T (TMEM) and read dP^T (8 arrivals)
-  B_DONE = 8,      // every MMA of the CTA completed (dK, dV final)
+  B_DONE = 8,      // every MMA of the item completed (dK, dV final)
   B_PREADY = 9,    // compute warps wrote P^T (TMEM) (8 arrivals)
   B_DRAIN = 10,    // abort path only: every MMA issued so far has completed
-  B_COUNT = 11
+  B_KVEMPTY = 11,  // the item's last S^T and dP^T MMAs (the last readers of K and V) are done
+  B_ACCFREE = 12,  // the compute warps have read the item's dV and dK (8 arrivals)
+  B_ROWFULL = 13,  // +buffer: the producer staged an item's bitmap row and description
+  B_ROWEMPTY = 15, // +buffer: its readers are done with it (8 compute warps + the MMA thread)
+  B_COUNT = 17
 };
 
 
@@ -161,30 +170,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ BwdParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;           // head-dim columns per compute warp
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  int* const queue = p.status + 2 + 2 * (p.NT + 1) + 2;  // work queue (mask.cuh)
+  if ((sbase & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment (see Smem)
+    if (threadIdx.x == 0) set_status(p.status, kDevBadMeta, 0x2ff);
+    if (threadIdx.x == 0) queue_finish(queue);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * B_COUNT + 4);
-  int* s_ntiles = reinterpret_cast<int*>(smem + L::kBar + 8 * B_COUNT + 8);
-  uint32_t* bmrow = reinterpret_cast<uint32_t*>(smem + L::kRow);
+  int4* info = reinterpret_cast<int4*>(smem + L::kInfo);  // [2]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const WaitCtl wait{abort_flag, p.status, p.wait_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
-  cta_work(blockIdx.x, p.B * p.NT, p.H, item_idx, h);
-  const int item = p.sched[item_idx];
-  const int b = item >> 16;
-  const int kt = item & 0xFFFF;
-  if (b < 0 || b >= p.B || kt >= p.NT) {  // a schedule entry that no descriptor build wrote
-    if (threadIdx.x == 0) set_status(p.status, kDevBadSchedule, item_idx);
-    return;
-  }
-  const int bh = b * p.H + h;
+  const int n_items = p.B * p.NT * p.H;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -192,6 +195,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_QFULL + x), 1);
       mbar_init(bar(B_QEMPTY + x), 1);
+      mbar_init(bar(B_ROWFULL + x), 1);
+      mbar_init(bar(B_ROWEMPTY + x), kComputeWarps + 1);
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
@@ -199,19 +204,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_DONE), 1);
     mbar_init(bar(B_PREADY), kComputeWarps);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_KVEMPTY), 1);
+    mbar_init(bar(B_ACCFREE), kComputeWarps);
     fence_barrier_init();
-  }
-  if (warp == 0) {
-    // this CTA's bitmap row (W <= 64 words) and its count of non-empty query tiles
-    const uint32_t* row = p.bm + (static_cast<size_t>(b) * p.NT + kt) * p.W;
-    int cnt = 0;
-    for (int w = lane; w < p.W; w += 32) {
-      const uint32_t x = row[w];
-      bmrow[w] = x;
-      cnt += __popc((x | (x >> 1)) & 0x55555555u);
-    }
-    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
-    if (lane == 0) *s_ntiles = cnt;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -221,48 +216,103 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nt = *s_ntiles;
-  const int row0 = bh * p.S;
-  // asynchronous work issued so far, for the abort path: query-tile slots armed (producer), any
-  // MMA issued (MMA thread)
-  int m_armed = 0;
+  // asynchronous work issued so far, for the abort path: K/V loads and query-tile slots armed
+  // (producer), any MMA issued (MMA thread)
+  int kv_armed = 0, g_armed = 0;
   bool mma_issued = false;
 
   if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && nt > 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(B_KV), 2 * L::kTileBytes);
-      for (int x = 0; x < D / 64; ++x) {
-        tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
-        tma_load_2d(sbase + L::kV + x * 16384u, &tmV, x * 64, row0 + kt * 128, bar(B_KV));
+    }
+    bool ok = true;
+    int gbase = 0;
+    for (int k = 0; ok; ++k) {
+      const int rb = k & 1;
+      // the row buffer is free once its readers are done with item k - 2
+      if (k >= 2) {
+        const bool free_ = wait(bar(B_ROWEMPTY + rb), ((k >> 1) - 1) & 1, 0x200);
+        __syncwarp();
+        if (!free_) { ok = false; break; }
       }
-      int qt = next_tile(bmrow, p.NT, 0);
-      for (int m = 0; m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
-        const int slot = m & 1;
-        const size_t r = static_cast<size_t>(row0) + qt * 128;
-        // a slot is free once the dK MMA of the tile two back (its last reader) is done
-        if (m >= 2 && !wait(bar(B_QEMPTY + slot), ((m - 2) >> 1) & 1, 0x201))
-          break;
-        const uint32_t full = bar(B_QFULL + slot);
-        m_armed = m + 1;
-        mbar_arrive_expect_tx(full, 2u * (L::kTileBytes + 512u));
-        for (int x = 0; x < D / 64; ++x) {
-          tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
-                      row0 + qt * 128, full);
-          tma_load_2d(sbase + L::kdO + slot * L::kTileBytes + x * 16384u, &tmdO, x * 64,
-                      row0 + qt * 128, full);
+      // the next work item from the queue (schedule order: longest rows first); the end
+      // marker stops every role
+      int jj = 0;
+      if (lane == 0) jj = atomicAdd(queue, 1);
+      jj = __shfl_sync(0xFFFFFFFFu, jj, 0);
+      if (jj >= n_items) {
+        if (lane == 0) {
+          info[rb] = make_int4(-1, 0, 0, 1);
+          mbar_arrive(bar(B_ROWFULL + rb));
         }
-        bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, full);
-        bulk_load(sbase + L::kDelta + slot * 512u, p.delta + r, 512u, full);
+        break;
       }
+      int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
+      cta_work(jj, n_items / p.H, p.H, item_idx, h);
+      const int item = p.sched[item_idx];
+      const int b = item >> 16, kt = item & 0xFFFF;
+      const bool valid = b >= 0 && b < p.B && kt < p.NT;
+      uint32_t* row = reinterpret_cast<uint32_t*>(smem + L::kRow + rb * 256u);
+      int cnt = 0;
+      if (valid) {
+        const uint32_t* src = p.bm + (static_cast<size_t>(b) * p.NT + kt) * p.W;
+        for (int w = lane; w < p.W; w += 32) {
+          const uint32_t x = src[w];
+          row[w] = x;
+          cnt += __popc((x | (x >> 1)) & 0x55555555u);
+        }
+      }
+      cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+      if (lane == 0) {
+        if (!valid) set_status(p.status, kDevBadSchedule, item_idx);  // nothing is computed
+        info[rb] = make_int4(valid ? item : -1, h, cnt, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ROWFULL + rb));
+      if (lane == 0 && cnt > 0) {
+        const int row0 = (b * p.H + h) * p.S;
+        // K and V of this item once the previous item's last S^T and dP^T are done
+        if (kv_armed > 0 && !wait(bar(B_KVEMPTY), (kv_armed - 1) & 1, 0x201)) ok = false;
+        if (ok) {
+          ++kv_armed;
+          mbar_arrive_expect_tx(bar(B_KV), 2 * L::kTileBytes);
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_2d(sbase + L::kK + x * 16384u, &tmK, x * 64, row0 + kt * 128, bar(B_KV));
+            tma_load_2d(sbase + L::kV + x * 16384u, &tmV, x * 64, row0 + kt * 128, bar(B_KV));
+          }
+        }
+        int qt = next_tile(row, p.NT, 0);
+        for (int m = 0; ok && m < cnt; ++m, qt = next_tile(row, p.NT, qt + 1)) {
+          const int g = gbase + m, slot = g & 1;
+          const size_t r = static_cast<size_t>(row0) + qt * 128;
+          // a slot is free once the dK MMA of the tile two back (its last reader) is done
+          if (g >= 2 && !wait(bar(B_QEMPTY + slot), ((g - 2) >> 1) & 1, 0x202)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar(B_QFULL + slot);
+          g_armed = g + 1;
+          mbar_arrive_expect_tx(full, 2u * (L::kTileBytes + 512u));
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_2d(sbase + L::kQ + slot * L::kTileBytes + x * 16384u, &tmQ, x * 64,
+                        row0 + qt * 128, full);
+            tma_load_2d(sbase + L::kdO + slot * L::kTileBytes + x * 16384u, &tmdO, x * 64,
+                        row0 + qt * 128, full);
+          }
+          bulk_load(sbase + L::kLse2 + slot * 512u, p.lse2 + r, 512u, full);
+          bulk_load(sbase + L::kDelta + slot * 512u, p.delta + r, 512u, full);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      gbase += cnt;
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
+    if (lane == 0) {
       constexpr uint32_t idSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t idKM = make_idesc_bf16(128, D, 0, 1);    // dK, dV
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV;
@@ -270,71 +320,81 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // the issuing thread shares its SM sub-partition with two compute warps, and every
       // instruction it needs between MMAs leaves the tensor pipe waiting longer)
       const uint32_t dK0 = sdesc_lo(sK, 16u), dV0 = sdesc_lo(sV, 16u);
-      const uint32_t dQ0 = sdesc_lo(sbase + L::kQ, 16u), ddO0 = sdesc_lo(sbase + L::kdO, 16u);
-      // tile 0: S^T -> RA, dP^T -> RB
-      bool ok = wait(bar(B_KV), 0, 0x202) &&
-                wait(bar(B_QFULL), 0, 0x203);
-      if (ok) {
+      // S^T(g) = K Q(g)^T -> region X(g) (g even: RA, odd: RB); dP^T(g) = V dO(g)^T -> X(g + 1)
+      auto issue_st = [&](int g) -> bool {
+        const int slot = g & 1;
+        if (!wait(bar(B_QFULL + slot), (g >> 1) & 1, 0x203)) return false;
         tc_fence_after();
         mma_issued = true;
+        const uint32_t X = slot ? kColRB : kColRA;
+        const uint32_t dQn = sdesc_lo(sbase + L::kQ + slot * L::kTileBytes, 16u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lo(tmem + kColRA, dK0 + kstep_kmajor(kk), dQ0 + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
+          umma_ss_lo(tmem + X, dK0 + kstep_kmajor(kk), dQn + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL));
-      }
-      if (ok) {
-        tc_fence_after();
+        return true;
+      };
+      auto issue_dpt = [&](int g) {  // its dO landed with its Q (waited for before S^T(g))
+        const int slot = g & 1;
+        const uint32_t Y = slot ? kColRA : kColRB;
+        const uint32_t ddOn = sdesc_lo(sbase + L::kdO + slot * L::kTileBytes, 16u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lo(tmem + kColRB, dV0 + kstep_kmajor(kk), ddO0 + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
+          umma_ss_lo(tmem + Y, dV0 + kstep_kmajor(kk), ddOn + kstep_kmajor(kk), idSS, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_DPFULL));
-      }
-      for (int m = 0; ok && m < nt; ++m) {
-        const uint32_t X = (m & 1) ? kColRB : kColRA;
-        const uint32_t Y = (m & 1) ? kColRA : kColRB;
-        const uint32_t sQ = sbase + L::kQ + (m & 1) * L::kTileBytes;
-        const uint32_t sdO = sbase + L::kdO + (m & 1) * L::kTileBytes;
-        // dV += P^T dO as soon as P^T is in X, while the compute warps work on dS^T.
-        // P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96)
-        if (!wait(bar(B_PREADY), m & 1, 0x210)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts_lo(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                     sdesc_lo(sdO, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        if (!wait(bar(B_PDS), m & 1, 0x205)) break;
-        tc_fence_after();
-        if (m + 1 < nt) {
-          // the next tile's S^T into Y (its dP^T was consumed), so that its P can start while
-          // the tensor pipe runs dK
-          const uint32_t sQn = sbase + L::kQ + ((m + 1) & 1) * L::kTileBytes;
-          if (!wait(bar(B_QFULL + ((m + 1) & 1)), ((m + 1) >> 1) & 1, 0x203))
+      };
+      bool ok = true;
+      int gbase = 0, kq = 0;  // query tiles and computed items before the current one
+      for (int k = 0; ok; ++k) {
+        const int rb = k & 1;
+        if (!wait(bar(B_ROWFULL + rb), (k >> 1) & 1, 0x204)) break;
+        if (info[rb].w) break;  // no more work items
+        const int nt = info[rb].z;
+        mbar_arrive(bar(B_ROWEMPTY + rb));
+        if (nt == 0) continue;
+        // the first tile: S^T and dP^T as soon as this item's K and V landed
+        ok = wait(bar(B_KV), kq & 1, 0x205) && issue_st(gbase);
+        if (!ok) break;
+        issue_dpt(gbase);
+        if (nt == 1) umma_commit(bar(B_KVEMPTY));  // no further reader of K and V
+        for (int m = 0; ok && m < nt; ++m) {
+          const int g = gbase + m, slot = g & 1;
+          const uint32_t X = slot ? kColRB : kColRA;
+          const uint32_t sQ = sbase + L::kQ + slot * L::kTileBytes;
+          const uint32_t sdO = sbase + L::kdO + slot * L::kTileBytes;
+          // dV += P^T dO as soon as P^T is in X, while the compute warps work on dS^T.
+          // P^T pairs: queries [0,64) at X columns [0,32), [64,128) at [64,96).  The first dV of
+          // an item overwrites the accumulator once the compute warps have read the previous one.
+          if (!wait(bar(B_PREADY), g & 1, 0x206) ||
+              (m == 0 && kq >= 1 && !wait(bar(B_ACCFREE), (kq - 1) & 1, 0x207))) {
+            ok = false;
             break;
+          }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_lo(tmem + Y, dK0 + kstep_kmajor(kk), sdesc_lo(sQn, 16u) + kstep_kmajor(kk), idSS,
-                       kk > 0 ? 1u : 0u);
-          umma_commit(bar(B_SFULL));
-        }
-        // dK += dS^T Q with dS^T read from X: queries [64h + 32c, +32) at columns 64h + 32 + 16c
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_lo(tmem + kColDV, tmem + X + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                       sdesc_lo(sdO, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+          if (!wait(bar(B_PDS), g & 1, 0x208)) { ok = false; break; }
+          tc_fence_after();
+          // the next tile's S^T into Y (its dP^T was consumed), so that its P can start while
+          // the tensor pipe runs dK
+          if (m + 1 < nt && !issue_st(g + 1)) { ok = false; break; }
+          // dK += dS^T Q with dS^T read from X: queries [64h + 32c, +32) at columns 64h + 32 + 16c
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts_lo(tmem + kColDK, tmem + X + 64 * (kk >> 2) + 32 + 8 * (kk & 3),
-                     sdesc_lo(sQ, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_QEMPTY + (m & 1)));
-        if (m + 1 < nt) {
-          // dP^T of the next tile into X, after dV and dK above have read P^T and dS^T from it
-          // (its dO landed with its Q, waited for before S^T)
-          const uint32_t sdOn = sbase + L::kdO + ((m + 1) & 1) * L::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_lo(tmem + X, dV0 + kstep_kmajor(kk), sdesc_lo(sdOn, 16u) + kstep_kmajor(kk), idSS,
-                       kk > 0 ? 1u : 0u);
-          umma_commit(bar(B_DPFULL));
-        } else {
-          umma_commit(bar(B_DONE));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_lo(tmem + kColDK, tmem + X + 64 * (kk >> 2) + 32 + 8 * (kk & 3),
+                       sdesc_lo(sQ, 16384u) + kstep_mnmajor(kk), idKM, (m > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(B_QEMPTY + slot));
+          if (m + 1 < nt) {
+            // dP^T of the next tile into X, after dV and dK above have read P^T and dS^T from it
+            issue_dpt(g + 1);
+            if (m + 2 == nt) umma_commit(bar(B_KVEMPTY));  // the item's last S^T and dP^T
+          }
         }
+        if (ok) umma_commit(bar(B_DONE));
+        gbase += nt;
+        ++kq;
       }
     }
   } else {
@@ -342,98 +402,132 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int quarter = warp & 3;
     const int hf = warp >> 2;
     const int r = quarter * 32 + lane;  // key row (S^T, dP^T, dV, dK)
-    const int j = kt * 128 + r;         // key column owned for S^T / dP^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    if (warp == 0 && h == 0) {
-      // The backward descriptor must describe the transposed mask of the forward one: tile
-      // (kt, q) of this bitmap row has the state of tile (q, kt) of the forward bitmap.  Checked
-      // once per key tile (head 0); a mismatch (two MaskSpecs that do not describe the same
-      // mask) is recorded in the status word, the computation goes on.
-      bool bad = false;
-      for (int q = lane; q < p.NT; q += 32) {
-        const uint32_t cb = (bmrow[q >> 4] >> (2 * (q & 15))) & 3u;
-        const uint32_t cf =
-            (p.bm_f[(static_cast<size_t>(b) * p.NT + q) * p.W + (kt >> 4)] >> (2 * (kt & 15))) & 3u;
-        bad |= cb != cf;
-      }
-      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, kDevDescMismatch, kt);
-    }
-    RowIntervals<MAXNI> ri;
-    load_row_intervals(p.itab, b, p.NI, p.S, j, ri);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int qt = next_tile(bmrow, p.NT, 0);
-    for (int m = 0; ok && m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
-      const bool full = tile_is_full(bmrow, qt);
-      const uint32_t X = (m & 1) ? kColRB : kColRA;
-      const uint32_t Y = (m & 1) ? kColRA : kColRB;
-
-      // ---- P^T: S^T from X, written back in place as bf16 pairs; fp32 P kept for dS ----
-      bool ready = wait(bar(B_SFULL), m & 1, 0x206) &&
-                   wait(bar(B_QFULL + (m & 1)), (m >> 1) & 1, 0x207);
+    int gbase = 0, kq = 0;
+    // An item's description and this key column's intervals are fetched one item ahead, so that
+    // the global loads overlap the previous item's epilogue.
+    struct Item {
+      int4 it;
+      RowIntervals<MAXNI> ri;
+    };
+    auto fetch = [&](int kf, Item& x) -> bool {
+      const bool ready = wait(bar(B_ROWFULL + (kf & 1)), (kf >> 1) & 1, 0x210);
       __syncwarp();
-      if (!ready) { ok = false; break; }
-      tc_fence_after();
-      float pf[2][32];
-      const uint32_t lse2_base = sbase + L::kLse2 + (m & 1) * 512u;
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int q0 = 64 * hf + 32 * ch;  // first query of the chunk within the tile
-        uint32_t sr[32], pp[16];
-        tmem_ld32(tmem + lane_off + X + q0, sr);
-        tmem_wait_ld();
-        if (full) {
-          p_chunk<true>(sr, lse2_base + q0 * 4u, sl2, 0u, pf[ch], pp);
-        } else {
-          const int i0 = qt * 128 + q0;
-          const uint32_t vis = visible_bits_any(i0, ri, p.NI, p.check, p.masked != 0);
-          p_chunk<false>(sr, lse2_base + q0 * 4u, sl2, vis, pf[ch], pp);
+      if (!ready) return false;
+      x.it = info[kf & 1];
+      if (x.it.x >= 0)
+        load_row_intervals(p.itab, x.it.x >> 16, p.NI, p.S, (x.it.x & 0xFFFF) * 128 + r, x.ri);
+      return true;
+    };
+    Item cur;
+    cur.it = make_int4(-1, 0, 0, 0);
+    ok = fetch(0, cur);
+    for (int k = 0; ok && cur.it.w == 0; ++k) {
+      const int rb = k & 1;
+      const uint32_t* bmrow = reinterpret_cast<const uint32_t*>(smem + L::kRow + rb * 256u);
+      const int nt = cur.it.z;
+      const int b = cur.it.x >> 16, kt = cur.it.x & 0xFFFF, h = cur.it.y;
+      const int row0 = (b * p.H + h) * p.S;
+      const int j = kt * 128 + r;  // key column owned for S^T / dP^T
+      if (warp == 0 && h == 0 && cur.it.x >= 0) {
+        // The backward descriptor must describe the transposed mask of the forward one: tile
+        // (kt, q) of this bitmap row has the state of tile (q, kt) of the forward bitmap.
+        // Checked once per key tile (head 0); a mismatch (two MaskSpecs that do not describe the
+        // same mask) is recorded in the status word, the computation goes on.
+        bool bad = false;
+        for (int q = lane; q < p.NT; q += 32) {
+          const uint32_t cb = (bmrow[q >> 4] >> (2 * (q & 15))) & 3u;
+          const uint32_t cf =
+              (p.bm_f[(static_cast<size_t>(b) * p.NT + q) * p.W + (kt >> 4)] >> (2 * (kt & 15))) & 3u;
+          bad |= cb != cf;
         }
-        // P^T pairs into X columns this warp has already read: hf * 64 + ch * 16
-        tmem_st16(tmem + lane_off + X + hf * 64 + ch * 16, pp);
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(p.status, kDevDescMismatch, kt);
       }
+      int qt = next_tile(bmrow, p.NT, 0);
+      for (int m = 0; m < nt; ++m, qt = next_tile(bmrow, p.NT, qt + 1)) {
+        const int g = gbase + m, slot = g & 1;
+        const bool full = tile_is_full(bmrow, qt);
+        const uint32_t X = slot ? kColRB : kColRA;
+        const uint32_t Y = slot ? kColRA : kColRB;
 
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PREADY));
-
-      // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T as bf16 pairs into X ----
-      ready = wait(bar(B_DPFULL), m & 1, 0x20e);
-      __syncwarp();
-      if (!ready) { ok = false; break; }
-      tc_fence_after();
+        // ---- P^T: S^T from X, written back in place as bf16 pairs; fp32 P kept for dS ----
+        bool ready = wait(bar(B_SFULL), g & 1, 0x211) &&
+                     wait(bar(B_QFULL + slot), (g >> 1) & 1, 0x212);
+        __syncwarp();
+        if (!ready) { ok = false; break; }
+        tc_fence_after();
+        float pf[2][32];
+        const uint32_t lse2_base = sbase + L::kLse2 + slot * 512u;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int q0 = 64 * hf + 32 * ch;
-        uint32_t dpr[32], dd[16];
-        tmem_ld32(tmem + lane_off + Y + q0, dpr);
-        tmem_wait_ld();
-        ds_chunk(pf[ch], dpr, sbase + L::kDelta + (m & 1) * 512u + q0 * 4u, dd);
-        // dS^T pairs into X columns this warp has read and P^T does not use: 64 hf + 32 + 16 ch
-        tmem_st16(tmem + lane_off + X + hf * 64 + 32 + ch * 16, dd);
+        for (int ch = 0; ch < 2; ++ch) {
+          const int q0 = 64 * hf + 32 * ch;  // first query of the chunk within the tile
+          uint32_t sr[32], pp[16];
+          tmem_ld32(tmem + lane_off + X + q0, sr);
+          tmem_wait_ld();
+          if (full) {
+            p_chunk<true>(sr, lse2_base + q0 * 4u, sl2, 0u, pf[ch], pp);
+          } else {
+            const int i0 = qt * 128 + q0;
+            const uint32_t vis = visible_bits_any(i0, cur.ri, p.NI, p.check, p.masked != 0);
+            p_chunk<false>(sr, lse2_base + q0 * 4u, sl2, vis, pf[ch], pp);
+          }
+          // P^T pairs into X columns this warp has already read: hf * 64 + ch * 16
+          tmem_st16(tmem + lane_off + X + hf * 64 + ch * 16, pp);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PREADY));
+
+        // ---- dS^T = P^T * (dP^T - D): dP^T from Y; dS^T as bf16 pairs into X ----
+        ready = wait(bar(B_DPFULL), g & 1, 0x213);
+        __syncwarp();
+        if (!ready) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int q0 = 64 * hf + 32 * ch;
+          uint32_t dpr[32], dd[16];
+          tmem_ld32(tmem + lane_off + Y + q0, dpr);
+          tmem_wait_ld();
+          ds_chunk(pf[ch], dpr, sbase + L::kDelta + slot * 512u + q0 * 4u, dd);
+          // dS^T pairs into X columns this warp has read and P^T does not use: 64 hf + 32 + 16 ch
+          tmem_st16(tmem + lane_off + X + hf * 64 + 32 + ch * 16, dd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PDS));
       }
-      tmem_wait_st();
-      tc_fence_before();
+      // the bitmap row and the item description are no longer needed
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PDS));
-
-    }
-    __syncwarp();
-
-    // ---- epilogue: dV, dK (scaled) -> bf16, this warp's half of the head dim ----
-    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
-    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
-    const bool done = nt > 0 && ok && wait(bar(B_DONE), 0, 0x20f);
-    __syncwarp();
-    if (done) {
+      if (lane == 0) mbar_arrive(bar(B_ROWEMPTY + rb));
+      if (!ok) break;
+      const Item done_item = cur;
+      if (!fetch(k + 1, cur)) { ok = false; break; }  // (the producer stages an end marker last)
+      if (done_item.it.x < 0) continue;  // an invalid schedule entry: nothing to write
+      __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
+      __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(row0) + j) * D + hf * kHalf;
+      if (nt == 0) {  // a key tile that no query sees
+        uint4* dva = reinterpret_cast<uint4*>(dvrow);
+        uint4* dka = reinterpret_cast<uint4*>(dkrow);
+        for (int q = 0; q < kHalf / 8; ++q) {
+          dva[q] = make_uint4(0, 0, 0, 0);
+          dka[q] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      // ---- epilogue: dV, dK (scaled) -> bf16, this warp's half of the head dim ----
+      const bool fin = wait(bar(B_DONE), kq & 1, 0x214);
+      __syncwarp();
+      if (!fin) { ok = false; break; }
       tc_fence_after();
       const float sc = p.scale;
-      // dV, then dK (scaled), as bf16 pairs of this row's columns, stored a warp's 32 rows at a
-      // time with coalesced stores
+      uint32_t ob[2][kHalf / 2];  // dV, then dK (scaled), as bf16 pairs of this row's columns
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
-        uint32_t ob[kHalf / 2];
 #pragma unroll
         for (int c = 0; c < kHalf; c += 32) {
           uint32_t a[32];
@@ -442,19 +536,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const float f = x == 0 ? 1.f : sc;
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            ob[(c + e) / 2] = pack_bf16x2(__uint_as_float(a[e]) * f, __uint_as_float(a[e + 1]) * f);
+            ob[x][(c + e) / 2] = pack_bf16x2(__uint_as_float(a[e]) * f, __uint_as_float(a[e + 1]) * f);
         }
-        __nv_bfloat16* rowp = x == 0 ? dvrow : dkrow;
-        store_rows_coalesced<kHalf / 8>(
-            ob, reinterpret_cast<char*>(rowp - static_cast<size_t>(lane) * D), D * 2u, lane);
       }
-    } else {
-      uint4* dva = reinterpret_cast<uint4*>(dvrow);
-      uint4* dka = reinterpret_cast<uint4*>(dkrow);
-      for (int q = 0; q < kHalf / 8; ++q) {
-        dva[q] = make_uint4(0, 0, 0, 0);
-        dka[q] = make_uint4(0, 0, 0, 0);
-      }
+      // the accumulators are free for the next item
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACCFREE));
+      // a warp's 32 rows at a time, with coalesced stores
+      store_rows_coalesced<kHalf / 8>(
+          ob[0], reinterpret_cast<char*>(dvrow - static_cast<size_t>(lane) * D), D * 2u, lane);
+      store_rows_coalesced<kHalf / 8>(
+          ob[1], reinterpret_cast<char*>(dkrow - static_cast<size_t>(lane) * D), D * 2u, lane);
+      gbase += nt;
+      ++kq;
     }
   }
 
@@ -464,10 +559,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (*abort_flag) {
     // A wait gave up.  Copies and MMAs already issued still land in shared memory and TMEM:
     // wait for them before TMEM is freed and the CTA exits.
-    if (warp == kProducerWarp && lane == 0 && nt > 0) {
-      mbar_wait_drain(bar(B_KV), 0, p.status, 0x2f0);
-      for (int s = 0; s < 2 && s < m_armed; ++s)
-        mbar_wait_drain(bar(B_QFULL + s), ((m_armed - 1 - s) >> 1) & 1, p.status, 0x2f1);
+    if (warp == kProducerWarp && lane == 0) {
+      if (kv_armed > 0) mbar_wait_drain(bar(B_KV), (kv_armed - 1) & 1, p.status, 0x2f0);
+      for (int g = g_armed - 2; g < g_armed; ++g)
+        if (g >= 0) mbar_wait_drain(bar(B_QFULL + (g & 1)), (g >> 1) & 1, p.status, 0x2f1);
     }
     if (warp == kMmaWarp && lane == 0 && mma_issued) {
       umma_commit(bar(B_DRAIN));
@@ -476,6 +571,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
   }
   tc_fence_after();
+  if (threadIdx.x == 0) queue_finish(queue);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
@@ -538,7 +634,13 @@ int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, co
   if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
       !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
     return -1;
-  const dim3 grid(p.B * p.NT * p.H);
+  // persistent: one CTA per SM (one fits: 195 KB of shared memory, all 512 TMEM columns)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return -1;
+  const int items = p.B * p.NT * p.H;
+  const dim3 grid(items < sms ? items : sms);
   // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
     if (p.NI <= 4) return bwd_launch<128, 4>(grid, stream, mq, mk, mv, mdo, p);

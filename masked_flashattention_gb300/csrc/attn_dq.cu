@@ -120,8 +120,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   constexpr int kHalf = D / 2;  // dQ columns per compute warp
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  int* const queue = p.status + 2 + 2 * (p.NT + 1) + 4;  // work queue (mask.cuh)
   if ((sbase & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment (see Smem)
     if (threadIdx.x == 0) set_status(p.status, kDevBadMeta, 0x3ff);
+    if (threadIdx.x == 0) queue_finish(queue);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -181,13 +183,25 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     bool ok = true;
     int gbase = 0;
-    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+    for (int k = 0; ok; ++k) {
       const int rb = k & 1;
       // the row buffer is free once its readers are done with item k - 2
       if (k >= 2) {
         const bool free_ = wait(bar(B_ROWEMPTY + rb), ((k >> 1) - 1) & 1, 0x300);
         __syncwarp();
         if (!free_) { ok = false; break; }
+      }
+      // the next work item from the queue (schedule order: longest rows first); the end
+      // marker stops every role
+      int j = 0;
+      if (lane == 0) j = atomicAdd(queue, 1);
+      j = __shfl_sync(0xFFFFFFFFu, j, 0);
+      if (j >= n_items) {
+        if (lane == 0) {
+          info[rb] = make_int4(-1, 0, 0, 1);
+          mbar_arrive(bar(B_ROWFULL + rb));
+        }
+        break;
       }
       int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
       cta_work(j, n_items / p.H, p.H, item_idx, h);
@@ -298,9 +312,10 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         return true;
       };
       bool ok = true;
-      for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+      for (int k = 0; ok; ++k) {
         const int rb = k & 1;
         if (!wait(bar(B_ROWFULL + rb), (k >> 1) & 1, 0x305)) break;
+        if (info[rb].w) break;  // no more work items
         const int nt = info[rb].z;
         mbar_arrive(bar(B_ROWEMPTY + rb));
         if (nt == 0) continue;
@@ -359,8 +374,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     };
     Item cur;
     cur.it = make_int4(-1, 0, 0, 0);
-    if (static_cast<int>(blockIdx.x) < n_items) ok = fetch(0, cur);
-    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+    ok = fetch(0, cur);
+    for (int k = 0; ok && cur.it.w == 0; ++k) {
       const int rb = k & 1;
       const uint32_t* bmrow = reinterpret_cast<const uint32_t*>(smem + L::kRow + rb * 256u);
       const int nt = cur.it.z;
@@ -433,9 +448,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       if (!ok) break;
       // the next item: description, intervals, constants, and its Q and dO into TMEM
       const Item done_item = cur;
-      if (j + static_cast<int>(gridDim.x) < n_items) {
-        if (!fetch(k + 1, cur)) { ok = false; break; }
-      }
+      if (!fetch(k + 1, cur)) { ok = false; break; }  // (the producer stages an end marker last)
       if (done_item.it.x < 0) continue;  // an invalid schedule entry: nothing to write
       __nv_bfloat16* qrow = p.dq + (row0 + i) * D + hf * kHalf;
       if (nt == 0) {  // a query tile that sees no key
@@ -492,6 +505,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __syncthreads();
   }
   tc_fence_after();
+  if (threadIdx.x == 0) queue_finish(queue);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 

@@ -112,8 +112,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   constexpr int kHalf = D / 2;  // output columns per softmax warp in the merge
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  int* const queue = p.status + 2 + 2 * (p.NT + 1) + 0;  // work queue (mask.cuh)
   if ((sbase & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment (see Smem)
     if (threadIdx.x == 0) set_status(p.status, kDevBadMeta, 0x1ff);
+    if (threadIdx.x == 0) queue_finish(queue);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -171,13 +173,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     bool ok = true;
     int gbase = 0;  // key tiles of the previous items
-    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+    for (int k = 0; ok; ++k) {
       const int rb = k & 1;
       // the row buffer is free once its readers are done with item k - 2
       if (k >= 2) {
         const bool free_ = wait(bar(B_ROWEMPTY + rb), ((k >> 1) - 1) & 1, 0x100);
         __syncwarp();
         if (!free_) { ok = false; break; }
+      }
+      // the next work item from the queue (schedule order: longest rows first); the end
+      // marker stops every role
+      int j = 0;
+      if (lane == 0) j = atomicAdd(queue, 1);
+      j = __shfl_sync(0xFFFFFFFFu, j, 0);
+      if (j >= n_items) {
+        if (lane == 0) {
+          info[rb] = make_int4(-1, 0, 0, 1);
+          mbar_arrive(bar(B_ROWFULL + rb));
+        }
+        break;
       }
       int item_idx, h;  // head-grouped chunks of the schedule (L2 locality, longest rows first)
       cta_work(j, n_items / p.H, p.H, item_idx, h);
@@ -287,9 +301,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         return true;
       };
       bool ok = true;
-      for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+      for (int k = 0; ok; ++k) {
         const int rb = k & 1;
         if (!wait(bar(B_ROWFULL + rb), (k >> 1) & 1, 0x106)) break;
+        if (info[rb].w) break;  // no more work items
         const int nt = info[rb].z;
         mbar_arrive(bar(B_ROWEMPTY + rb));
         if (nt == 0) continue;
@@ -336,8 +351,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         load_row_intervals(p.itab, itf.x >> 16, p.NI, p.S, (itf.x & 0xFFFF) * 128 + r, rif);
       return true;
     };
-    if (static_cast<int>(blockIdx.x) < n_items) ok = fetch(0, it, ri);
-    for (int j = blockIdx.x, k = 0; ok && j < n_items; j += gridDim.x, ++k) {
+    ok = fetch(0, it, ri);
+    for (int k = 0; ok && it.w == 0; ++k) {
       const int rb = k & 1;
       const uint32_t* bmrow = reinterpret_cast<const uint32_t*>(smem + L::kRow + rb * 256u);
       const int nt = it.z;
@@ -437,7 +452,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // the next item's description and intervals
       int4 it_next = make_int4(-1, 0, 0, 0);
       RowIntervals<MAXNI> ri_next;
-      if (j + static_cast<int>(gridDim.x) < n_items && !fetch(k + 1, it_next, ri_next)) {
+      if (!fetch(k + 1, it_next, ri_next)) {  // (the producer stages an end marker last)
         ok = false;
         break;
       }
@@ -521,6 +536,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
   }
   tc_fence_after();
+  if (threadIdx.x == 0) queue_finish(queue);
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 

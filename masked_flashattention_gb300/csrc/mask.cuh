@@ -42,6 +42,19 @@ __device__ __forceinline__ void cta_work(int q, int n_items, int H, int& item_id
   }
 }
 
+// Work queue of a persistent attention kernel (two ints in the descriptor's work buffer): q[0]
+// hands out work items in schedule order to whichever CTA asks next, q[1] counts the CTAs that
+// have finished.  The last CTA of a launch returns both to zero, ready for the next launch (every
+// CTA has taken its last item before it counts itself finished).
+__device__ __forceinline__ void queue_finish(int* q) {
+  __threadfence();
+  if (atomicAdd(q + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(q, 0);
+    atomicExch(q + 1, 0);
+    __threadfence();
+  }
+}
+
 // Forms of the partial-tile visibility check (full and empty tiles never run one):
 //   kCheckUnsigned    per score: for each stored interval [s, e) one subtraction and one unsigned
 //                     comparison, (u32)(x - s) < (u32)(e - s) (the paper's section 4.4 test);

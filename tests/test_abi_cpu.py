@@ -114,7 +114,7 @@ def test_descriptor_sizes(B):
     # status: the status word, the preprocess kernel's grid barrier and its two histograms of
     # per-row tile counts (0..NT)
     assert sizes == [2 * 3 * 32768 * 8, 2 * NT * 16 * 4, 2 * 2 * 32768 * 8, 2 * NT * 16 * 4,
-                     2 * NT * 4, 2 * NT * 4, 4 * (2 + 2 * (NT + 1))]
+                     2 * NT * 4, 2 * NT * 4, 4 * (2 + 2 * (NT + 1) + 6)]
     # masked form: one more slot per row (the runs around ni visible intervals)
     msizes = B.cm_descriptor_sizes(f, b, 2, 32768, form=B.CM_FORM_MASKED)
     assert msizes[0] == 2 * 4 * 32768 * 8 and msizes[2] == 2 * 3 * 32768 * 8
