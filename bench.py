@@ -2,7 +2,8 @@
 
 One step = the whole hot path on one batch of synthetic input already resident in HBM:
 Execution Descriptor build (preprocess kernels, forward and backward halves), attention forward,
-attention backward (D prologue, dK/dV kernel, dQ kernel), each stage bracketed by CUDA events.
+attention backward (dQ kernel, which also forms the per-row constants, then the dK/dV kernel),
+each stage bracketed by CUDA events.
 The headline workload is the shared-prompt RM mask at 32K; the three-interval packed 32K
 workload is timed in the same run and reported beside it.
 
@@ -245,7 +246,7 @@ def preprocess_sweep(Bd, fwd, bwd, seg_np, nseg_np, S, dev, target_mb=64.0, reps
     return {"B": Bs, "MB": nbytes / 2**20, "us": us, "gbs": nbytes / (us * 1e-6) / 1e9}
 
 
-STAGES = ("build", "fwd", "prologue", "dkdv", "dq")
+STAGES = ("build", "fwd", "dq", "dkdv")
 
 
 class Problem:
@@ -277,8 +278,9 @@ class Problem:
                               device=dev)
 
     def step(self, stream, ev=None, io=None):
-        """The whole hot path once: descriptor build, forward, backward (three stages).  `ev`
-        (6 CUDA events) brackets each stage; `io` swaps in another set of inputs and outputs."""
+        """The whole hot path once: descriptor build, forward, backward (dQ, which also forms the
+        per-row constants, then dK/dV).  `ev` (5 CUDA events) brackets each stage; `io` swaps in
+        another set of inputs and outputs."""
         Bd, x = self.Bd, io or self
         if ev is not None:
             ev[0].record(stream)
@@ -288,16 +290,14 @@ class Problem:
         Bd.cm_attn_fwd(self.desc, x.q, x.k, x.v, x.o, x.lse, self.scale, stream)
         if ev is not None:
             ev[2].record(stream)
-        Bd.cm_attn_bwd_prologue(x.o, x.lse, x.do, self.ws, stream)
+        Bd.cm_attn_bwd_dq(self.desc, x.q, x.k, x.v, x.o, x.lse, x.do, x.dq, self.ws, self.scale,
+                          stream)
         if ev is not None:
             ev[3].record(stream)
         Bd.cm_attn_bwd_dkdv(self.desc, x.q, x.k, x.v, x.do, x.dk, x.dv, self.ws, self.scale,
                             stream)
         if ev is not None:
             ev[4].record(stream)
-        Bd.cm_attn_bwd_dq(self.desc, x.q, x.k, x.v, x.do, x.dq, self.ws, self.scale, stream)
-        if ev is not None:
-            ev[5].record(stream)
 
     def check_status(self):
         st = self.Bd.cm_get_status(self.desc)
@@ -308,7 +308,8 @@ class Problem:
 def time_steps(prob, stream, steps):
     """Per-stage mean milliseconds over `steps` steps (CUDA events on the launching stream)."""
     import torch
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(steps)]
     for s in range(steps):
         prob.step(stream, evs[s])
     torch.cuda.synchronize(prob.dev)
@@ -332,9 +333,8 @@ def workload_report(prob, ms, pairs, tiles, peak_burst):
         exe = executed * d * E / t / 1e12
         kern[name] = {"ms": ms[name], "method_tflops": eff, "executed_tflops": exe,
                       "executed_frac_of_burst": exe / peak_burst}
-    kern["prologue"] = {"ms": ms["prologue"]}
     kern["build"] = {"ms": ms["build"]}
-    bwd_ms = ms["prologue"] + ms["dkdv"] + ms["dq"]
+    bwd_ms = ms["dkdv"] + ms["dq"]
     step_ms = ms["build"] + ms["fwd"] + bwd_ms
     eff_step = 14 * d * V / (step_ms / 1e3) / 1e12
     return {
@@ -535,7 +535,7 @@ def run_gpu(args):
                 prob.step(stream)
             ams = time_steps(prob, stream, args.steps)
             prob.check_status()
-            f_ms, b_ms = ams["fwd"], ams["prologue"] + ams["dkdv"] + ams["dq"]
+            f_ms, b_ms = ams["fwd"], ams["dkdv"] + ams["dq"]
             ablation[name] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_bwd_ms": f_ms + b_ms,
                               "dkdv_ms": ams["dkdv"], "dq_ms": ams["dq"]}
         prob.desc = visible_desc
@@ -600,8 +600,8 @@ def run_gpu(args):
                     "wall_s": e2e_wall,
                     "how": "copies on two copy streams, double-buffered, overlapping compute"},
             # per step: descriptor (one cooperative launch, after a memset of its counters),
-            # forward, prologue, dK/dV, dQ
-            "gpu_launches": 5 * args.steps,
+            # forward, dQ, dK/dV
+            "gpu_launches": 4 * args.steps,
             "clocks": clk,
         }
         if ablation is not None:

@@ -223,15 +223,17 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
                        void* dv, void* workspace, size_t workspace_bytes, int B, int H, int S,
                        int d, float scale, void* stream);
 
-/* The three stages of cm_attn_bwd, for callers that queue or time them one by one.  Queued in
- * this order on one stream with the same workspace they compute exactly what cm_attn_bwd does.
- *   cm_attn_bwd_prologue  writes the workspace: per row of B*H*S, -D = -sum_c dO[c] * O[c] and
- *                         -LSE * log2(e) (-inf for a row that sees nothing), fp32; reads o, lse,
- *                         d_o (device, layouts as above);
+/* The stages of cm_attn_bwd, for callers that queue or time them one by one.  cm_attn_bwd queues
+ * cm_attn_bwd_dq, then cm_attn_bwd_dkdv, on one stream with one workspace.
+ *   cm_attn_bwd_dq        dq along query tiles with the forward descriptor; reads q, k, v, o, lse,
+ *                         d_o (device, layouts as above) and writes the workspace: per row of
+ *                         every query tile that sees at least one key, -D = -sum_c dO[c] * O[c]
+ *                         and -LSE * log2(e) (-inf for a row that sees nothing), fp32;
  *   cm_attn_bwd_dkdv      dk, dv along key tiles with the backward descriptor (section 3.3);
- *                         reads q, k, v, d_o and the prologue's workspace;
- *   cm_attn_bwd_dq        dq along query tiles with the forward descriptor; reads q, k, v, d_o
- *                         and the prologue's workspace.
+ *                         reads q, k, v, d_o and the workspace written by cm_attn_bwd_dq (or by
+ *                         cm_attn_bwd_prologue) earlier on the same stream;
+ *   cm_attn_bwd_prologue  writes the whole workspace (every row) from o, lse and d_o alone, for
+ *                         callers that run cm_attn_bwd_dkdv without cm_attn_bwd_dq.
  * Same argument rules and error codes as cm_attn_bwd. */
 CM_API int cm_attn_bwd_prologue(const void* o, const float* lse, const void* d_o, void* workspace,
                                 size_t workspace_bytes, int B, int H, int S, int d,
@@ -241,9 +243,9 @@ CM_API int cm_attn_bwd_dkdv(const cm_descriptor* desc, const void* q, const void
                             const void* workspace, size_t workspace_bytes, int B, int H, int S,
                             int d, float scale, void* stream);
 CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* k, const void* v,
-                          const void* d_o, void* dq, const void* workspace,
-                          size_t workspace_bytes, int B, int H, int S, int d, float scale,
-                          void* stream);
+                          const void* o, const float* lse, const void* d_o, void* dq,
+                          void* workspace, size_t workspace_bytes, int B, int H, int S, int d,
+                          float scale, void* stream);
 
 /* Limit of every bounded wait inside the attention kernels, for the whole process, in ns
  * (0 restores the default of 2 s; at most 60 s, else CM_ERR_INVALID_ARG).  A wait that reaches it

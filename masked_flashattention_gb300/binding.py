@@ -81,8 +81,8 @@ def lib() -> ctypes.CDLL:
         L.cm_attn_bwd_prologue.argtypes = [vp, vp, vp, vp, sz, i32, i32, i32, i32, vp]
         L.cm_attn_bwd_dkdv.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp,
                                        sz, i32, i32, i32, i32, ctypes.c_float, vp]
-        L.cm_attn_bwd_dq.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, sz,
-                                     i32, i32, i32, i32, ctypes.c_float, vp]
+        L.cm_attn_bwd_dq.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp, vp,
+                                     vp, sz, i32, i32, i32, i32, ctypes.c_float, vp]
         L.cm_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         L.cm_attn_bwd_noalloc.argtypes = [ctypes.POINTER(cm_descriptor), vp, vp, vp, vp, vp, vp,
                                           vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
@@ -354,15 +354,16 @@ def cm_attn_bwd_dkdv(desc: Descriptor, q, k, v, d_o, dk, dv, workspace: torch.Te
            "cm_attn_bwd_dkdv")
 
 
-def cm_attn_bwd_dq(desc: Descriptor, q, k, v, d_o, dq, workspace: torch.Tensor,
+def cm_attn_bwd_dq(desc: Descriptor, q, k, v, o, lse, d_o, dq, workspace: torch.Tensor,
                    scale: float | None = None, stream=None) -> None:
-    """Stage 3 of cm_attn_bwd: dQ along query tiles (forward descriptor)."""
-    B, H, S, d = _bwd_shapes(q, ((k, "k"), (v, "v"), (d_o, "dO"), (dq, "dq")))
+    """First stage of cm_attn_bwd: dQ along query tiles (forward descriptor); also writes the
+    workspace's per-row constants (-D and -LSE*log2e) that cm_attn_bwd_dkdv reads."""
+    B, H, S, d = _bwd_shapes(q, ((k, "k"), (v, "v"), (o, "O"), (d_o, "dO"), (dq, "dq")))
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     nbytes = workspace.numel() * workspace.element_size()
     _check(lib().cm_attn_bwd_dq(ctypes.byref(desc.c), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                d_o.data_ptr(), dq.data_ptr(), workspace.data_ptr(), nbytes,
-                                B, H, S, d, scale, _stream(stream)),
+                                o.data_ptr(), lse.data_ptr(), d_o.data_ptr(), dq.data_ptr(),
+                                workspace.data_ptr(), nbytes, B, H, S, d, scale, _stream(stream)),
            "cm_attn_bwd_dq")
 
 

@@ -260,12 +260,12 @@ CM_API int cm_attn_bwd_dkdv(const cm_descriptor* desc, const void* q, const void
 }
 
 CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* k, const void* v,
-                          const void* d_o, void* dq, const void* workspace,
-                          size_t workspace_bytes, int B, int H, int S, int d, float scale,
-                          void* stream) {
+                          const void* o, const float* lse, const void* d_o, void* dq,
+                          void* workspace, size_t workspace_bytes, int B, int H, int S, int d,
+                          float scale, void* stream) {
   int rc = check_attn(desc, B, H, S, d, scale);
   if (rc != CM_OK) return rc;
-  rc = check_ptrs({q, k, v, d_o, dq});
+  rc = check_ptrs({q, k, v, o, lse, d_o, dq});
   if (rc != CM_OK) return rc;
   rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
   if (rc != CM_OK) return rc;
@@ -274,9 +274,10 @@ CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* 
   g.bm = desc->bm_f;
   g.sched = desc->sched_f;
   g.status = desc->status;
-  g.delta = static_cast<const float*>(workspace);
-  g.lse2 = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
-                                          row_floats_bytes(B, H, S));
+  g.delta = static_cast<float*>(workspace);
+  g.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + row_floats_bytes(B, H, S));
+  g.lse = lse;
+  g.o = static_cast<const __nv_bfloat16*>(o);
   g.q = static_cast<const __nv_bfloat16*>(q);
   g.d_o = static_cast<const __nv_bfloat16*>(d_o);
   g.dq = static_cast<__nv_bfloat16*>(dq);
@@ -307,13 +308,12 @@ CM_API int cm_attn_bwd(const cm_descriptor* desc, const void* q, const void* k, 
   if (rc != CM_OK) return rc;
   rc = check_workspace(workspace, workspace_bytes, B, H, S, d);
   if (rc != CM_OK) return rc;
-  rc = cm_attn_bwd_prologue(o, lse, d_o, workspace, workspace_bytes, B, H, S, d, stream);
+  // dQ first: it also writes the per-row constants that dK/dV reads
+  rc = cm_attn_bwd_dq(desc, q, k, v, o, lse, d_o, dq, workspace, workspace_bytes, B, H, S, d, scale,
+                      stream);
   if (rc != CM_OK) return rc;
-  rc = cm_attn_bwd_dkdv(desc, q, k, v, d_o, dk, dv, workspace, workspace_bytes, B, H, S, d, scale,
-                        stream);
-  if (rc != CM_OK) return rc;
-  return cm_attn_bwd_dq(desc, q, k, v, d_o, dq, workspace, workspace_bytes, B, H, S, d, scale,
-                        stream);
+  return cm_attn_bwd_dkdv(desc, q, k, v, d_o, dk, dv, workspace, workspace_bytes, B, H, S, d, scale,
+                          stream);
 }
 
 CM_API int cm_get_status(const cm_descriptor* desc, void* stream) {

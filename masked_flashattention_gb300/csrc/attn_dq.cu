@@ -18,6 +18,12 @@
 // once), so all three MMAs of a key tile take their A operand from TMEM and read only K or V from
 // shared memory: S = Q K^T, dP = dO V^T, dQ += dS K.
 //
+// The per-row constants of the backward come from here too: with its rows of dO the compute warps
+// load the same rows of O and form D = rowsum(dO * O) (the two warps of a row each sum half the
+// columns and exchange the halves), and take -LSE * log2(e) from the forward's LSE.  They use them
+// for dS and write them to the workspace, where the dK/dV kernel, queued after this one, reads
+// them: no separate pass over O and dO.
+//
 // Warp roles (352 threads):
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (query rows 32*(w%4) ..) and
 //              column half w / 4 of each 128-key tile: it reads S, then P = exp2(S *
@@ -72,7 +78,9 @@ struct Smem {
   // description {b << 16 | q_tile (or -1 for an invalid schedule entry), head, tile count}
   static constexpr uint32_t kRow = kBar + 256u;
   static constexpr uint32_t kInfo = kRow + 2u * 256u;
-  static constexpr uint32_t kTotal = kInfo + 32u;
+  // halves of D = rowsum(dO * O), exchanged by the two warps of a row: [2 halves][128 rows]
+  static constexpr uint32_t kDPart = kInfo + 32u;
+  static constexpr uint32_t kTotal = kDPart + 2u * 128u * 4u;
   static constexpr uint32_t kAlloc = kTotal;
 };
 static_assert(Smem<128>::kAlloc <= 232448, "dQ kernel shared memory exceeds 227 KB");
@@ -92,7 +100,8 @@ enum {
   B_DQFREE = 22,  // the compute warps have read the item's dQ (8 arrivals)
   B_ROWFULL = 23, // +buffer: the producer staged an item's bitmap row and description
   B_ROWEMPTY = 25,// +buffer: its readers are done with it (8 compute warps + 2 issuers)
-  B_COUNT = 27
+  B_DPAIR = 27,   // +quarter: the two warps of a row exchanged their halves of D (2 arrivals)
+  B_COUNT = 31
 };
 
 // Rows `row0 .. row0+31` (one per lane) of a [rows][D] bf16 matrix, this warp's half of their bf16
@@ -110,6 +119,31 @@ __device__ __forceinline__ void rows_to_tmem(const __nv_bfloat16* m, size_t row0
     load_rows_coalesced<4>(w, base, D * 2u, lane);
     tmem_st16(taddr, w);
   }
+}
+
+// Like rows_to_tmem for dO, and returns this lane's half of D = sum_c dO[c] * O[c] (fp32) over
+// the same columns of O.
+template <int D>
+__device__ __forceinline__ float do_rows_to_tmem(const __nv_bfloat16* d_o, const __nv_bfloat16* o,
+                                                 size_t row0, int hf, int lane, uint32_t taddr) {
+  constexpr int NC = D / 16;  // 16-byte chunks in half a row
+  const size_t off = row0 * D + hf * (D / 2);
+  uint32_t w[4 * NC], u[4 * NC];
+  load_rows_coalesced<NC>(w, reinterpret_cast<const char*>(d_o + off), D * 2u, lane);
+  load_rows_coalesced<NC>(u, reinterpret_cast<const char*>(o + off), D * 2u, lane);
+  if constexpr (D == 128) {
+    tmem_st32(taddr, w);
+  } else {
+    tmem_st16(taddr, w);
+  }
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < 4 * NC; ++e) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[e]));
+    acc = fma2(a, b, acc);
+  }
+  return acc.x + acc.y;
 }
 
 template <int D, int MAXNI>
@@ -160,6 +194,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
     mbar_init(bar(B_DQFREE), kComputeWarps);
+    for (int s = 0; s < 4; ++s) mbar_init(bar(B_DPAIR + s), 2);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -349,6 +384,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       RowIntervals<MAXNI> ri;
       float lse2, negd;  // -LSE * log2(e) (-inf for a row that sees nothing) and -D, per row
     };
+    int nprep = 0;  // items with key tiles prepared so far (phase of the D exchange)
     auto fetch = [&](int kf, Item& x) -> bool {
       const bool ready = wait(bar(B_ROWFULL + (kf & 1)), (kf >> 1) & 1, 0x310);
       __syncwarp();
@@ -358,17 +394,35 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const int b = x.it.x >> 16, qt = x.it.x & 0xFFFF;
       const size_t row = static_cast<size_t>(b * p.H + x.it.y) * p.S + qt * 128 + r;
       load_row_intervals(p.itab, b, p.NI, p.S, qt * 128 + r, x.ri);
-      x.lse2 = p.lse2[row];
-      x.negd = p.delta[row];
-      if (x.it.z > 0) {
-        // the warp's 32 rows of Q and dO into TMEM.  The previous item's S and dP MMAs, which
-        // read them, are done: this warp has read the last dP of that item.
-        rows_to_tmem<D>(p.q, row - lane, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
-        rows_to_tmem<D>(p.d_o, row - lane, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_QDO));
+      if (x.it.z == 0) return true;  // a query tile that sees no key: nothing to prepare
+      // the warp's 32 rows of Q and dO into TMEM.  The previous item's S and dP MMAs, which read
+      // them, are done: this warp has read the last dP of that item.
+      rows_to_tmem<D>(p.q, row - lane, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
+      const float dpart =
+          do_rows_to_tmem<D>(p.d_o, p.o, row - lane, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QDO));
+      // D = rowsum(dO * O): this warp's half and the other half's, through shared memory (the
+      // slot is rewritten only at the next item, after the partner has read it)
+      float* dslot = reinterpret_cast<float*>(smem + L::kDPart);  // [2 halves][128 rows]
+      dslot[hf * 128 + r] = dpart;
+      __syncwarp();
+      const uint32_t pb = bar(B_DPAIR + quarter);
+      if (lane == 0) mbar_arrive(pb);
+      const bool paired = wait(pb, nprep & 1, 0x314);
+      __syncwarp();
+      if (!paired) return false;
+      const float dsum = hf == 0 ? dpart + dslot[128 + r] : dslot[r] + dpart;
+      ++nprep;
+      const float l = p.lse[row];
+      x.lse2 = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
+      x.negd = -dsum;
+      // the per-row constants of the backward, for the dK/dV kernel that runs after this one
+      if (hf == 0) {
+        p.delta[row] = x.negd;
+        p.lse2[row] = x.lse2;
       }
       return true;
     };

@@ -55,10 +55,12 @@ struct DqParams {
   const uint32_t* bm;    // forward bitmaps [B][NT][W]
   const int32_t* sched;  // (b << 16 | q_tile), longest first
   int32_t* status;
-  const float* delta;    // [B][H][S] -rowsum(dO * O)
-  const float* lse2;     // [B][H][S] -LSE * log2(e)
-  const __nv_bfloat16* q;    // read once per CTA into TMEM
-  const __nv_bfloat16* d_o;  // read once per CTA into TMEM
+  float* delta;          // [B][H][S] -rowsum(dO * O), computed and written by the kernel
+  float* lse2;           // [B][H][S] -LSE * log2(e), computed and written by the kernel
+  const float* lse;      // [B][H][S] natural log (forward output)
+  const __nv_bfloat16* o;    // forward output, read once per work item (for D)
+  const __nv_bfloat16* q;    // read once per work item into TMEM
+  const __nv_bfloat16* d_o;  // read once per work item into TMEM
   __nv_bfloat16* dq;
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)

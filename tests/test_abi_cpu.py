@@ -186,10 +186,12 @@ def test_backward_stage_validation_happens_on_the_host(B):
                               None) == B.CM_ERR_INVALID_ARG
     assert L.cm_attn_bwd_dkdv(ctypes.byref(d), p, p, p, p, odd, p, p, need, 1, 2, 256, 64, 0.1,
                               None) == B.CM_ERR_INVALID_ARG
-    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, need - 1, 1, 2, 256, 64, 0.1,
+    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, p, p, need - 1, 1, 2, 256, 64, 0.1,
                             None) == B.CM_ERR_INVALID_ARG
-    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, need, 1, 2, 256, 64,
+    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, p, p, p, p, p, need, 1, 2, 256, 64,
                             float("inf"), None) == B.CM_ERR_INVALID_ARG
+    assert L.cm_attn_bwd_dq(ctypes.byref(d), p, p, p, None, p, p, p, p, need, 1, 2, 256, 64, 0.1,
+                            None) == B.CM_ERR_INVALID_ARG  # o is read for D
     # cm_attn_bwd checks everything before its first stage: a bad dq pointer is caught even
     # though the prologue's own arguments are fine
     assert L.cm_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, need, 1, 2, 256, 64,
