@@ -383,6 +383,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       int4 it;
       RowIntervals<MAXNI> ri;
       float lse2, negd;  // -LSE * log2(e) (-inf for a row that sees nothing) and -D, per row
+      float dpart;       // this warp's half of D, until the exchange with the other half completes
+      int dphase;        // phase of that exchange
     };
     int nprep = 0;  // items with key tiles prepared so far (phase of the D exchange)
     auto fetch = [&](int kf, Item& x) -> bool {
@@ -404,26 +406,19 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_QDO));
-      // D = rowsum(dO * O): this warp's half and the other half's, through shared memory (the
-      // slot is rewritten only at the next item, after the partner has read it)
+      // D = rowsum(dO * O): this warp's half goes to shared memory for the other half's warp;
+      // the exchange completes when the item starts (after the previous item's epilogue), so its
+      // latency stays off the critical path.  A slot is rewritten only at the next item, after
+      // the partner has read it.
       float* dslot = reinterpret_cast<float*>(smem + L::kDPart);  // [2 halves][128 rows]
       dslot[hf * 128 + r] = dpart;
       __syncwarp();
-      const uint32_t pb = bar(B_DPAIR + quarter);
-      if (lane == 0) mbar_arrive(pb);
-      const bool paired = wait(pb, nprep & 1, 0x314);
-      __syncwarp();
-      if (!paired) return false;
-      const float dsum = hf == 0 ? dpart + dslot[128 + r] : dslot[r] + dpart;
+      if (lane == 0) mbar_arrive(bar(B_DPAIR + quarter));
+      x.dpart = dpart;
+      x.dphase = nprep & 1;
       ++nprep;
       const float l = p.lse[row];
       x.lse2 = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
-      x.negd = -dsum;
-      // the per-row constants of the backward, for the dK/dV kernel that runs after this one
-      if (hf == 0) {
-        p.delta[row] = x.negd;
-        p.lse2[row] = x.lse2;
-      }
       return true;
     };
     Item cur;
@@ -436,6 +431,20 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const int b = cur.it.x >> 16, qt = cur.it.x & 0xFFFF;
       const size_t row0 = static_cast<size_t>(b * p.H + cur.it.y) * p.S;
       const int i = qt * 128 + r;
+      if (nt > 0) {
+        // the other half of D; then the per-row constants, for the dK/dV kernel that runs after
+        // this one
+        const float* dslot = reinterpret_cast<const float*>(smem + L::kDPart);
+        const bool paired = wait(bar(B_DPAIR + quarter), cur.dphase, 0x314);
+        __syncwarp();
+        if (!paired) { ok = false; break; }
+        const float dsum = hf == 0 ? cur.dpart + dslot[128 + r] : dslot[r] + cur.dpart;
+        cur.negd = -dsum;
+        if (hf == 0) {
+          p.delta[row0 + i] = cur.negd;
+          p.lse2[row0 + i] = cur.lse2;
+        }
+      }
       const float2 lse2x2 = make_float2(cur.lse2, cur.lse2), negd2 = make_float2(cur.negd, cur.negd);
       int kt = next_tile(bmrow, p.NT, 0);
       for (int n = 0; n < nt; ++n, kt = next_tile(bmrow, p.NT, kt + 1)) {
