@@ -210,10 +210,10 @@ CM_API int cm_attn_fwd(const cm_descriptor* desc, const void* q, const void* k, 
 CM_API int cm_attn_bwd_workspace_size(int B, int H, int S, int d, size_t* bytes);
 
 /* Backward: dq, dk, dv (device bf16 [B][H][S][d]) of sum(o * dO) given the forward's o and lse.
- * Section 3.3: each traversal direction has its own descriptor.  Three kernels, the three stages
- * below in this order: a prologue (D, LSE * log2(e) into the workspace), dK and dV along key
- * tiles with the backward half of the descriptor (itab_b, bm_b, sched_b), and dQ along query
- * tiles with the forward half (itab_f, bm_f, sched_f).  Every output element is written exactly
+ * Section 3.3: each traversal direction has its own descriptor.  Two kernels, the stages below
+ * in this order: dQ along query tiles with the forward half of the descriptor (itab_f, bm_f,
+ * sched_f), which also writes D and LSE * log2(e) into the workspace, then dK and dV along key
+ * tiles with the backward half (itab_b, bm_b, sched_b), which read them.  Every output element is written exactly
  * once (no atomics), so results are deterministic.  `workspace` (device, >= the size above,
  * 16-byte aligned) is overwritten.  Every argument is checked before the first stage is queued.
  * The dK/dV stage also checks on the device that bm_b is the transpose of bm_f and records

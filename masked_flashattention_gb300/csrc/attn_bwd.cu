@@ -2,13 +2,20 @@
 // for sm_103a.
 //
 // The backward pass traverses key tiles, so it uses the backward descriptor: per key column j,
-// the visible query intervals, and per (key tile, query tile) the 2-bit state.  One CTA owns one
-// 128-key tile of one (sample, head) and walks the non-empty query tiles of its bitmap row:
+// the visible query intervals, and per (key tile, query tile) the 2-bit state.  A work item is one
+// 128-key tile of one (sample, head); its CTA walks the non-empty query tiles of the item's
+// bitmap row:
 //
 //   S^T  = K Q^T            (tcgen05, TMEM)        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
 //   dP^T = V dO^T           (tcgen05, TMEM)        dS^T = P^T * (dP^T - D),  D = rowsum(dO * O)
 //   dK  += dS^T Q           (TMEM accumulator; dS^T is the A operand, read from TMEM)
 //   dV  += P^T dO           (TMEM accumulator; P^T is the A operand, read from TMEM)
+//
+// The CTAs are persistent (one per SM).  The producer warp takes items from a work queue in the
+// descriptor's status buffer (atomic counter over the schedule, longest bitmap rows first) and
+// stages each item's bitmap row and description into one of two buffers, so the next item's K, V
+// and first query tiles load while the current item's gradients are written.  LSE*log2e and -D
+// per query row come from the workspace that the dQ kernel fills; this kernel runs after it.
 //
 // dQ is computed by a second kernel that walks query tiles (attn_dq.cu); adding every key tile's
 // dQ partial into an fp32 accumulator here would make L2 read-modify-write traffic the bound.
@@ -21,8 +28,8 @@
 //   warps 0-7  compute.  Warp w serves TMEM lane quarter w % 4 (key rows 32*(w%4) ..) and column
 //              half w / 4: queries [64*half, +64) of S^T / dP^T and head-dim columns
 //              [half*d/2, +d/2) of dV and dK.
-//   warp 8     TMA producer: K, V once; per query tile Q and dO (+ LSE*log2e and D by bulk
-//              copy) into one of two slots, one barrier per slot.
+//   warp 8     producer: work queue, bitmap row; TMA of K, V once per item; per query tile Q
+//              and dO (+ LSE*log2e and -D by bulk copy) into one of two slots, one barrier each.
 //   warp 9     MMA issuer (one thread).
 // TMEM (512 columns): dV [0, d), dK [128, 128+d), and two 128-column regions RA [256, 384),
 // RB [384, 512) whose roles alternate between query tiles.  For tile m with X = RA (m even) or
@@ -35,9 +42,11 @@
 //   dS^T; once dS^T is written it issues S^T(m+1) -> Y (its dP^T was consumed), dK(m) (A = dS^T
 //   from X) and dP^T(m+1) -> X (after dV and dK read it).  Both gradient MMAs take their A operand
 //   from TMEM, so shared memory carries only K, V, Q and dO, and the next tile's P overlaps dK.
-// Shared memory: K, V, Q and dO (two slots each, 128-byte swizzle), LSE*log2e and D (per slot),
-// barriers, and the CTA's row of the backward bitmap (the non-empty query tiles are found by
-// scanning it).
+// Shared memory: K, V (one item), Q and dO (two slots each, 128-byte swizzle), LSE*log2e and -D
+// (per slot), barriers, and two item buffers (bitmap row of the backward bitmap, item description;
+// the non-empty query tiles are found by scanning the row).  The item's dK and dV leave TMEM
+// through registers and coalesced row stores once every MMA of the item is done; the next
+// item's first MMA waits only for the compute warps to have read them.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>

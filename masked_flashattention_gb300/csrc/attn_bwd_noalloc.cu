@@ -13,9 +13,9 @@
 // device address, so the address is looked up once per device with cudaGetSymbolAddress (with
 // that device current) and cached; the first call on a device does that lookup, so it should come
 // before any stream capture.  All calls share the array and it keeps the last call's contents:
-// the backward's prologue kernel rewrites D and LSE * log2(e) at the start of every call before
-// anything reads them, and calls whose work overlaps on the GPU (e.g. on different streams) race
-// on the array.
+// the backward's dQ kernel, which runs first, rewrites D and LSE * log2(e) of every row that the
+// dK/dV kernel will read, and calls whose work overlaps on the GPU (e.g. on different streams)
+// race on the array.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <mutex>

@@ -9,8 +9,8 @@
 // the forward Interval Table), recomputes S and dP, and keeps dQ in TMEM.  It writes dQ once, in
 // bf16, with no atomics.
 //
-// Persistent CTAs: one CTA per SM takes the work items j = blockIdx.x, + gridDim.x, ... of the
-// longest-first schedule.  Barrier phases, K/V slots and TMEM buffers run on across items (global
+// Persistent CTAs: one CTA per SM; its producer warp takes the next work item of the
+// longest-first schedule from a work queue (an atomic counter in the descriptor's status buffer).  Barrier phases, K/V slots and TMEM buffers run on across items (global
 // tile counter g), so the next item's K/V tiles load and its first S MMAs run while the compute
 // warps write the previous item's dQ.
 //

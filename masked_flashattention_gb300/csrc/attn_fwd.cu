@@ -5,8 +5,8 @@
 // mask, and partial tiles check every score against the row's intervals (mask.cuh), replacing
 // invisible scores with -inf before the online softmax.
 //
-// Persistent CTAs: one CTA per SM takes the work items j = blockIdx.x, + gridDim.x, ... of the
-// longest-first schedule.  Barrier phases, K/V stages and S buffers run on across items (global
+// Persistent CTAs: one CTA per SM; its producer warp takes the next work item of the
+// longest-first schedule from a work queue (an atomic counter in the descriptor's status buffer).  Barrier phases, K/V stages and S buffers run on across items (global
 // tile counter g), so the next item's Q and first K/V tiles load, and its first S MMAs run, while
 // the softmax warps finish the previous item's last tiles and write its O.
 //

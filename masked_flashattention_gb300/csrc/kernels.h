@@ -37,8 +37,8 @@ struct BwdParams {
   const int32_t* sched;  // (b << 16 | k_tile), longest first
   int32_t* status;
   const float* lse;      // [B][H][S] natural log (forward output)
-  float* delta;          // [B][H][S] -rowsum(dO * O), written by the prologue
-  float* lse2;           // [B][H][S] -LSE * log2(e) (-inf for rows that see nothing), prologue
+  float* delta;          // [B][H][S] -rowsum(dO * O), written by the dQ kernel (or prologue)
+  float* lse2;           // [B][H][S] -LSE * log2(e) (-inf for rows that see nothing), same
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H, S, NT, W, NI;
@@ -81,10 +81,12 @@ int launch_descriptor(const DevProg& fwd, const DevProg& bwd, const void* gen_ke
                       uint64_t wait_ns, cudaStream_t stream);
 int launch_attn_fwd(const FwdParams& p, int d, const void* q, const void* k, const void* v,
                     cudaStream_t stream);
-// Backward prologue: per row -D = -rowsum(dO * O) and -LSE * log2(e) (rows = B * H * S).
+// Backward prologue: per row -D = -rowsum(dO * O) and -LSE * log2(e) (rows = B * H * S), for
+// callers that run the dK/dV kernel without the dQ kernel.
 int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse, float* delta,
                         float* lse2, size_t rows, cudaStream_t stream);
-// dK and dV along key tiles (backward descriptor); reads the prologue's outputs.
+// dK and dV along key tiles (backward descriptor); reads the per-row constants that the dQ
+// kernel (or the prologue) wrote.
 int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, const void* v,
                      const void* d_o, cudaStream_t stream);
 int launch_attn_dq(const DqParams& p, int d, const void* k, const void* v, cudaStream_t stream);
