@@ -73,10 +73,13 @@ struct Smem {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kK = 0;                                 // kKStages slots
   static constexpr uint32_t kV = kK + kKStages * kTileBytes;        // kVStages slots
-  static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
+  // the next item's Q and dO tiles (TMA, 128-byte swizzle), copied into TMEM by the compute warps
+  static constexpr uint32_t kQS = kV + kVStages * kTileBytes;
+  static constexpr uint32_t kdOS = kQS + kTileBytes;
+  static constexpr uint32_t kBar = kdOS + kTileBytes;
   // per item (two buffers): the bitmap row (at most 64 words, NT <= 1024) and the item's
   // description {b << 16 | q_tile (or -1 for an invalid schedule entry), head, tile count}
-  static constexpr uint32_t kRow = kBar + 256u;
+  static constexpr uint32_t kRow = kBar + 512u;
   static constexpr uint32_t kInfo = kRow + 2u * 256u;
   // halves of D = rowsum(dO * O), exchanged by the two warps of a row: [2 halves][128 rows]
   static constexpr uint32_t kDPart = kInfo + 32u;
@@ -101,44 +104,37 @@ enum {
   B_ROWFULL = 23, // +buffer: the producer staged an item's bitmap row and description
   B_ROWEMPTY = 25,// +buffer: its readers are done with it (8 compute warps + 2 issuers)
   B_DPAIR = 27,   // +quarter: the two warps of a row exchanged their halves of D (2 arrivals)
-  B_COUNT = 31
+  B_QSFULL = 31,  // the next item's Q and dO tiles landed in shared memory (TMA)
+  B_QSEMPTY = 32, // the compute warps have copied them into TMEM (8 arrivals)
+  B_COUNT = 33
 };
+static_assert(8 * B_COUNT + 8 <= 512, "dQ kernel barrier area");
 
-// Rows `row0 .. row0+31` (one per lane) of a [rows][D] bf16 matrix, this warp's half of their bf16
-// pairs, into TMEM at `taddr` (coalesced loads; see load_rows_coalesced).
+// This lane's row of a 128-row tile staged by TMA with the 128-byte swizzle (boxes of 64 columns:
+// the 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16) of its box), this warp's
+// half of the columns, as bf16 pairs in w.  Lanes 8 apart read different chunk positions, so
+// the reads are free of bank conflicts.
 template <int D>
-__device__ __forceinline__ void rows_to_tmem(const __nv_bfloat16* m, size_t row0, int hf, int lane,
-                                             uint32_t taddr) {
-  const char* base = reinterpret_cast<const char*>(m + row0 * D + hf * (D / 2));
-  if constexpr (D == 128) {
-    uint32_t w[32];
-    load_rows_coalesced<8>(w, base, D * 2u, lane);
-    tmem_st32(taddr, w);
-  } else {
-    uint32_t w[16];
-    load_rows_coalesced<4>(w, base, D * 2u, lane);
-    tmem_st16(taddr, w);
+__device__ __forceinline__ void staged_row(uint32_t tile, int r, int hf, uint32_t (&w)[D / 4]) {
+  constexpr int NC = D / 16;                       // 16-byte chunks in half a row
+  const uint32_t box = tile + (D == 128 ? hf * 16384u : 0u);
+  const int c0 = D == 128 ? 0 : hf * NC;           // first chunk of the half within the box row
+  const uint32_t rowb = box + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint32_t addr = rowb + ((static_cast<uint32_t>(c0 + c) ^ (r & 7)) << 4);
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]), "=r"(w[4 * c + 3])
+                 : "r"(addr));
   }
 }
 
-// Like rows_to_tmem for dO, and returns this lane's half of D = sum_c dO[c] * O[c] (fp32) over
-// the same columns of O.
-template <int D>
-__device__ __forceinline__ float do_rows_to_tmem(const __nv_bfloat16* d_o, const __nv_bfloat16* o,
-                                                 size_t row0, int hf, int lane, uint32_t taddr) {
-  constexpr int NC = D / 16;  // 16-byte chunks in half a row
-  const size_t off = row0 * D + hf * (D / 2);
-  uint32_t w[4 * NC], u[4 * NC];
-  load_rows_coalesced<NC>(w, reinterpret_cast<const char*>(d_o + off), D * 2u, lane);
-  load_rows_coalesced<NC>(u, reinterpret_cast<const char*>(o + off), D * 2u, lane);
-  if constexpr (D == 128) {
-    tmem_st32(taddr, w);
-  } else {
-    tmem_st16(taddr, w);
-  }
+// This lane's half of D = sum_c dO[c] * O[c] (fp32) over the columns in w (dO) and u (O).
+template <int N>
+__device__ __forceinline__ float half_dot(const uint32_t (&w)[N], const uint32_t (&u)[N]) {
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 4 * NC; ++e) {
+  for (int e = 0; e < N; ++e) {
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[e]));
     acc = fma2(a, b, acc);
@@ -149,6 +145,7 @@ __device__ __forceinline__ float do_rows_to_tmem(const __nv_bfloat16* d_o, const
 template <int D, int MAXNI>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ DqParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;  // dQ columns per compute warp
@@ -195,6 +192,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(bar(B_DRAIN + 1), 1);
     mbar_init(bar(B_DQFREE), kComputeWarps);
     for (int s = 0; s < 4; ++s) mbar_init(bar(B_DPAIR + s), 2);
+    mbar_init(bar(B_QSFULL), 1);
+    mbar_init(bar(B_QSEMPTY), kComputeWarps);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -205,9 +204,9 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // asynchronous work issued so far, for the abort path: K and V slots armed (producer), any MMA
-  // issued (issuers)
-  int gk_armed = 0, gv_armed = 0;
+  // asynchronous work issued so far, for the abort path: K and V slots and Q/dO stagings armed
+  // (producer), any MMA issued (issuers)
+  int gk_armed = 0, gv_armed = 0, qs_armed = 0;
   bool mma_issued = false;
 
   if (warp == kProducerWarp) {
@@ -215,6 +214,8 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
     }
     bool ok = true;
     int gbase = 0;
@@ -262,8 +263,22 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       if (lane == 0) mbar_arrive(bar(B_ROWFULL + rb));
       if (lane == 0 && cnt > 0) {
         const int row0 = (b * p.H + h) * p.S;
+        // Q and dO of this item into the staging tiles once the compute warps have copied the
+        // previous item's into TMEM; O and the LSE, which they read from global memory, into L2
+        if (qs_armed > 0 && !wait(bar(B_QSEMPTY), (qs_armed - 1) & 1, 0x309)) ok = false;
+        if (ok) {
+          ++qs_armed;
+          mbar_arrive_expect_tx(bar(B_QSFULL), 2u * L::kTileBytes);
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_2d(sbase + L::kQS + x * 16384u, &tmQ, x * 64, row0 + qt * 128, bar(B_QSFULL));
+            tma_load_2d(sbase + L::kdOS + x * 16384u, &tmdO, x * 64, row0 + qt * 128, bar(B_QSFULL));
+          }
+          const size_t r0 = static_cast<size_t>(row0) + qt * 128;
+          prefetch_l2_bulk(p.o + r0 * D, L::kTileBytes);
+          prefetch_l2_bulk(p.lse + r0, 512u);
+        }
         int kt = next_tile(row, p.NT, 0);
-        for (int n = 0; n < cnt; ++n, kt = next_tile(row, p.NT, kt + 1)) {
+        for (int n = 0; ok && n < cnt; ++n, kt = next_tile(row, p.NT, kt + 1)) {
           const int g = gbase + n, sk = g % kKStages, sv = g % kVStages;
           if (g >= kKStages && !wait(bar(B_KEMPTY + sk), ((g / kKStages) - 1) & 1, 0x301)) {
             ok = false;
@@ -397,14 +412,28 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const size_t row = static_cast<size_t>(b * p.H + x.it.y) * p.S + qt * 128 + r;
       load_row_intervals(p.itab, b, p.NI, p.S, qt * 128 + r, x.ri);
       if (x.it.z == 0) return true;  // a query tile that sees no key: nothing to prepare
-      // the warp's 32 rows of Q and dO into TMEM.  The previous item's S and dP MMAs, which read
-      // them, are done: this warp has read the last dP of that item.
-      rows_to_tmem<D>(p.q, row - lane, hf, lane, tmem + lane_off + kColQ + hf * (D / 4));
-      const float dpart =
-          do_rows_to_tmem<D>(p.d_o, p.o, row - lane, hf, lane, tmem + lane_off + kColDO + hf * (D / 4));
+      const float l = p.lse[row];
+      // this warp's half of the row of O (for D), from global memory (the producer prefetched it
+      // into L2); then Q and dO from the staging tiles into TMEM.  The previous item's S and dP
+      // MMAs, which read Q and dO in TMEM, are done: this warp has read the last dP of that item.
+      constexpr int NC = D / 16;
+      uint32_t u[4 * NC], w[4 * NC];
+      load_rows_coalesced<NC>(u, reinterpret_cast<const char*>(p.o + (row - lane) * D + hf * (D / 2)),
+                              D * 2u, lane);
+      const bool staged = wait(bar(B_QSFULL), nprep & 1, 0x315);
+      __syncwarp();
+      if (!staged) return false;
+      staged_row<D>(sbase + L::kQS, r, hf, w);
+      if constexpr (D == 128) tmem_st32(tmem + lane_off + kColQ + hf * (D / 4), w);
+      else tmem_st16(tmem + lane_off + kColQ + hf * (D / 4), w);
+      staged_row<D>(sbase + L::kdOS, r, hf, w);
+      if constexpr (D == 128) tmem_st32(tmem + lane_off + kColDO + hf * (D / 4), w);
+      else tmem_st16(tmem + lane_off + kColDO + hf * (D / 4), w);
+      const float dpart = half_dot(w, u);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QSEMPTY));  // the staging tiles are read
       if (lane == 0) mbar_arrive(bar(B_QDO));
       // D = rowsum(dO * O): this warp's half goes to shared memory for the other half's warp;
       // the exchange completes when the item starts (after the previous item's epilogue), so its
@@ -417,7 +446,6 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       x.dpart = dpart;
       x.dphase = nprep & 1;
       ++nprep;
-      const float l = p.lse[row];
       x.lse2 = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
       return true;
     };
@@ -560,6 +588,7 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       for (int g = gv_armed - kVStages; g < gv_armed; ++g)
         if (g >= 0)
           mbar_wait_drain(bar(B_VFULL + g % kVStages), (g / kVStages) & 1, p.status, 0x3f2);
+      if (qs_armed > 0) mbar_wait_drain(bar(B_QSFULL), (qs_armed - 1) & 1, p.status, 0x3f4);
     }
     if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0 && mma_issued) {
       umma_commit(bar(B_DRAIN + warp - kMmaWarp));
@@ -576,20 +605,22 @@ attn_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
 template <int D, int MAXNI>
 int dq_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mk, const CUtensorMap& mv,
-              const DqParams& p) {
+              const CUtensorMap& mq, const CUtensorMap& mdo, const DqParams& p) {
   const uint32_t smem = dq::Smem<D>::kAlloc;
   if (cudaFuncSetAttribute(dq::attn_dq_kernel<D, MAXNI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return -1;
-  dq::attn_dq_kernel<D, MAXNI><<<grid, dq::kThreads, smem, stream>>>(mk, mv, p);
+  dq::attn_dq_kernel<D, MAXNI><<<grid, dq::kThreads, smem, stream>>>(mk, mv, mq, mdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_attn_dq(const DqParams& p, int d, const void* k, const void* v, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
-  CUtensorMap mk, mv;
-  if (!make_bf16_tile_map(&mk, k, rows, d) || !make_bf16_tile_map(&mv, v, rows, d)) return -1;
-  // persistent: one CTA per SM (one fits: 160 KB of shared memory, all 512 TMEM columns)
+  CUtensorMap mk, mv, mq, mdo;
+  if (!make_bf16_tile_map(&mk, k, rows, d) || !make_bf16_tile_map(&mv, v, rows, d) ||
+      !make_bf16_tile_map(&mq, p.q, rows, d) || !make_bf16_tile_map(&mdo, p.d_o, rows, d))
+    return -1;
+  // persistent: one CTA per SM (one fits: 226 KB of shared memory, all 512 TMEM columns)
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -598,11 +629,11 @@ int launch_attn_dq(const DqParams& p, int d, const void* k, const void* v, cudaS
   const dim3 grid(items < sms ? items : sms);
   // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
-    if (p.NI <= 4) return dq_launch<128, 4>(grid, stream, mk, mv, p);
-    return dq_launch<128, 9>(grid, stream, mk, mv, p);
+    if (p.NI <= 4) return dq_launch<128, 4>(grid, stream, mk, mv, mq, mdo, p);
+    return dq_launch<128, 9>(grid, stream, mk, mv, mq, mdo, p);
   }
-  if (p.NI <= 4) return dq_launch<64, 4>(grid, stream, mk, mv, p);
-  return dq_launch<64, 9>(grid, stream, mk, mv, p);
+  if (p.NI <= 4) return dq_launch<64, 4>(grid, stream, mk, mv, mq, mdo, p);
+  return dq_launch<64, 9>(grid, stream, mk, mv, mq, mdo, p);
 }
 
 }  // namespace cm
