@@ -79,7 +79,9 @@ struct Smem {
   static constexpr uint32_t kV = kTileBytes;
   static constexpr uint32_t kQ = 2 * kTileBytes;      // two slots
   static constexpr uint32_t kdO = 4 * kTileBytes;      // two slots
-  static constexpr uint32_t kLse2 = 6 * kTileBytes;    // [2 slots][128 floats]: -LSE * log2(e)
+  // an item's dV, then its dK, on their way out (bf16, laid out for the TMA store)
+  static constexpr uint32_t kStage = 6 * kTileBytes;
+  static constexpr uint32_t kLse2 = 7 * kTileBytes;    // [2 slots][128 floats]: -LSE * log2(e)
   static constexpr uint32_t kDelta = kLse2 + 1024u;    // [2 slots][128 floats]: -D
   static constexpr uint32_t kBar = kDelta + 1024u;
   // per item (two buffers): the bitmap row (at most 64 words, NT <= 1024) and the item's
@@ -108,8 +110,12 @@ enum {
   B_ACCFREE = 12,  // the compute warps have read the item's dV and dK (8 arrivals)
   B_ROWFULL = 13,  // +buffer: the producer staged an item's bitmap row and description
   B_ROWEMPTY = 15, // +buffer: its readers are done with it (8 compute warps + the MMA thread)
-  B_COUNT = 17
+  B_SDV = 17,      // the compute warps wrote the item's dV into the staging tile (8 arrivals)
+  B_SDK = 18,      // ... and then its dK (8 arrivals)
+  B_SFREE = 19,    // the TMA store of the staging tile has read it (twice per item: dV, dK)
+  B_COUNT = 20
 };
+static_assert(8 * B_COUNT + 8 <= 256, "backward barrier area");
 
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -176,6 +182,7 @@ template <int D, int MAXNI>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                 const __grid_constant__ BwdParams p) {
   using L = Smem<D>;
   constexpr int kHalf = D / 2;           // head-dim columns per compute warp
@@ -215,6 +222,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_KVEMPTY), 1);
     mbar_init(bar(B_ACCFREE), kComputeWarps);
+    mbar_init(bar(B_SDV), kComputeWarps);
+    mbar_init(bar(B_SDK), kComputeWarps);
+    mbar_init(bar(B_SFREE), 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -415,6 +425,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float sl2 = p.scale_log2;
     bool ok = true;
     int gbase = 0, kq = 0;
+    int ne = 0;  // items whose dV and dK went out through the staging tile
     // An item's description and this key column's intervals are fetched one item ahead, so that
     // the global loads overlap the previous item's epilogue.
     struct Item {
@@ -552,14 +563,44 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_ACCFREE));
-      // a warp's 32 rows at a time, with coalesced stores
-      store_rows_coalesced<kHalf / 8>(
-          ob[0], reinterpret_cast<char*>(dvrow - static_cast<size_t>(lane) * D), D * 2u, lane);
-      store_rows_coalesced<kHalf / 8>(
-          ob[1], reinterpret_cast<char*>(dkrow - static_cast<size_t>(lane) * D), D * 2u, lane);
+      // dV, then dK, leave through the staging tile: each warp writes its rows and columns there,
+      // one thread stores the tile with TMA.  The stores run on while the next item starts; the
+      // tile is rewritten once the previous store has read it.
+      const bool storer = warp == 0 && lane == 0;
+      const uint32_t stg = sbase + L::kStage;
+      for (int x = 0; x < 2 && ok; ++x) {
+        const int step = 2 * ne + x;  // stores through the staging tile so far
+        if (step > 0) {
+          if (storer) {
+            bulk_wait_read_all();
+            mbar_arrive(bar(B_SFREE));
+          }
+          const bool free_ = wait(bar(B_SFREE), (step - 1) & 1, 0x215);
+          __syncwarp();
+          if (!free_) { ok = false; break; }
+        }
+        const uint32_t box = stg + (D == 128 ? hf * 16384u : 0u);
+        const int c0 = D == 128 ? 0 : hf * (kHalf / 8);
+#pragma unroll
+        for (int c = 0; c < kHalf / 8; ++c)
+          st_shared_v4(swz128_chunk(box, r, c0 + c), ob[x][4 * c], ob[x][4 * c + 1], ob[x][4 * c + 2],
+                       ob[x][4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(x == 0 ? B_SDV : B_SDK));
+        if (storer) {
+          if (!wait(bar(x == 0 ? B_SDV : B_SDK), ne & 1, 0x216)) { ok = false; break; }
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_2d(x == 0 ? &tmdV : &tmdK, bx * 64, row0 + kt * 128, stg + bx * 16384u);
+          bulk_commit_group();
+        }
+      }
+      ++ne;
       gbase += nt;
       ++kq;
     }
+    // the last TMA stores complete before the CTA exits (and its shared memory goes)
+    if (warp == 0 && lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -627,23 +668,26 @@ int launch_bwd_prologue(int d, const void* o, const void* d_o, const float* lse,
 }
 
 template <int D, int MAXNI>
-int bwd_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, const BwdParams& p) {
+int bwd_launch(dim3 grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk,
+               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdk,
+               const CUtensorMap& mdv, const BwdParams& p) {
   const uint32_t smem = bwd::Smem<D>::kAlloc;
   if (cudaFuncSetAttribute(bwd::attn_bwd_kernel<D, MAXNI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return -1;
-  bwd::attn_bwd_kernel<D, MAXNI><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  bwd::attn_bwd_kernel<D, MAXNI><<<grid, bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, const void* v,
                      const void* d_o, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.H * p.S;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   if (!make_bf16_tile_map(&mq, q, rows, d) || !make_bf16_tile_map(&mk, k, rows, d) ||
-      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d))
+      !make_bf16_tile_map(&mv, v, rows, d) || !make_bf16_tile_map(&mdo, d_o, rows, d) ||
+      !make_bf16_tile_map(&mdk, p.dk, rows, d) || !make_bf16_tile_map(&mdv, p.dv, rows, d))
     return -1;
-  // persistent: one CTA per SM (one fits: 195 KB of shared memory, all 512 TMEM columns)
+  // persistent: one CTA per SM (one fits: 227 KB of shared memory, all 512 TMEM columns)
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -652,11 +696,11 @@ int launch_attn_dkdv(const BwdParams& p, int d, const void* q, const void* k, co
   const dim3 grid(items < sms ? items : sms);
   // interval registers: 4 cover every visible-form workload here; 9 the largest tables
   if (d == 128) {
-    if (p.NI <= 4) return bwd_launch<128, 4>(grid, stream, mq, mk, mv, mdo, p);
-    return bwd_launch<128, 9>(grid, stream, mq, mk, mv, mdo, p);
+    if (p.NI <= 4) return bwd_launch<128, 4>(grid, stream, mq, mk, mv, mdo, mdk, mdv, p);
+    return bwd_launch<128, 9>(grid, stream, mq, mk, mv, mdo, mdk, mdv, p);
   }
-  if (p.NI <= 4) return bwd_launch<64, 4>(grid, stream, mq, mk, mv, mdo, p);
-  return bwd_launch<64, 9>(grid, stream, mq, mk, mv, mdo, p);
+  if (p.NI <= 4) return bwd_launch<64, 4>(grid, stream, mq, mk, mv, mdo, mdk, mdv, p);
+  return bwd_launch<64, 9>(grid, stream, mq, mk, mv, mdo, mdk, mdv, p);
 }
 
 }  // namespace cm

@@ -110,19 +110,16 @@ enum {
 };
 static_assert(8 * B_COUNT + 8 <= 512, "dQ kernel barrier area");
 
-// This lane's row of a 128-row tile staged by TMA with the 128-byte swizzle (boxes of 64 columns:
-// the 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16) of its box), this warp's
-// half of the columns, as bf16 pairs in w.  Lanes 8 apart read different chunk positions, so
-// the reads are free of bank conflicts.
+// This lane's row of a 128-row tile staged by TMA with the 128-byte swizzle (boxes of 64
+// columns), this warp's half of the columns, as bf16 pairs in w; free of bank conflicts.
 template <int D>
 __device__ __forceinline__ void staged_row(uint32_t tile, int r, int hf, uint32_t (&w)[D / 4]) {
   constexpr int NC = D / 16;                       // 16-byte chunks in half a row
   const uint32_t box = tile + (D == 128 ? hf * 16384u : 0u);
   const int c0 = D == 128 ? 0 : hf * NC;           // first chunk of the half within the box row
-  const uint32_t rowb = box + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    const uint32_t addr = rowb + ((static_cast<uint32_t>(c0 + c) ^ (r & 7)) << 4);
+    const uint32_t addr = swz128_chunk(box, r, c0 + c);
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]), "=r"(w[4 * c + 3])
                  : "r"(addr));

@@ -145,13 +145,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// element-wise add of a shared-memory tile into global memory through a tensor map
-// (fp32 add for an fp32 map); completion is tracked with bulk groups of the issuing thread
-__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t x, int32_t y,
-                                                  uint32_t src) {
+// store of a shared-memory tile (laid out as a TMA load of the same box would leave it) into
+// global memory through a tensor map; completion is tracked with bulk groups of the issuing thread
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {
   asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
@@ -444,6 +443,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Address of the 16-byte chunk c of row r in a box of 128-byte rows laid out with the 128-byte
+// swizzle (what a TMA load of the box with that swizzle leaves in shared memory, and what a TMA
+// store of it expects; the box starts on a 1024-byte boundary): r * 128 + ((c ^ (r % 8)) * 16).
+// The 8 lanes of a quarter-warp that access the same chunk of 8 consecutive rows hit 8 different
+// 16-byte bank groups.
+__device__ __forceinline__ uint32_t swz128_chunk(uint32_t box, int r, int c) {
+  return box + static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4);
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
