@@ -10,9 +10,11 @@
 // bf16, with no atomics.
 //
 // Persistent CTAs: one CTA per SM; its producer warp takes the next work item of the
-// longest-first schedule from a work queue (an atomic counter in the descriptor's status buffer).  Barrier phases, K/V slots and TMEM buffers run on across items (global
-// tile counter g), so the next item's K/V tiles load and its first S MMAs run while the compute
-// warps write the previous item's dQ.
+// longest-first schedule from a work queue (an atomic counter in the descriptor's status
+// buffer).  Barrier phases, K/V slots and TMEM buffers run on across items (global tile counter
+// g), so the next item's K/V tiles load and its first S MMAs run while the compute warps write
+// the previous item's dQ.  The producer also brings the next item's Q and dO tiles into shared
+// memory (TMA), from where the compute warps copy them into TMEM at the item boundary.
 //
 // Q and dO stay in TMEM for a whole item (the compute warps load their rows from global memory
 // once), so all three MMAs of a key tile take their A operand from TMEM and read only K or V from
