@@ -44,9 +44,11 @@
 //   from TMEM, so shared memory carries only K, V, Q and dO, and the next tile's P overlaps dK.
 // Shared memory: K, V (one item), Q and dO (two slots each, 128-byte swizzle), LSE*log2e and -D
 // (per slot), barriers, and two item buffers (bitmap row of the backward bitmap, item description;
-// the non-empty query tiles are found by scanning the row).  The item's dK and dV leave TMEM
-// through registers and coalesced row stores once every MMA of the item is done; the next
-// item's first MMA waits only for the compute warps to have read them.
+// the non-empty query tiles are found by scanning the row), and a staging tile through which the
+// item's dV and then dK leave: once every MMA of the item is done the compute warps read them
+// from TMEM, write them there in the layout of a TMA load, and one thread stores the tile with
+// TMA.  The next item's first MMA waits only for the compute warps to have read the
+// accumulators.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>

@@ -16,8 +16,8 @@
 // the previous item's dQ.  The producer also brings the next item's Q and dO tiles into shared
 // memory (TMA), from where the compute warps copy them into TMEM at the item boundary.
 //
-// Q and dO stay in TMEM for a whole item (the compute warps load their rows from global memory
-// once), so all three MMAs of a key tile take their A operand from TMEM and read only K or V from
+// Q and dO stay in TMEM for a whole item (the compute warps copy their rows there once), so all
+// three MMAs of a key tile take their A operand from TMEM and read only K or V from
 // shared memory: S = Q K^T, dP = dO V^T, dQ += dS K.
 //
 // The per-row constants of the backward come from here too: with its rows of dO the compute warps
@@ -32,7 +32,8 @@
 //              scale*log2e - LSE*log2e) stays in registers while dP is computed into the same
 //              TMEM columns, then dS = P * (dP - D) is written back there as bf16 pairs.
 //   warp 8     producer: per item, stages the bitmap row in shared memory (the whole warp), then
-//              lane 0 loads K through a 3-slot ring and V through a 2-slot ring.
+//              lane 0 loads the item's Q and dO into the staging tiles (one item ahead), and K
+//              through a 3-slot ring and V through a 2-slot ring.
 //   warps 9-10 MMA issuers, one thread each: the thread of warp 9 + t issues S(g), dP(g) and
 //              dQ(g) of the key tiles g with g % 2 == t.  A thread that issues tcgen05 MMAs
 //              stalls on every barrier wait, and the tensor pipe holds too few queued 128 x 128
