@@ -342,9 +342,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // instruction it needs between MMAs leaves the tensor pipe waiting longer)
       const uint32_t dK0 = sdesc_lo(sK, 16u), dV0 = sdesc_lo(sV, 16u);
       // S^T(g) = K Q(g)^T -> region X(g) (g even: RA, odd: RB); dP^T(g) = V dO(g)^T -> X(g + 1)
-      auto issue_st = [&](int g) -> bool {
+      // first: the first tile of an item.  For the others the compute warps saw Q and dO of the
+      // tile land before their PDS arrival, which this thread has waited for: one wait less in
+      // the issue loop (each costs the tensor pipe a gap)
+      auto issue_st = [&](int g, bool first) -> bool {
         const int slot = g & 1;
-        if (!wait(bar(B_QFULL + slot), (g >> 1) & 1, 0x203)) return false;
+        if (first && !wait(bar(B_QFULL + slot), (g >> 1) & 1, 0x203)) return false;
         tc_fence_after();
         mma_issued = true;
         const uint32_t X = slot ? kColRB : kColRA;
@@ -374,7 +377,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_arrive(bar(B_ROWEMPTY + rb));
         if (nt == 0) continue;
         // the first tile: S^T and dP^T as soon as this item's K and V landed
-        ok = wait(bar(B_KV), kq & 1, 0x205) && issue_st(gbase);
+        ok = wait(bar(B_KV), kq & 1, 0x205) && issue_st(gbase, true);
         if (!ok) break;
         issue_dpt(gbase);
         if (nt == 1) umma_commit(bar(B_KVEMPTY));  // no further reader of K and V
@@ -400,7 +403,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
           // the next tile's S^T into Y (its dP^T was consumed), so that its P can start while
           // the tensor pipe runs dK
-          if (m + 1 < nt && !issue_st(g + 1)) { ok = false; break; }
+          if (m + 1 < nt && !issue_st(g + 1, false)) { ok = false; break; }
           // dK += dS^T Q with dS^T read from X: queries [64h + 32c, +32) at columns 64h + 32 + 16c
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -520,6 +523,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         tmem_wait_st();
         tc_fence_before();
+        // the next tile's Q and dO have landed (the MMA thread relies on it for S^T(g+1))
+        if (m + 1 < nt) {
+          ready = wait(bar(B_QFULL + (slot ^ 1)), ((g + 1) >> 1) & 1, 0x218);
+          __syncwarp();
+          if (!ready) { ok = false; break; }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_PDS));
       }
