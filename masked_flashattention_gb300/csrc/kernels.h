@@ -59,8 +59,8 @@ struct DqParams {
   float* lse2;           // [B][H][S] -LSE * log2(e), computed and written by the kernel
   const float* lse;      // [B][H][S] natural log (forward output)
   const __nv_bfloat16* o;    // forward output, read once per work item (for D)
-  const __nv_bfloat16* q;    // read once per work item into TMEM
-  const __nv_bfloat16* d_o;  // read once per work item into TMEM
+  const __nv_bfloat16* q;    // staged once per work item by TMA, then copied into TMEM
+  const __nv_bfloat16* d_o;  // staged once per work item by TMA, then copied into TMEM
   __nv_bfloat16* dq;
   int B, H, S, NT, W, NI;
   int check;             // form of the partial-tile check (kCheck* in mask.cuh)
