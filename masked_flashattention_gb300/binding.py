@@ -334,7 +334,8 @@ def _bwd_shapes(q, others):
 
 
 def cm_attn_bwd_prologue(o, lse, d_o, workspace: torch.Tensor, stream=None) -> None:
-    """Stage 1 of cm_attn_bwd: per-row -D and -LSE * log2(e) into the workspace."""
+    """Per-row -D and -LSE * log2(e) of every row into the workspace, for callers that run
+    cm_attn_bwd_dkdv without cm_attn_bwd_dq (cm_attn_bwd itself does not use it)."""
     B, H, S, d = _bwd_shapes(o, ((d_o, "dO"),))
     nbytes = workspace.numel() * workspace.element_size()
     _check(lib().cm_attn_bwd_prologue(o.data_ptr(), lse.data_ptr(), d_o.data_ptr(),
@@ -344,7 +345,8 @@ def cm_attn_bwd_prologue(o, lse, d_o, workspace: torch.Tensor, stream=None) -> N
 
 def cm_attn_bwd_dkdv(desc: Descriptor, q, k, v, d_o, dk, dv, workspace: torch.Tensor,
                      scale: float | None = None, stream=None) -> None:
-    """Stage 2 of cm_attn_bwd: dK and dV along key tiles (backward descriptor)."""
+    """Second stage of cm_attn_bwd: dK and dV along key tiles (backward descriptor); reads the
+    per-row constants that cm_attn_bwd_dq (or cm_attn_bwd_prologue) wrote into the workspace."""
     B, H, S, d = _bwd_shapes(q, ((k, "k"), (v, "v"), (d_o, "dO"), (dk, "dk"), (dv, "dv")))
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     nbytes = workspace.numel() * workspace.element_size()

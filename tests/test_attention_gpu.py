@@ -266,3 +266,43 @@ def test_maximum_sequence_length_causal():
         if r0 == S - 128:
             _assert_close("dK last keys", dk[0, 0, R].cpu(), rk[R])
             _assert_close("dV last keys", dv[0, 0, R].cpu(), rv[R])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_stages_with_the_standalone_prologue(d):
+    """The dK/dV stage after the standalone prologue (no dQ stage) gives the oracle's dK and dV,
+    and the prologue's per-row constants (-D, -LSE*log2e) agree with the ones the dQ stage
+    writes into its workspace (same values up to the order of the fp32 sums)."""
+    from masked_flashattention_gb300 import specs
+    B = _lib()
+    wid, S = 3, 1024
+    w = W.scaled(W.WORKLOADS[wid], S, B=2, H=2, d=d)
+    seg, nseg = W.segments(wid, w.B, S, seed=41)
+    Q, K, V, dO = W.full_tensors(w, seed=42)
+    f, b = B.cm_compile_spec(specs.FWD[wid]), B.cm_compile_spec(specs.BWD[wid])
+    desc = B.Descriptor(f, b, w.B, S)
+    B.cm_build_descriptor(f, b, torch.from_numpy(seg).cuda(), torch.from_numpy(nseg).cuda(), desc)
+    q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
+    o, lse = B.attention_forward(desc, q, k, v)
+    n = B.cm_attn_bwd_workspace_size(w.B, w.H, S, d)
+    ws_pro = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ws_dq = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+    B.cm_attn_bwd_prologue(o, lse, do, ws_pro)
+    B.cm_attn_bwd_dkdv(desc, q, k, v, do, dk, dv, ws_pro)
+    B.cm_attn_bwd_dq(desc, q, k, v, o, lse, do, dq, ws_dq)
+    torch.cuda.synchronize()
+    assert B.cm_get_status(desc) == 0
+    a, c = ws_pro.view(torch.float32).cpu(), ws_dq.view(torch.float32).cpu()
+    assert torch.equal(torch.isfinite(a), torch.isfinite(c))
+    fin = torch.isfinite(a)
+    assert torch.allclose(a[fin], c[fin], rtol=1e-4, atol=1e-5)
+    dk, dv = dk.cpu(), dv.cpu()
+    for bb in range(w.B):
+        nb = int(nseg[bb])
+        mask = lambda r0, r1, bb=bb, nb=nb: M.dense_mask(wid, seg[bb], nb, S, rows=np.arange(r0, r1))
+        for h in range(w.H):
+            _, rk, rv = A.attention_backward(Q[bb, h], K[bb, h], V[bb, h], dO[bb, h], mask,
+                                             block_rows=2048)
+            _assert_close(f"dK b{bb}h{h}", dk[bb, h], rk)
+            _assert_close(f"dV b{bb}h{h}", dv[bb, h], rv)
