@@ -249,9 +249,10 @@ CM_API int cm_attn_bwd_dq(const cm_descriptor* desc, const void* q, const void* 
 
 /* Limit of every bounded wait inside the attention kernels, for the whole process, in ns
  * (0 restores the default of 2 s; at most 60 s, else CM_ERR_INVALID_ARG).  A wait that reaches it
- * makes its CTA stop: the CTA waits for the copies and MMAs it already issued, writes zeros where
- * it had no result, records CM_ERR_TIMEOUT in the status word (cm_get_status) and exits; the
- * context stays usable.  This is a diagnostic hook: a very small limit makes ordinary waits
+ * makes its CTA stop: the CTA waits for the copies and MMAs it already issued, records
+ * CM_ERR_TIMEOUT in the status word (cm_get_status) and exits, leaving the outputs of the work
+ * items it had not finished unwritten (the call's outputs are then undefined); the context and
+ * the descriptor stay usable.  This is a diagnostic hook: a very small limit makes ordinary waits
  * expire, which tests the time-out path without a fault.  Not synchronised with launches in
  * flight on other host threads.  (The pages describe no failure handling; this is the library's
  * own.) */
